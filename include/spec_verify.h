@@ -1,0 +1,166 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify.so, the verify-and-sample step of
+ * speculative decoding on NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Beschleunigung von Sonar durch Spekulation", Perplexity,
+ * section "Spekulatives Decoding", phases "Akzeptanz" and "Zielgenerierung";
+ * section "Ziel-Entwurf"): after the target model has scored a draft of K
+ * tokens, find the longest prefix of the draft the target accepts, and draw
+ * one extra token from the target at the first mismatch or after the last
+ * draft token, so that at most K + 1 tokens leave one step.  Acceptance
+ * compares the full draft and target distributions; the rule used is that of
+ * the method the page cites ("Fast Inference from Transformers via
+ * Speculative Decoding"):
+ *
+ *   p_i = softmax(target_i / T), q_i = softmax(draft_i / T)      (over V)
+ *   accept draft token x_i  iff  u_i < min(1, p_i(x_i) / q_i(x_i)), in order i = 0..K-1
+ *   j = first rejected position, or K if none
+ *   extra token ~ max(0, p_j - q_j) / W  if j < K,   ~ p_K  if j == K
+ *   (inverse CDF: first v with cumulative weight C_v > u_b * W)
+ *
+ * With T == 0 (greedy): accept iff x_i == argmax target_i (lowest index on
+ * ties) and the extra token is argmax target_j.  The tree variant ("Speculative-
+ * Decoding / Medusa" blog, section 三 Attention Tree) follows, from the root,
+ * the child whose token equals the target's argmax at the current node.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer except `stream` is DEVICE memory owned by the caller; the
+ *     library allocates nothing and keeps no pointer after the call returns.
+ *   - Logits are row-major with the vocabulary contiguous (row stride V
+ *     elements), fp32 or bf16, aligned to their element size.
+ *   - Calls are stream-ordered and asynchronous: they enqueue kernels on
+ *     `stream` (a cudaStream_t; NULL means the legacy default stream) and
+ *     return without synchronising.  Outputs are valid once the stream has
+ *     reached that point.
+ *   - Argument errors are found on the host before anything is enqueued and
+ *     return a status (nothing is written).  A failed launch returns
+ *     SPEC_ERR_CUDA.  Errors that depend on device data are OR-ed as
+ *     SPEC_DEV_* bits into *dev_status (which the caller zeroes); kernels never
+ *     trap and never abort.
+ *   - All arithmetic on the device is fp32 (bf16 inputs are widened exactly);
+ *     cumulative sums for the inverse CDF are carried in fp64 above the level
+ *     of one 16-byte group of logits.
+ *   - Workspace: spec_verify_linear and spec_verify_tree need a caller-owned
+ *     device workspace of spec_workspace_bytes_*() bytes, 16-byte aligned and
+ *     zero-filled before its first use.  Every call leaves it zero-filled
+ *     again, so one zeroing suffices for any number of calls, but one
+ *     workspace must not be shared by calls that may run at the same time.
+ *   - The functions keep no mutable global state apart from a per-thread copy
+ *     of the last error message; they may be called from several host threads.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spec_status {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* a null, misaligned or out-of-range argument */
+    SPEC_ERR_UNSUPPORTED = 2, /* valid, but beyond what this build handles (e.g. V too large) */
+    SPEC_ERR_CUDA = 3,        /* the CUDA runtime reported an error; see spec_last_error() */
+    SPEC_ERR_WORKSPACE = 4    /* workspace missing, too small or misaligned */
+} spec_status;
+
+typedef enum spec_dtype {
+    SPEC_F32 = 0,  /* IEEE binary32 logits */
+    SPEC_BF16 = 1  /* bfloat16 logits (upper half of an IEEE binary32) */
+} spec_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define SPEC_DEV_BAD_TOKEN     1u  /* a draft token outside [0, V): treated as rejected */
+#define SPEC_DEV_NONFINITE     2u  /* a row whose max or exp-sum is not finite; outputs unspecified */
+#define SPEC_DEV_TIMEOUT       4u  /* a bounded wait on a copy gave up; outputs unspecified */
+#define SPEC_DEV_ZERO_RESIDUAL 8u  /* residual weight W == 0 at a rejection: drew from p_j instead */
+#define SPEC_DEV_BAD_TREE     16u  /* parents[] not topological (0 <= parents[c] < c): edge ignored */
+#define SPEC_DEV_BAD_LENGTH   32u  /* spec_sample_bonus: accept_len[b] outside [0, K]; token -1 */
+
+/* Bytes of workspace spec_verify_linear needs for B sequences of K draft tokens. */
+size_t spec_workspace_bytes_linear(int B, int K);
+
+/* Bytes of workspace spec_verify_tree needs for B sequences of N tree nodes. */
+size_t spec_workspace_bytes_tree(int B, int N);
+
+/*
+ * Linear verify and (optionally) the extra token, in one launch.
+ *
+ *   target_logits [B, K+1, V]  row i scores draft token i; row K is the tail.
+ *   draft_logits  [B, K, V]    the draft's logits for the same positions; may be
+ *                              NULL when temperature == 0 (greedy) or K == 0.
+ *   dtype, B >= 0, K >= 0, V >= 1.
+ *   draft_tokens  [B, K] int32 the drafted tokens x_i (may be NULL when K == 0).
+ *   u_accept      [B, K] fp32  uniforms in [0, 1) for the acceptance tests;
+ *                              ignored (may be NULL) when greedy or K == 0.
+ *   u_bonus       [B]    fp32  uniform in [0, 1) for the extra token, or NULL to
+ *                              emit no extra token (spec_sample_bonus can draw it
+ *                              later); ignored when greedy except as the switch.
+ *   temperature   T >= 0, finite; T == 0 selects greedy mode.
+ * Outputs (device, caller-owned):
+ *   accept_len    [B]      j = number of accepted draft tokens, 0 <= j <= K.
+ *   out_tokens    [B, K+1] x_0..x_{j-1}, then the extra token (if u_bonus), then -1.
+ *                          Required when u_bonus != NULL, else may be NULL.
+ *   num_emitted   [B]      j + 1 with an extra token, j without.
+ *   probs_out     [B, K, 3] or NULL: p_i(x_i), q_i(x_i), min(1, p_i/q_i) for every
+ *                          position (computed for all K, not only up to j); sampling only.
+ *   dev_status    [1]      SPEC_DEV_* bits OR-ed in.
+ *   workspace, workspace_bytes: see the conventions above.
+ */
+spec_status spec_verify_linear(const void *target_logits, const void *draft_logits,
+                               spec_dtype dtype, int B, int K, int V,
+                               const int32_t *draft_tokens, const float *u_accept,
+                               const float *u_bonus, float temperature,
+                               int32_t *accept_len, int32_t *out_tokens, int32_t *num_emitted,
+                               float *probs_out, uint32_t *dev_status,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The extra token alone, for callers that already hold accept_len: draws from
+ * max(0, p_j - q_j) / W at j = accept_len[b] < K, or from p_K when j == K
+ * (argmax of target row j when temperature == 0).  Same layouts as above.
+ *   accept_len  [B] int32 (device, input); u_bonus [B] (ignored when greedy).
+ *   bonus_token [B] int32 (device, output); -1 where accept_len[b] is out of
+ *               range (and SPEC_DEV_BAD_LENGTH is set).
+ * Needs no workspace.
+ */
+spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits,
+                              spec_dtype dtype, int B, int K, int V,
+                              const int32_t *accept_len, const float *u_bonus, float temperature,
+                              int32_t *bonus_token, uint32_t *dev_status, void *stream);
+
+/*
+ * Greedy verify of a candidate tree ("Speculative-Decoding / Medusa" blog,
+ * section 三): at the current node take argmax of its target row; move to the
+ * lowest-index child whose token equals it; stop when none does or max_depth
+ * nodes were accepted; the extra token is argmax at the last accepted node.
+ *
+ *   target_logits [B, N, V]  row n holds the target logits after node n;
+ *                            node 0 is the root (the last accepted token).
+ *   parents       [N] int32  parents[0] ignored; 0 <= parents[c] < c for c >= 1.
+ *   node_tokens   [B, N]     candidate token of each node (column 0 ignored).
+ *   max_depth >= 0, N >= 1, V >= 1.
+ * Outputs (max_depth + 1 columns, -1 padded):
+ *   path_nodes [B, max_depth+1]  0, n_1, n_2, ... (node ids of the accepted path)
+ *   path_len   [B]               number of accepted non-root nodes
+ *   out_tokens [B, max_depth+1]  tokens of n_1..n_len, then the extra token
+ */
+spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B, int N, int V,
+                             const int32_t *parents, const int32_t *node_tokens, int max_depth,
+                             int32_t *path_nodes, int32_t *path_len, int32_t *out_tokens,
+                             uint32_t *dev_status, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/* Static text for a status code. */
+const char *spec_status_string(spec_status status);
+
+/* Detail of the last error returned on the calling host thread ("" if none). */
+const char *spec_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,166 @@
+"""CPU oracle for the speculative-decoding verify-and-sample step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library: the arithmetic lives in ``spec_oracle.c`` (plain C,
+float64, one sequential loop per row), compiled here with gcc, and this module
+only marshals numpy arrays into it.
+
+The functions follow "Beschleunigung von Sonar durch Spekulation" (Perplexity),
+sections "Spekulatives Decoding" and "Ziel-Entwurf", with the acceptance rule of
+the method that page cites ("Fast Inference from Transformers via Speculative
+Decoding"), and section 三 (Attention Tree) of the "Speculative-Decoding /
+Medusa" blog for the tree walk.  The header of ``spec_oracle.c`` lists every
+reading taken where the pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+F32 = 0
+BF16 = 1
+FLAG_ZERO_RESIDUAL = 1
+FLAG_BAD_TOKEN = 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc (OpenMP over sequences) and return the .so path."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-Wall",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib):
+    P = ctypes.c_void_p
+    i32 = ctypes.c_int
+    lib.oracle_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, ctypes.c_float,
+                                         P, P, P, P, P, P]
+    lib.oracle_verify_linear.restype = i32
+    lib.oracle_sample_bonus.argtypes = [P, P, i32, i32, i32, i32, P, P, ctypes.c_float,
+                                        P, P, P]
+    lib.oracle_sample_bonus.restype = i32
+    lib.oracle_verify_tree.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, P, P]
+    lib.oracle_verify_tree.restype = i32
+    lib.oracle_threads.argtypes = [i32]
+    lib.oracle_threads.restype = i32
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library.  A path loads that build."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def threads(n: int = 0, lib=None) -> int:
+    """Set (n > 0) and return the number of OpenMP threads the oracle uses."""
+    return (lib or load()).oracle_threads(int(n))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a):
+    """numpy float32 -> (array, F32); numpy uint16 holding bf16 bits -> (array, BF16)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype == np.uint16:
+        return a, BF16
+    raise TypeError("oracle logits must be float32 or uint16 (bf16 bits), got %s" % a.dtype)
+
+
+def verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperature, lib=None):
+    """Linear verify.  target [B, K+1, V], draft [B, K, V] (None allowed when
+    temperature == 0), draft_tokens [B, K] int32, u_accept [B, K] float32,
+    u_bonus [B] float32 or None.  Returns a dict of numpy arrays."""
+    lib = lib or load()
+    target, dt = _logits(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    if draft is not None:
+        draft, dd = _logits(draft)
+        assert dd == dt and draft.shape == (B, K, V)
+    tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
+    ua = None if u_accept is None else np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, K)
+    ub = None if u_bonus is None else np.ascontiguousarray(u_bonus, dtype=np.float32).reshape(B)
+    out = dict(
+        accept_len=np.zeros(B, np.int32),
+        out_tokens=np.zeros((B, K + 1), np.int32),
+        num_emitted=np.zeros(B, np.int32),
+        probs=np.zeros((B, K, 3), np.float64),
+        bonus_cdf=np.zeros((B, 2), np.float64),
+        flags=np.zeros(B, np.uint32),
+    )
+    rc = lib.oracle_verify_linear(
+        _ptr(target), _ptr(draft), dt, B, K, V, _ptr(tokens), _ptr(ua), _ptr(ub),
+        ctypes.c_float(temperature), _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+        _ptr(out["num_emitted"]), _ptr(out["probs"]), _ptr(out["bonus_cdf"]), _ptr(out["flags"]))
+    if rc != 0:
+        raise ValueError("oracle_verify_linear rejected its arguments")
+    return out
+
+
+def sample_bonus(target, draft, accept_len, u_bonus, temperature, lib=None):
+    """The extra token alone at row accept_len[b] of each sequence."""
+    lib = lib or load()
+    target, dt = _logits(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    if draft is not None:
+        draft, dd = _logits(draft)
+        assert dd == dt and draft.shape == (B, K, V)
+    al = np.ascontiguousarray(accept_len, dtype=np.int32).reshape(B)
+    ub = None if u_bonus is None else np.ascontiguousarray(u_bonus, dtype=np.float32).reshape(B)
+    out = dict(bonus_token=np.zeros(B, np.int32), bonus_cdf=np.zeros((B, 2), np.float64),
+               flags=np.zeros(B, np.uint32))
+    rc = lib.oracle_sample_bonus(_ptr(target), _ptr(draft), dt, B, K, V, _ptr(al), _ptr(ub),
+                                 ctypes.c_float(temperature), _ptr(out["bonus_token"]),
+                                 _ptr(out["bonus_cdf"]), _ptr(out["flags"]))
+    if rc != 0:
+        raise ValueError("oracle_sample_bonus rejected its arguments")
+    return out
+
+
+def verify_tree(target, parents, node_tokens, max_depth, lib=None):
+    """Greedy tree verify.  target [B, N, V], parents [N], node_tokens [B, N]."""
+    lib = lib or load()
+    target, dt = _logits(target)
+    B, N, V = target.shape
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(N)
+    tok = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
+    out = dict(path_nodes=np.zeros((B, max_depth + 1), np.int32),
+               path_len=np.zeros(B, np.int32),
+               out_tokens=np.zeros((B, max_depth + 1), np.int32))
+    rc = lib.oracle_verify_tree(_ptr(target), dt, B, N, V, _ptr(par), _ptr(tok), int(max_depth),
+                                _ptr(out["path_nodes"]), _ptr(out["path_len"]),
+                                _ptr(out["out_tokens"]))
+    if rc != 0:
+        raise ValueError("oracle_verify_tree rejected its arguments")
+    return out

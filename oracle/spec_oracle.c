@@ -1,0 +1,339 @@
+/*
+ * spec_oracle.c -- CPU oracle for the speculative-decoding verify-and-sample step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header or constant with the CUDA
+ * library; it has its own bf16 decoder and its own definitions of every step.
+ *
+ * What it computes, and where each step comes from:
+ *
+ *   "Beschleunigung von Sonar durch Spekulation" (Perplexity blog,
+ *   English title "Accelerating Sonar through speculation"):
+ *     - section "Spekulatives Decoding": a draft of n tokens is checked by the
+ *       target, the longest acceptable prefix is kept, and the target gives
+ *       one more token for free, so at most n + 1 tokens leave one step;
+ *       phase "Akzeptanz" finds the length of the longest acceptable prefix,
+ *       phase "Zielgenerierung" samples the target logits at the first
+ *       mismatch, or at the end of the draft, for the extra token.
+ *     - section "Ziel-Entwurf": acceptance compares the full draft and target
+ *       probability distributions; the method cited for it in the page's
+ *       reference list is "Fast Inference from Transformers via Speculative
+ *       Decoding" (standard speculative sampling).
+ *   "Speculative-Decoding / Medusa" blog, section 三 (Attention Tree): the
+ *     target's choice (greedy or sampled) at a node is looked up among that
+ *     node's candidate children, and verification continues along the child
+ *     that matches, until no child matches.
+ *
+ * Readings taken where the pages are silent (all restated in the design doc):
+ *   - accept draft token x_i iff u_i < min(1, p_i(x_i) / q_i(x_i)) (strict),
+ *     with p_i = softmax(target_i / T) and q_i = softmax(draft_i / T);
+ *     q_i(x_i) == 0 gives ratio +inf when p_i(x_i) > 0 and 0 otherwise;
+ *   - at the first rejection j < K the extra token is drawn from the
+ *     normalised residual max(0, p_j - q_j); if every draft token was
+ *     accepted it is drawn from p_K;
+ *   - inverse CDF: the first v whose inclusive cumulative weight C_v exceeds
+ *     u_b * W; if rounding leaves none, the last v with nonzero weight;
+ *     if W == 0 (possible only through rounding), fall back to p_j and flag;
+ *   - greedy mode (T == 0): accept iff x_i == argmax target_i (lowest index on
+ *     ties); the extra token is argmax target_j;
+ *   - tree: among the children of the current node (increasing node index),
+ *     take the first whose token equals argmax of the current node's target
+ *     row; stop when none matches or max_depth nodes were accepted; the extra
+ *     token is argmax at the last accepted node.
+ *
+ * Precision: every logit is widened to double (fp32 directly; bf16 by placing
+ * its 16 bits in the high half of an IEEE single), and all arithmetic is
+ * double, summed sequentially in vocabulary order.  The temperature is taken
+ * as the same single-precision value the GPU path receives, widened.
+ *
+ * Parallelism: sequences are independent problems; an OpenMP loop over them
+ * changes no arithmetic inside a sequence.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* flag bits returned per sequence */
+#define ORACLE_FLAG_ZERO_RESIDUAL 1u /* W == 0 at the first rejection: fell back to p_j */
+#define ORACLE_FLAG_BAD_TOKEN 2u     /* a draft token outside [0, V) */
+
+/* One logit, widened to double.  bf16 is the upper half of an IEEE single. */
+static double logit_at(const void *base, int dtype, size_t idx) {
+    if (dtype == ORACLE_F32) return (double)((const float *)base)[idx];
+    uint16_t h = ((const uint16_t *)base)[idx];
+    uint32_t w = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* p[v] = exp((l_v - max l) / T) / sum_v' exp((l_v' - max l) / T), sequential sums. */
+static void softmax_row(const void *logits, int dtype, size_t row, int V, double T, double *p) {
+    size_t off = row * (size_t)V;
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double l = logit_at(logits, dtype, off + v);
+        if (l > m) m = l;
+    }
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+        p[v] = exp((logit_at(logits, dtype, off + v) - m) / T);
+        S += p[v];
+    }
+    for (int v = 0; v < V; ++v) p[v] /= S;
+}
+
+/* Lowest index of the maximum logit of one row. */
+static int argmax_row(const void *logits, int dtype, size_t row, int V) {
+    size_t off = row * (size_t)V;
+    int best = 0;
+    double bv = logit_at(logits, dtype, off);
+    for (int v = 1; v < V; ++v) {
+        double l = logit_at(logits, dtype, off + v);
+        if (l > bv) { bv = l; best = v; }
+    }
+    return best;
+}
+
+/* Inverse-CDF draw from nonnegative weights w[0..V).  Returns the token and
+ * writes the cumulative interval [lo, hi) of the chosen token, normalised by W. */
+static int inverse_cdf(const double *w, int V, double u, double *lo, double *hi) {
+    double W = 0.0;
+    for (int v = 0; v < V; ++v) W += w[v];
+    double target = u * W;
+    double C = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double Cprev = C;
+        C += w[v];
+        if (C > target) {
+            *lo = Cprev / W;
+            *hi = C / W;
+            return v;
+        }
+    }
+    /* rounding left no index: the last token with nonzero weight */
+    int last = -1;
+    for (int v = 0; v < V; ++v)
+        if (w[v] > 0.0) last = v;
+    if (last < 0) { *lo = *hi = 0.0; return 0; }
+    double Cl = 0.0;
+    for (int v = 0; v < last; ++v) Cl += w[v];
+    *lo = Cl / W;
+    *hi = (Cl + w[last]) / W;
+    return last;
+}
+
+/* The extra token at row j of sequence b (sampling mode): residual
+ * max(0, p_j - q_j) if j < K, else p_K.  Returns the token; lo/hi as above. */
+static int extra_token_sampled(const void *target, const void *draft, int dtype, int b, int K, int V,
+                               int j, double T, double u, double *w, double *pj, double *qj,
+                               double *lo, double *hi, uint32_t *flag) {
+    softmax_row(target, dtype, (size_t)b * (K + 1) + j, V, T, pj);
+    if (j < K) {
+        softmax_row(draft, dtype, (size_t)b * K + j, V, T, qj);
+        double W = 0.0;
+        for (int v = 0; v < V; ++v) {
+            double d = pj[v] - qj[v];
+            w[v] = d > 0.0 ? d : 0.0;
+            W += w[v];
+        }
+        if (W > 0.0) return inverse_cdf(w, V, u, lo, hi);
+        *flag |= ORACLE_FLAG_ZERO_RESIDUAL;
+    }
+    return inverse_cdf(pj, V, u, lo, hi);
+}
+
+/*
+ * Linear verify of B sequences with K draft tokens each.
+ *   target [B, K+1, V], draft [B, K, V] (ignored when T == 0), row-major.
+ *   draft_tokens [B, K]; u_accept [B, K]; u_bonus [B] or NULL (no extra token).
+ * Outputs: accept_len [B]; out_tokens [B, K+1] (accepted draft tokens, then the
+ * extra token, then -1); num_emitted [B]; probs [B, K, 3] = (p_i(x_i),
+ * q_i(x_i), min(1, ratio)) for every position, or NULL; bonus_cdf [B, 2] = the
+ * chosen token's normalised cumulative interval, or NULL; flags [B] or NULL.
+ */
+int oracle_verify_linear(const void *target, const void *draft, int dtype, int B, int K, int V,
+                         const int32_t *draft_tokens, const float *u_accept, const float *u_bonus,
+                         float temperature, int32_t *accept_len, int32_t *out_tokens,
+                         int32_t *num_emitted, double *probs, double *bonus_cdf, uint32_t *flags) {
+    if (B < 0 || K < 0 || V < 1) return 1;
+    const double T = (double)temperature;
+    const int greedy = (temperature == 0.0f);
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            uint32_t flag = 0;
+            int j = K;
+            if (greedy) {
+                for (int i = 0; i < K; ++i) {
+                    int x = draft_tokens[(size_t)b * K + i];
+                    int am = argmax_row(target, dtype, (size_t)b * (K + 1) + i, V);
+                    if (x < 0 || x >= V) flag |= ORACLE_FLAG_BAD_TOKEN;
+                    if (x != am) { j = i; break; }
+                }
+            } else {
+                int decided = 0;
+                for (int i = 0; i < K; ++i) {
+                    int x = draft_tokens[(size_t)b * K + i];
+                    double px = 0.0, qx = 0.0, thr = 0.0;
+                    if (x >= 0 && x < V) {
+                        softmax_row(target, dtype, (size_t)b * (K + 1) + i, V, T, p);
+                        softmax_row(draft, dtype, (size_t)b * K + i, V, T, q);
+                        px = p[x];
+                        qx = q[x];
+                        double ratio = qx > 0.0 ? px / qx : (px > 0.0 ? INFINITY : 0.0);
+                        thr = ratio < 1.0 ? ratio : 1.0;
+                    } else {
+                        flag |= ORACLE_FLAG_BAD_TOKEN;
+                    }
+                    if (probs) {
+                        probs[((size_t)b * K + i) * 3 + 0] = px;
+                        probs[((size_t)b * K + i) * 3 + 1] = qx;
+                        probs[((size_t)b * K + i) * 3 + 2] = thr;
+                    }
+                    /* positions are tested in order; the first failure ends the prefix */
+                    if (!decided && !((double)u_accept[(size_t)b * K + i] < thr)) {
+                        j = i;
+                        decided = 1;
+                        if (!probs) break;
+                    }
+                }
+            }
+            accept_len[b] = j;
+            int32_t *row_out = out_tokens ? out_tokens + (size_t)b * (K + 1) : NULL;
+            if (row_out) {
+                for (int i = 0; i <= K; ++i) row_out[i] = -1;
+                for (int i = 0; i < j; ++i) row_out[i] = draft_tokens[(size_t)b * K + i];
+            }
+            if (u_bonus) {
+                int tok;
+                double lo = 0.0, hi = 0.0;
+                if (greedy) {
+                    tok = argmax_row(target, dtype, (size_t)b * (K + 1) + j, V);
+                } else {
+                    tok = extra_token_sampled(target, draft, dtype, b, K, V, j, T, (double)u_bonus[b],
+                                              w, p, q, &lo, &hi, &flag);
+                }
+                if (row_out) row_out[j] = tok;
+                if (bonus_cdf) {
+                    bonus_cdf[(size_t)b * 2 + 0] = lo;
+                    bonus_cdf[(size_t)b * 2 + 1] = hi;
+                }
+                num_emitted[b] = j + 1;
+            } else {
+                num_emitted[b] = j;
+            }
+            if (flags) flags[b] = flag;
+        }
+        free(p);
+        free(q);
+        free(w);
+    }
+    return 0;
+}
+
+/*
+ * The extra token alone, for a caller that already holds accept_len:
+ * residual at row j = accept_len[b] if j < K, else p_K; argmax of target row
+ * j when T == 0.  bonus_cdf [B, 2] and flags [B] may be NULL.
+ */
+int oracle_sample_bonus(const void *target, const void *draft, int dtype, int B, int K, int V,
+                        const int32_t *accept_len, const float *u_bonus, float temperature,
+                        int32_t *bonus_token, double *bonus_cdf, uint32_t *flags) {
+    if (B < 0 || K < 0 || V < 1) return 1;
+    const double T = (double)temperature;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 1)
+        for (int b = 0; b < B; ++b) {
+            uint32_t flag = 0;
+            int j = accept_len[b];
+            double lo = 0.0, hi = 0.0;
+            if (j < 0 || j > K) {
+                bonus_token[b] = -1;
+            } else if (temperature == 0.0f) {
+                bonus_token[b] = argmax_row(target, dtype, (size_t)b * (K + 1) + j, V);
+            } else {
+                bonus_token[b] = extra_token_sampled(target, draft, dtype, b, K, V, j, T,
+                                                     (double)u_bonus[b], w, p, q, &lo, &hi, &flag);
+            }
+            if (bonus_cdf) {
+                bonus_cdf[(size_t)b * 2 + 0] = lo;
+                bonus_cdf[(size_t)b * 2 + 1] = hi;
+            }
+            if (flags) flags[b] = flag;
+        }
+        free(p);
+        free(q);
+        free(w);
+    }
+    return 0;
+}
+
+/*
+ * Greedy tree verify ("Speculative-Decoding / Medusa", section 三).
+ *   target [B, N, V]: row n holds the target logits after node n (node 0 is
+ *   the root, i.e. the last token already accepted).
+ *   parents [N]: parents[0] = -1, 0 <= parents[c] < c otherwise.
+ *   node_tokens [B, N]: the candidate token of each node (column 0 unused).
+ * Outputs (max_depth + 1 columns, -1 padded): path_nodes = 0, n1, n2, ...;
+ * path_len = number of accepted non-root nodes; out_tokens = accepted node
+ * tokens followed by the extra token argmax(target row of the last node).
+ */
+int oracle_verify_tree(const void *target, int dtype, int B, int N, int V, const int32_t *parents,
+                       const int32_t *node_tokens, int max_depth, int32_t *path_nodes,
+                       int32_t *path_len, int32_t *out_tokens) {
+    if (B < 0 || N < 1 || V < 1 || max_depth < 0) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        int32_t *pn = path_nodes + (size_t)b * (max_depth + 1);
+        int32_t *ot = out_tokens + (size_t)b * (max_depth + 1);
+        for (int d = 0; d <= max_depth; ++d) pn[d] = ot[d] = -1;
+        int cur = 0, depth = 0;
+        pn[0] = 0;
+        while (depth < max_depth) {
+            int want = argmax_row(target, dtype, (size_t)b * N + cur, V);
+            int next = -1;
+            for (int c = 1; c < N; ++c) {
+                if (parents[c] == cur && node_tokens[(size_t)b * N + c] == want) {
+                    next = c;
+                    break;
+                }
+            }
+            if (next < 0) break;
+            ot[depth] = node_tokens[(size_t)b * N + next];
+            ++depth;
+            pn[depth] = next;
+            cur = next;
+        }
+        path_len[b] = depth;
+        ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);
+    }
+    return 0;
+}
+
+/* Number of OpenMP threads the oracle runs with; n > 0 sets it first. */
+int oracle_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}

@@ -1,0 +1,110 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle's C source (a
+flipped sign, a transposed ratio, a dropped temperature, a wrong row index, a
+non-strict comparison, a wrong bf16 shift, ...), compiles it on the CPU and
+runs the pins that should notice: every mutant must fail at least one of them.
+The committed oracle is never modified.
+"""
+import os
+import shutil
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+import test_tree_pins as tpins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
+
+# (name, text in the source, replacement)
+MUTANTS = [
+    ("residual_sign", "double d = pj[v] - qj[v];", "double d = qj[v] - pj[v];"),
+    ("residual_unclamped", "w[v] = d > 0.0 ? d : 0.0;", "w[v] = d;"),
+    ("ratio_transposed", "double ratio = qx > 0.0 ? px / qx", "double ratio = qx > 0.0 ? qx / px"),
+    ("draft_temperature_dropped", "softmax_row(draft, dtype, (size_t)b * K + i, V, T, q);",
+     "softmax_row(draft, dtype, (size_t)b * K + i, V, 1.0, q);"),
+    ("target_row_off_by_one", "softmax_row(target, dtype, (size_t)b * (K + 1) + i, V, T, p);",
+     "softmax_row(target, dtype, (size_t)b * (K + 1) + i + 1, V, T, p);"),
+    ("tail_from_row_zero", "softmax_row(target, dtype, (size_t)b * (K + 1) + j, V, T, pj);",
+     "softmax_row(target, dtype, (size_t)b * (K + 1) + (j < K ? j : 0), V, T, pj);"),
+    ("last_rejection_not_first", "j = i;\n                        decided = 1;", "j = i;"),
+    ("inverse_cdf_not_strict", "if (C > target) {", "if (C >= target) {"),
+    ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
+    ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
+    ("tree_extra_token_at_root", "ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);",
+     "ot[depth] = argmax_row(target, dtype, (size_t)b * N + 0, V);"),
+    ("tree_any_child", "if (parents[c] == cur && node_tokens", "if (parents[c] >= 0 && node_tokens"),
+]
+
+
+def _pin_suite(lib):
+    """Run the pins against `lib`; return the names of those that failed."""
+    failed = []
+    checks = [
+        ("distribution", lambda: pins.check_distribution_preserved(lib, 4, 2, 0.8, 9)),
+        ("distribution_k1", lambda: pins.check_distribution_preserved(lib, 5, 1, 1.0, 10)),
+        ("hand_example", lambda: pins.test_hand_worked_three_token_example(lib)),
+        ("greedy_argmax", lambda: pins.test_greedy_equals_argmax_decoding(lib)),
+        ("invariants", lambda: pins.test_invariants_random(lib, "f32")),
+        ("zero_weight", lambda: pins.test_residual_zero_weight_token_never_drawn(lib)),
+        ("bf16", lambda: pins.test_bf16_decoding_equals_fp32_values(lib)),
+        ("spike", lambda: pins.test_spiked_constant_row_closed_form(lib, 1000, 5.0, 1.0)),
+        ("tree", lambda: _tree_check(lib)),
+    ]
+    for name, fn in checks:
+        try:
+            fn()
+        except AssertionError:
+            failed.append(name)
+    return failed
+
+
+def _tree_check(lib):
+    rng = np.random.default_rng(5)
+    B, V, N = 40, 10, 12
+    parents = tpins._random_tree(rng, N)
+    target = rng.standard_normal((B, N, V)).astype(np.float32)
+    am = target.argmax(-1)
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for n in range(N):
+            ch = [c for c in range(N) if parents[c] == n]
+            pool = list(rng.permutation(V))
+            if ch and rng.random() < 0.8:
+                pool.remove(am[b, n])
+                pool.insert(0, am[b, n])
+            for c, t in zip(ch, pool):
+                tokens[b, c] = t
+    r = oracle.verify_tree(target, parents, tokens, 5, lib=lib)
+    for b in range(B):
+        path, bonus = tpins._brute_force_walk(target[b], parents, tokens[b], 5)
+        assert r["path_len"][b] == len(path) - 1
+        assert r["out_tokens"][b, len(path) - 1] == bonus
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="oracle_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+def test_unmutated_oracle_passes_suite(oracle_lib):
+    assert _pin_suite(oracle_lib) == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(workdir, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation anchor must occur exactly once: %r" % old
+    path = os.path.join(workdir, name + ".c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(workdir, name + ".so")
+    oracle.build(force=True, src=path, out=so)
+    lib = oracle.load(so)
+    failed = _pin_suite(lib)
+    assert failed, "planted mistake %r passed every pin" % name
