@@ -1,0 +1,245 @@
+"""Speculative-decoding verify-and-sample step for NVIDIA GB300 (sm_103a).
+
+Python binding of ``libspecverify.so`` (C ABI in ``include/spec_verify.h``).
+This module only marshals arguments: it allocates outputs and the workspace
+with PyTorch, passes raw device pointers and the current CUDA stream, and
+raises ``SpecError`` on a non-OK status.  Every step of the computation runs in
+the library's CUDA kernels; there is no fallback, and importing the functions
+fails loudly when the library has not been built.
+
+Entry points (same names as the C ABI):
+  spec_verify_linear   accept/reject K draft tokens per sequence and draw the
+                       extra token ("Beschleunigung von Sonar durch Spekulation",
+                       sections "Spekulatives Decoding" and "Ziel-Entwurf")
+  spec_sample_bonus    the extra token alone, given accept_len
+  spec_verify_tree     greedy walk of a Medusa candidate tree
+                       ("Speculative-Decoding / Medusa", section 三)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_UNSUPPORTED = 2
+SPEC_ERR_CUDA = 3
+SPEC_ERR_WORKSPACE = 4
+
+SPEC_F32 = 0
+SPEC_BF16 = 1
+
+DEV_BAD_TOKEN = 1
+DEV_NONFINITE = 2
+DEV_TIMEOUT = 4
+DEV_ZERO_RESIDUAL = 8
+DEV_BAD_TREE = 16
+DEV_BAD_LENGTH = 32
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__("%s (%s)" % (detail, _status_name(status)))
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library():
+    """Load libspecverify.so; raises ImportError if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libspecverify.so is not built (run __graft_entry__.build() or "
+                              "python -m sampling_online_softmax_gb300.build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        lib.spec_workspace_bytes_linear.argtypes = [i32, i32]
+        lib.spec_workspace_bytes_linear.restype = u64
+        lib.spec_workspace_bytes_tree.argtypes = [i32, i32]
+        lib.spec_workspace_bytes_tree.restype = u64
+        lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
+        lib.spec_verify_linear.restype = i32
+        lib.spec_sample_bonus.argtypes = [P, P, i32, i32, i32, i32, P, P, f32, P, P, P]
+        lib.spec_sample_bonus.restype = i32
+        lib.spec_verify_tree.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, u64, P]
+        lib.spec_verify_tree.restype = i32
+        lib.spec_status_string.argtypes = [i32]
+        lib.spec_status_string.restype = ctypes.c_char_p
+        lib.spec_last_error.argtypes = []
+        lib.spec_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load_library().spec_status_string(int(status)).decode()
+    except ImportError:
+        return "status %d" % status
+
+
+def _check(status: int):
+    if status != SPEC_OK:
+        raise SpecError(status, load_library().spec_last_error().decode() or "call failed")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError("logits must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _cuda(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def _stream_handle(device, stream):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream), s
+
+
+# one zero-filled workspace per (device, stream), grown on demand; every call
+# leaves it zero-filled again, so it is cleared only when allocated
+_ws_cache = {}
+_ws_lock = threading.Lock()
+
+
+def _workspace(device, stream, nbytes):
+    key = (device.index, stream.cuda_stream)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            with torch.cuda.stream(stream):
+                ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+        return ws
+
+
+def spec_workspace_bytes_linear(B: int, K: int) -> int:
+    return int(load_library().spec_workspace_bytes_linear(int(B), int(K)))
+
+
+def spec_workspace_bytes_tree(B: int, N: int) -> int:
+    return int(load_library().spec_workspace_bytes_tree(int(B), int(N)))
+
+
+def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperature, *,
+                       probs: bool = False, status=None, out=None, workspace=None, stream=None):
+    """Verify K draft tokens per sequence; returns a dict of device tensors.
+
+    target [B, K+1, V] and draft [B, K, V] (float32 or bfloat16; draft may be
+    None in greedy mode), draft_tokens [B, K] int32, u_accept [B, K] float32,
+    u_bonus [B] float32 or None (no extra token), temperature >= 0 (0: greedy).
+    Result: accept_len [B], out_tokens [B, K+1], num_emitted [B], status [1]
+    (SPEC_DEV_* bits, int32), and probs [B, K, 3] when requested.
+    """
+    lib = load_library()
+    _cuda(target, "target")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    _cuda(draft, "draft")
+    _cuda(draft_tokens, "draft_tokens", torch.int32)
+    _cuda(u_accept, "u_accept", torch.float32)
+    _cuda(u_bonus, "u_bonus", torch.float32)
+    if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
+        raise ValueError("draft must match target's dtype with shape [B, K, V]")
+    if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
+        raise ValueError("draft_tokens must be [B, K]")
+    h, s = _stream_handle(dev, stream)
+    if out is None:
+        out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                   num_emitted=torch.empty(B, dtype=torch.int32, device=dev))
+        if probs:
+            out["probs"] = torch.empty((B, K, 3), dtype=torch.float32, device=dev)
+    if status is None:
+        with torch.cuda.stream(s):
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out["status"] = status
+    nbytes = spec_workspace_bytes_linear(B, K)
+    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_linear(
+            _ptr(target), _ptr(draft), _dtype_code(target), B, K, V, _ptr(draft_tokens), _ptr(u_accept),
+            _ptr(u_bonus), float(temperature), _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+            _ptr(out["num_emitted"]), _ptr(out.get("probs")), _ptr(status), _ptr(ws), ws.numel(), h)
+    _check(st)
+    return out
+
+
+def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status=None, out=None, stream=None):
+    """The extra token alone at row accept_len[b]; returns dict(bonus_token [B], status [1])."""
+    lib = load_library()
+    _cuda(target, "target")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    _cuda(draft, "draft")
+    _cuda(accept_len, "accept_len", torch.int32)
+    _cuda(u_bonus, "u_bonus", torch.float32)
+    h, s = _stream_handle(dev, stream)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=dev)
+    if status is None:
+        with torch.cuda.stream(s):
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.spec_sample_bonus(_ptr(target), _ptr(draft), _dtype_code(target), B, K, V, _ptr(accept_len),
+                                   _ptr(u_bonus), float(temperature), _ptr(out), _ptr(status), h)
+    _check(st)
+    return dict(bonus_token=out, status=status)
+
+
+def spec_verify_tree(target, parents, node_tokens, max_depth, *, status=None, out=None, workspace=None,
+                     stream=None):
+    """Greedy tree walk; returns dict(path_nodes, path_len, out_tokens, status)."""
+    lib = load_library()
+    _cuda(target, "target")
+    B, N, V = target.shape
+    dev = target.device
+    _cuda(parents, "parents", torch.int32)
+    _cuda(node_tokens, "node_tokens", torch.int32)
+    h, s = _stream_handle(dev, stream)
+    D = int(max_depth)
+    if out is None:
+        out = dict(path_nodes=torch.empty((B, D + 1), dtype=torch.int32, device=dev),
+                   path_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, D + 1), dtype=torch.int32, device=dev))
+    if status is None:
+        with torch.cuda.stream(s):
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out["status"] = status
+    nbytes = spec_workspace_bytes_tree(B, N)
+    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_tree(_ptr(target), _dtype_code(target), B, N, V, _ptr(parents), _ptr(node_tokens), D,
+                                  _ptr(out["path_nodes"]), _ptr(out["path_len"]), _ptr(out["out_tokens"]),
+                                  _ptr(status), _ptr(ws), ws.numel(), h)
+    _check(st)
+    return out

@@ -1,0 +1,121 @@
+"""The C ABI library builds, loads and exports every declared symbol; host-side
+argument checks return their documented status without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sampling_online_softmax_gb300 as sv
+from sampling_online_softmax_gb300 import build as sv_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sv_build.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("spec_verify_linear", "spec_sample_bonus", "spec_verify_tree", "spec_status_string",
+              "spec_last_error", "spec_workspace_bytes_linear", "spec_workspace_bytes_tree"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(sv.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.spec_status_string(code).decode()
+        assert s.startswith("SPEC_")
+    assert "unknown" in lib.spec_status_string(99).decode()
+
+
+def test_workspace_sizes(lib):
+    assert sv.spec_workspace_bytes_linear(0, 4) == 0
+    a = sv.spec_workspace_bytes_linear(64, 4)
+    assert a >= 64 * 4 + 64 * 4 * 4 + 64 * 5 * 4 and a % 16 == 0
+    assert sv.spec_workspace_bytes_linear(128, 4) > a
+    t = sv.spec_workspace_bytes_tree(16, 64)
+    assert t >= 16 * 4 + 16 * 64 * 4
+    assert sv.spec_workspace_bytes_tree(16, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every case below fails on the host
+
+
+def _linear(lib, **kw):
+    args = dict(target=FAKE, draft=FAKE, dtype=1, B=2, K=3, V=100, tokens=FAKE, u=FAKE, ub=FAKE, T=1.0,
+                al=FAKE, ot=FAKE, ne=FAKE, probs=None, st=FAKE, ws=FAKE, wsb=1 << 20, stream=None)
+    args.update(kw)
+    return lib.spec_verify_linear(args["target"], args["draft"], args["dtype"], args["B"], args["K"], args["V"],
+                                  args["tokens"], args["u"], args["ub"], args["T"], args["al"], args["ot"],
+                                  args["ne"], args["probs"], args["st"], args["ws"], args["wsb"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=7), sv.SPEC_ERR_INVALID_ARG),
+    (dict(B=-1), sv.SPEC_ERR_INVALID_ARG),
+    (dict(K=-1), sv.SPEC_ERR_INVALID_ARG),
+    (dict(V=0), sv.SPEC_ERR_INVALID_ARG),
+    (dict(T=float("nan")), sv.SPEC_ERR_INVALID_ARG),
+    (dict(T=-0.5), sv.SPEC_ERR_INVALID_ARG),
+    (dict(T=float("inf")), sv.SPEC_ERR_INVALID_ARG),
+    (dict(T=1e-45), sv.SPEC_ERR_INVALID_ARG),          # log2(e)/T overflows float
+    (dict(target=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(target=ctypes.c_void_p(0x10001)), sv.SPEC_ERR_INVALID_ARG),  # misaligned bf16
+    (dict(draft=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(u=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(tokens=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(al=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(st=None), sv.SPEC_ERR_INVALID_ARG),
+    (dict(ot=None), sv.SPEC_ERR_INVALID_ARG),            # required with u_bonus
+    (dict(ws=None), sv.SPEC_ERR_WORKSPACE),
+    (dict(wsb=16), sv.SPEC_ERR_WORKSPACE),
+    (dict(ws=ctypes.c_void_p(0x10008)), sv.SPEC_ERR_WORKSPACE),
+    (dict(B=0), sv.SPEC_OK),                             # empty batch: nothing to do
+])
+def test_linear_host_validation(lib, kw, expect):
+    assert _linear(lib, **kw) == expect
+    if expect != sv.SPEC_OK:
+        assert lib.spec_last_error().decode() != ""
+
+
+def test_greedy_needs_no_draft(lib):
+    # greedy with a null draft and null uniforms passes validation up to the workspace check
+    assert _linear(lib, T=0.0, draft=None, u=None, ws=None) == sv.SPEC_ERR_WORKSPACE
+
+
+def test_bonus_and_tree_host_validation(lib):
+    f = lib.spec_sample_bonus
+    assert f(FAKE, FAKE, 1, -1, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 2, 2, 10, None, FAKE, 1.0, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 2, 2, 10, FAKE, None, 1.0, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 0, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, None) == sv.SPEC_OK
+    t = lib.spec_verify_tree
+    assert t(FAKE, 0, 2, 0, 10, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 0, 2, 5, 10, FAKE, FAKE, -1, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 0, 2, 5, 10, None, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert t(FAKE, 0, 2, 5, 10, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, None, 1 << 20, None) == sv.SPEC_ERR_WORKSPACE
+    assert t(FAKE, 0, 0, 5, 10, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    t = torch.zeros((1, 2, 8))
+    with pytest.raises(ValueError):
+        sv.spec_verify_linear(t, t[:, :1], torch.zeros((1, 1), dtype=torch.int32), torch.zeros((1, 1)),
+                              torch.zeros(1), 1.0)
