@@ -32,7 +32,8 @@
 //   * The leader CTA of each unit publishes its result and bumps a
 //     per-sequence counter; the last unit of a sequence to finish (no waiting
 //     anywhere) finds the first rejection with a warp ballot, writes the
-//     emitted tokens and resets the counter, leaving the workspace zeroed.
+//     emitted tokens, and zeroes the sequence's counter and entries, so the
+//     workspace is all zero again after every call.
 //   * No tensor cores (nothing here is a contraction); every wait is bounded
 //     and reports SPEC_DEV_TIMEOUT instead of trapping.
 #pragma once
@@ -796,8 +797,14 @@ __global__ void __launch_bounds__(kThreads, 3) spec_unit_kernel(const Params p) 
                     if (lane == 0) {
                         p.accept_len[b] = j;
                         p.num_emitted[b] = j + (has_bonus ? 1 : 0);
-                        p.ws_counter[b] = 0u;
                     }
+                    // leave this sequence's workspace entries zero for the next call,
+                    // whatever (B, K) that call uses the workspace with
+                    __syncwarp();
+                    if (MODE == kLinearSample)
+                        for (int i = lane; i < K; i += 32) p.ws_acc[static_cast<size_t>(b) * K + i] = 0;
+                    for (int i = lane; i <= K; i += 32) p.ws_val[static_cast<size_t>(b) * (K + 1) + i] = 0;
+                    if (lane == 0) p.ws_counter[b] = 0u;
                 }
             } else {  // tree walk
                 const int N = p.units_per_seq;
@@ -817,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 3) spec_unit_kernel(const Params p) 
                     am_s[cidx] = __ldcg(&p.ws_val[static_cast<size_t>(b) * N + cidx]);
                 }
                 __syncthreads();
+                for (int cidx = tid; cidx < N; cidx += kThreads) p.ws_val[static_cast<size_t>(b) * N + cidx] = 0;
                 if (warp == 0) {
                     const int D = p.max_depth;
                     int32_t *pn = p.path_nodes + static_cast<size_t>(b) * (D + 1);

@@ -163,7 +163,28 @@ def test_workspace_left_zeroed():
     sv.spec_verify_linear(d["target"], d["draft"], d["draft_tokens"], d["u_accept"], d["u_bonus"], 1.0,
                           workspace=ws)
     torch.cuda.synchronize()
-    assert int(ws[:5 * 4].sum()) == 0      # per-sequence counters reset by the last unit
+    assert int(ws.sum()) == 0              # counters and per-unit entries all reset
+
+
+def test_one_workspace_shared_by_different_shapes():
+    """A workspace used by a (B=3, K=2) call then serves a (B=6, K=3) call and a tree call."""
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    for B, K, V, T, seed in ((3, 2, 999, 1.0, 21), (6, 3, 1001, 0.8, 22), (6, 3, 1001, 0.0, 23), (2, 7, 500, 1.0, 24)):
+        d = rand_linear(B, K, V, "f32", seed=seed)
+        r = sv.spec_verify_linear(d["target"], d["draft"] if T > 0 else None, d["draft_tokens"], d["u_accept"],
+                                  d["u_bonus"], T, probs=T > 0, workspace=ws)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in r.items()}
+        o = oracle.verify_linear(to_oracle(d["target"]), to_oracle(d["draft"]) if T > 0 else None,
+                                 to_oracle(d["draft_tokens"]), to_oracle(d["u_accept"]), to_oracle(d["u_bonus"]), T)
+        assert_parity(g, o, d, T)
+        assert int(ws.sum()) == 0
+    t, par, tok = _random_tree_inputs(5, 9, 300, "f32", seed=3)
+    r = sv.spec_verify_tree(t, par, tok, 4, workspace=ws)
+    torch.cuda.synchronize()
+    o = oracle.verify_tree(to_oracle(t), to_oracle(par), to_oracle(tok), 4)
+    assert compare.compare_tree({k: v.cpu().numpy() for k, v in r.items()}, o).ok
+    assert int(ws.sum()) == 0
 
 
 # ----------------------------------------------------------- extra token alone
