@@ -27,8 +27,10 @@
  *
  * Readings taken where the pages are silent (all restated in the design doc):
  *   - accept draft token x_i iff u_i < min(1, p_i(x_i) / q_i(x_i)) (strict),
- *     with p_i = softmax(target_i / T) and q_i = softmax(draft_i / T);
- *     q_i(x_i) == 0 gives ratio +inf when p_i(x_i) > 0 and 0 otherwise;
+ *     with p_i = softmax(target_i / T) and q_i = softmax(draft_i / T); for
+ *     finite logits both are positive, and the quotient is evaluated as
+ *     exp(((t_x - m_t) - (d_x - m_d)) / T) * S_d / S_t so that it stays
+ *     defined where p and q both underflow in double;
  *   - at the first rejection j < K the extra token is drawn from the
  *     normalised residual max(0, p_j - q_j); if every draft token was
  *     accepted it is drawn from p_K;
@@ -75,8 +77,10 @@ static double logit_at(const void *base, int dtype, size_t idx) {
     return (double)f;
 }
 
-/* p[v] = exp((l_v - max l) / T) / sum_v' exp((l_v' - max l) / T), sequential sums. */
-static void softmax_row(const void *logits, int dtype, size_t row, int V, double T, double *p) {
+/* p[v] = exp((l_v - m) / T) / S with m = max_v l_v and S = sum_v exp((l_v - m) / T),
+ * summed sequentially; m and S are returned too. */
+static void softmax_row(const void *logits, int dtype, size_t row, int V, double T, double *p,
+                        double *m_out, double *S_out) {
     size_t off = row * (size_t)V;
     double m = -INFINITY;
     for (int v = 0; v < V; ++v) {
@@ -89,6 +93,8 @@ static void softmax_row(const void *logits, int dtype, size_t row, int V, double
         S += p[v];
     }
     for (int v = 0; v < V; ++v) p[v] /= S;
+    if (m_out) *m_out = m;
+    if (S_out) *S_out = S;
 }
 
 /* Lowest index of the maximum logit of one row. */
@@ -136,9 +142,9 @@ static int inverse_cdf(const double *w, int V, double u, double *lo, double *hi)
 static int extra_token_sampled(const void *target, const void *draft, int dtype, int b, int K, int V,
                                int j, double T, double u, double *w, double *pj, double *qj,
                                double *lo, double *hi, uint32_t *flag) {
-    softmax_row(target, dtype, (size_t)b * (K + 1) + j, V, T, pj);
+    softmax_row(target, dtype, (size_t)b * (K + 1) + j, V, T, pj, NULL, NULL);
     if (j < K) {
-        softmax_row(draft, dtype, (size_t)b * K + j, V, T, qj);
+        softmax_row(draft, dtype, (size_t)b * K + j, V, T, qj, NULL, NULL);
         double W = 0.0;
         for (int v = 0; v < V; ++v) {
             double d = pj[v] - qj[v];
@@ -189,11 +195,16 @@ int oracle_verify_linear(const void *target, const void *draft, int dtype, int B
                     int x = draft_tokens[(size_t)b * K + i];
                     double px = 0.0, qx = 0.0, thr = 0.0;
                     if (x >= 0 && x < V) {
-                        softmax_row(target, dtype, (size_t)b * (K + 1) + i, V, T, p);
-                        softmax_row(draft, dtype, (size_t)b * K + i, V, T, q);
+                        double mt, St, md, Sd;
+                        softmax_row(target, dtype, (size_t)b * (K + 1) + i, V, T, p, &mt, &St);
+                        softmax_row(draft, dtype, (size_t)b * K + i, V, T, q, &md, &Sd);
                         px = p[x];
                         qx = q[x];
-                        double ratio = qx > 0.0 ? px / qx : (px > 0.0 ? INFINITY : 0.0);
+                        /* p_i(x) / q_i(x), written as one quotient of the two softmax
+                         * terms so that it stays defined where p and q both underflow */
+                        double tx = logit_at(target, dtype, ((size_t)b * (K + 1) + i) * (size_t)V + x);
+                        double dx = logit_at(draft, dtype, ((size_t)b * K + i) * (size_t)V + x);
+                        double ratio = exp(((tx - mt) - (dx - md)) / T) * (Sd / St);
                         thr = ratio < 1.0 ? ratio : 1.0;
                     } else {
                         flag |= ORACLE_FLAG_BAD_TOKEN;

@@ -23,13 +23,16 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
 MUTANTS = [
     ("residual_sign", "double d = pj[v] - qj[v];", "double d = qj[v] - pj[v];"),
     ("residual_unclamped", "w[v] = d > 0.0 ? d : 0.0;", "w[v] = d;"),
-    ("ratio_transposed", "double ratio = qx > 0.0 ? px / qx", "double ratio = qx > 0.0 ? qx / px"),
-    ("draft_temperature_dropped", "softmax_row(draft, dtype, (size_t)b * K + i, V, T, q);",
-     "softmax_row(draft, dtype, (size_t)b * K + i, V, 1.0, q);"),
-    ("target_row_off_by_one", "softmax_row(target, dtype, (size_t)b * (K + 1) + i, V, T, p);",
-     "softmax_row(target, dtype, (size_t)b * (K + 1) + i + 1, V, T, p);"),
-    ("tail_from_row_zero", "softmax_row(target, dtype, (size_t)b * (K + 1) + j, V, T, pj);",
-     "softmax_row(target, dtype, (size_t)b * (K + 1) + (j < K ? j : 0), V, T, pj);"),
+    ("ratio_transposed", "double ratio = exp(((tx - mt) - (dx - md)) / T) * (Sd / St);",
+     "double ratio = exp(((dx - md) - (tx - mt)) / T) * (St / Sd);"),
+    ("ratio_sums_dropped", "double ratio = exp(((tx - mt) - (dx - md)) / T) * (Sd / St);",
+     "double ratio = exp(((tx - mt) - (dx - md)) / T);"),
+    ("draft_temperature_dropped", "softmax_row(draft, dtype, (size_t)b * K + i, V, T, q, &md, &Sd);",
+     "softmax_row(draft, dtype, (size_t)b * K + i, V, 1.0, q, &md, &Sd);"),
+    ("target_row_off_by_one", "softmax_row(target, dtype, (size_t)b * (K + 1) + i, V, T, p, &mt, &St);",
+     "softmax_row(target, dtype, (size_t)b * (K + 1) + i + 1, V, T, p, &mt, &St);"),
+    ("tail_from_row_zero", "softmax_row(target, dtype, (size_t)b * (K + 1) + j, V, T, pj, NULL, NULL);",
+     "softmax_row(target, dtype, (size_t)b * (K + 1) + (j < K ? j : 0), V, T, pj, NULL, NULL);"),
     ("last_rejection_not_first", "j = i;\n                        decided = 1;", "j = i;"),
     ("inverse_cdf_not_strict", "if (C > target) {", "if (C >= target) {"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),

@@ -265,13 +265,19 @@ def test_greedy_equals_argmax_decoding(oracle_lib):
 
 
 def test_tiny_temperature_reduces_to_greedy(oracle_lib):
+    """At T -> 0 with draft tokens drawn as a T -> 0 draft would (its argmax),
+    speculative sampling is greedy decoding: p/q -> 0 when x misses the target's
+    argmax, -> infinity (or 1) when it hits it; the residual and p_K become
+    one-hot at the target's argmax."""
     rng = np.random.default_rng(12)
     B, K, V = 30, 4, 50
     base = rng.permutation(np.arange(V, dtype=np.float32))       # distinct, gaps >= 1
     target = np.stack([[rng.permutation(base) for _ in range(K + 1)] for _ in range(B)])
     draft = np.stack([[rng.permutation(base) for _ in range(K)] for _ in range(B)])
     am = target.argmax(-1)
-    tokens = np.where(rng.random((B, K)) < 0.6, am[:, :K], rng.integers(0, V, (B, K))).astype(np.int32)
+    # a draft sampled at T -> 0 proposes its own argmax; half the time it agrees with the target
+    dam = draft.argmax(-1)
+    tokens = np.where(rng.random((B, K)) < 0.5, am[:, :K], dam).astype(np.int32)
     u = rng.random((B, K)).astype(np.float32)
     ub = rng.random(B).astype(np.float32)
     g = oracle.verify_linear(target, None, tokens, None, ub, 0.0, lib=oracle_lib)
