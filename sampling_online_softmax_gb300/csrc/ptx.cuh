@@ -61,6 +61,11 @@ __device__ __forceinline__ double ld_dsmem_f64(uint32_t addr) {
     asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
     return v;
 }
+__device__ __forceinline__ long long ld_dsmem_s64(uint32_t addr) {
+    long long v;
+    asm volatile("ld.shared::cluster.s64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_dsmem_s32(uint32_t addr, int v) {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

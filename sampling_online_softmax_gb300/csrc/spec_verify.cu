@@ -33,8 +33,16 @@ spec_status fail(spec_status s, const char *fmt, ...) {
 inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
 inline bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-// Shared-memory budget per CTA that still lets three CTAs share one SM.
-constexpr size_t kTargetDynSmem = 70 * 1024;
+// Stage sizing: about 32 KB of logits per CTA and unit, and a ring of stages
+// that lets two CTAs share an SM (the ring alone hides HBM latency).
+#ifndef SPEC_STAGE_TARGET
+#define SPEC_STAGE_TARGET (40 * 1024)
+#endif
+#ifndef SPEC_SMEM_PER_CTA
+#define SPEC_SMEM_PER_CTA (110 * 1024)
+#endif
+constexpr size_t kStageTarget = SPEC_STAGE_TARGET;
+constexpr size_t kSmemPerCta = SPEC_SMEM_PER_CTA;
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -71,79 +79,91 @@ struct Shape {
     int C;          // CTAs per cluster
     int L;          // slice length (elements)
     int row_buf;    // bytes per row buffer
+    int stage;      // bytes per stage
+    int nstage;     // stages in the ring
     size_t dyn;     // dynamic shared memory per CTA
 };
 
-Shape shape_for(int C, int V, int eb, int rows_alloc, bool sample, int stage_ints) {
+size_t round128(size_t n) { return (n + 127) / 128 * 128; }
+
+// Stage geometry for cluster size C (nstage left at 0).
+Shape stage_for(int C, int V, int eb, int rows_alloc, bool sample, int stage_min) {
     Shape s;
     const int G = 16 / eb;
     s.C = C;
     int L = (V + C - 1) / C;
     L = ((L + G - 1) / G) * G;
     s.L = L;
-    s.row_buf = ((L * eb + 32) + 127) / 128 * 128;
-    size_t dyn = static_cast<size_t>(rows_alloc) * s.row_buf;
-    if (sample) {
-        const size_t ngmax = static_cast<size_t>(L) * eb / 16 + 2;
-        dyn += (ngmax * 4 + 127) / 128 * 128;
-    }
-    dyn = std::max(dyn, static_cast<size_t>(stage_ints) * 4);
-    s.dyn = std::max<size_t>(dyn, 128);
+    s.row_buf = static_cast<int>(round128(static_cast<size_t>(L) * eb + 32));
+    s.stage = std::max(rows_alloc * s.row_buf, static_cast<int>(round128(static_cast<size_t>(stage_min))));
+    s.nstage = 0;
+    s.dyn = sample ? round128((static_cast<size_t>(L) * eb / 16 + 2) * 4) : 0;  // per-group weights
     return s;
 }
 
-// Cluster size: the smallest power of two whose slice fits the shared-memory
-// target (else the device maximum); then doubled while the grid would not
-// give every SM two CTAs.
-bool choose_shape(int64_t units, int V, int eb, int rows_alloc, bool sample, int stage_ints,
-                  const DeviceInfo &di, Shape *out) {
-    int C = 0;
+// Ring depth for a stage geometry within `budget` bytes of shared memory (0 if none fits).
+Shape with_stages(Shape s, size_t budget) {
+    const size_t extra = s.dyn;
+    int n = 0;
+    while (n < kMaxStages && extra + static_cast<size_t>(n + 1) * s.stage <= budget) ++n;
+    s.nstage = n;
+    s.dyn = extra + static_cast<size_t>(n) * s.stage;
+    return s;
+}
+
+// Cluster size: the smallest power of two whose stage holds about kStageTarget
+// bytes (16 if none); the ring takes what two CTAs per SM leave, else what one does.
+bool choose_shape(int V, int eb, int rows_alloc, bool sample, int stage_min, const DeviceInfo &di, Shape *out) {
+    int C = 16;
     for (int c = 1; c <= 16; c *= 2)
-        if (shape_for(c, V, eb, rows_alloc, sample, stage_ints).dyn <= kTargetDynSmem) {
+        if (static_cast<size_t>(stage_for(c, V, eb, rows_alloc, sample, stage_min).stage) <= kStageTarget) {
             C = c;
             break;
         }
-    if (C == 0)
-        for (int c = 1; c <= 16; c *= 2)
-            if (shape_for(c, V, eb, rows_alloc, sample, stage_ints).dyn <= di.max_dyn) {
-                C = c;
-                break;
-            }
-    if (C == 0) return false;
-    while (C < 16 && units * C < 2LL * di.sms) C *= 2;
-    *out = shape_for(C, V, eb, rows_alloc, sample, stage_ints);
-    return true;
+    Shape s = stage_for(C, V, eb, rows_alloc, sample, stage_min);
+    Shape two = with_stages(s, std::min(kSmemPerCta, di.max_dyn));
+    if (two.nstage >= 2) {
+        *out = two;
+        return true;
+    }
+    Shape one = with_stages(s, di.max_dyn);
+    if (one.nstage >= 1) {
+        *out = one;
+        return true;
+    }
+    return false;
 }
 
-// Whether at least one cluster of this shape can be resident (cached per device, kernel, shape).
-bool cluster_fits(int dev, const void *kernel, const cudaLaunchConfig_t &cfg) {
+// Clusters of this kernel and shape that can be resident at once (cached).
+int active_clusters(int dev, const void *kernel, const cudaLaunchConfig_t &cfg) {
     static std::mutex mu;
-    static std::map<std::tuple<int, const void *, unsigned, size_t>, bool> cache;
+    static std::map<std::tuple<int, const void *, unsigned, size_t>, int> cache;
     const auto key = std::make_tuple(dev, kernel, cfg.attrs[0].val.clusterDim.x, cfg.dynamicSmemBytes);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
     cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-    const bool ok = (e == cudaSuccess && n > 0);
-    if (e != cudaSuccess) cudaGetLastError();  // clear the (non-sticky) error
-    cache[key] = ok;
-    return ok;
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the (non-sticky) error
+        n = 0;
+    }
+    cache[key] = n;
+    return n;
 }
 
 template <int EB, int MODE>
-spec_status launch(const Params &p0, int64_t units, int rows_alloc, int stage_ints, cudaStream_t stream) {
+spec_status launch(const Params &p0, int rows_alloc, int stage_min, cudaStream_t stream) {
     DeviceInfo di;
     int dev = 0;
     spec_status st = device_info(&di, &dev);
     if (st != SPEC_OK) return st;
-    Shape sh;
     constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
-    if (!choose_shape(units, p0.V, EB, rows_alloc, kSample, stage_ints, di, &sh))
+    Shape sh;
+    if (!choose_shape(p0.V, EB, rows_alloc, kSample, stage_min, di, &sh))
         return fail(SPEC_ERR_UNSUPPORTED, "V=%d does not fit a 16-CTA cluster's shared memory", p0.V);
-    if (units * sh.C > INT_MAX) return fail(SPEC_ERR_UNSUPPORTED, "grid too large (%lld units)", (long long)units);
 
-    auto kernel = spec_unit_kernel<EB, MODE>;
+    auto kernel = spec_verify_kernel<EB, MODE>;
     {
         // per device and kernel, once: allow the largest dynamic shared memory and 16-CTA clusters
         static bool configured[kMaxDevices] = {};
@@ -165,33 +185,44 @@ spec_status launch(const Params &p0, int64_t units, int rows_alloc, int stage_in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // a cluster shape the GPU cannot place is replaced by the next smaller one
+    // persistent grid: as many clusters as fit at once (a shape that cannot be
+    // placed at all is replaced by the next smaller cluster)
+    int nclusters = 0;
     for (;;) {
         attr[0].val.clusterDim.x = static_cast<unsigned>(sh.C);
-        cfg.gridDim = dim3(static_cast<unsigned>(units * sh.C), 1, 1);
+        cfg.gridDim = dim3(static_cast<unsigned>(sh.C), 1, 1);
         cfg.dynamicSmemBytes = sh.dyn;
-        if (cluster_fits(dev, reinterpret_cast<const void *>(kernel), cfg)) break;
+        nclusters = active_clusters(dev, reinterpret_cast<const void *>(kernel), cfg);
+        if (nclusters > 0) break;
         if (sh.C == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster shape fits (smem=%zu)", sh.dyn);
-        sh = shape_for(sh.C / 2, p0.V, EB, rows_alloc, kSample, stage_ints);
-        if (sh.dyn > di.max_dyn) return fail(SPEC_ERR_UNSUPPORTED, "no cluster shape fits V=%d", p0.V);
+        Shape smaller = with_stages(stage_for(sh.C / 2, p0.V, EB, rows_alloc, kSample, stage_min), di.max_dyn);
+        if (smaller.nstage < 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster shape fits V=%d", p0.V);
+        sh = smaller;
     }
+    nclusters = std::min(nclusters, p0.n_units);
+    cfg.gridDim = dim3(static_cast<unsigned>(nclusters * sh.C), 1, 1);
     Params p = p0;
     p.slice_len = sh.L;
     p.row_buf_bytes = sh.row_buf;
+    p.stage_bytes = sh.stage;
+    p.nstage = sh.nstage;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
     if (e != cudaSuccess)
-        return fail(SPEC_ERR_CUDA, "launch (C=%d, smem=%zu): %s", sh.C, sh.dyn, cudaGetErrorString(e));
+        return fail(SPEC_ERR_CUDA, "launch (C=%d, stages=%d, smem=%zu): %s", sh.C, sh.nstage, sh.dyn,
+                    cudaGetErrorString(e));
     return SPEC_OK;
 }
 
-// Workspace layout: [counter: B u32][accept bits: B*K i32][values: B*U i32], 16-byte aligned parts.
+// Workspace layout (16-byte aligned parts): [counter: B u32][first rejection: B i32]
+// [accept bits: B*K i32][values: B*U i32].
 struct WsLayout {
-    size_t counter, acc, val, total;
+    size_t counter, first, acc, val, total;
 };
 WsLayout ws_layout(int B, int K, int units_per_seq) {
     WsLayout w;
     w.counter = 0;
-    w.acc = align16(static_cast<size_t>(B) * 4);
+    w.first = align16(static_cast<size_t>(B) * 4);
+    w.acc = w.first + align16(static_cast<size_t>(B) * 4);
     w.val = w.acc + align16(static_cast<size_t>(B) * K * 4);
     w.total = w.val + align16(static_cast<size_t>(B) * units_per_seq * 4);
     return w;
@@ -247,7 +278,6 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     }
     if (!accept_len || !num_emitted || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "an output pointer is null");
     if (u_bonus && !out_tokens) return fail(SPEC_ERR_INVALID_ARG, "out_tokens is required with u_bonus");
-    if (static_cast<int64_t>(K) + 1 > INT_MAX / 16) return fail(SPEC_ERR_UNSUPPORTED, "K too large");
     const WsLayout wl = ws_layout(B, K, K + 1);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
@@ -271,13 +301,14 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     p.status = dev_status;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     p.ws_counter = reinterpret_cast<uint32_t *>(ws + wl.counter);
+    p.ws_first = reinterpret_cast<int32_t *>(ws + wl.first);
     p.ws_acc = reinterpret_cast<int32_t *>(ws + wl.acc);
     p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
-    const int64_t units = static_cast<int64_t>(B) * (K + 1);
+    if (static_cast<int64_t>(B) * (K + 1) > INT_MAX / 16) return fail(SPEC_ERR_UNSUPPORTED, "B * (K + 1) too large");
+    p.n_units = B * (K + 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sample)
-        return eb == 4 ? launch<4, kLinearSample>(p, units, 2, 0, s) : launch<2, kLinearSample>(p, units, 2, 0, s);
-    return eb == 4 ? launch<4, kLinearGreedy>(p, units, 1, 0, s) : launch<2, kLinearGreedy>(p, units, 1, 0, s);
+    if (sample) return eb == 4 ? launch<4, kLinearSample>(p, 2, 0, s) : launch<2, kLinearSample>(p, 2, 0, s);
+    return eb == 4 ? launch<4, kLinearGreedy>(p, 1, 0, s) : launch<2, kLinearGreedy>(p, 1, 0, s);
 }
 
 extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits, spec_dtype dtype,
@@ -310,10 +341,10 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     p.accept_len_in = accept_len;
     p.bonus_token = bonus_token;
     p.status = dev_status;
+    p.n_units = B;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sample)
-        return eb == 4 ? launch<4, kBonusSample>(p, B, 2, 0, s) : launch<2, kBonusSample>(p, B, 2, 0, s);
-    return eb == 4 ? launch<4, kBonusGreedy>(p, B, 1, 0, s) : launch<2, kBonusGreedy>(p, B, 1, 0, s);
+    if (sample) return eb == 4 ? launch<4, kBonusSample>(p, 2, 0, s) : launch<2, kBonusSample>(p, 2, 0, s);
+    return eb == 4 ? launch<4, kBonusGreedy>(p, 1, 0, s) : launch<2, kBonusGreedy>(p, 1, 0, s);
 }
 
 extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B, int N, int V,
@@ -330,7 +361,6 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     if (!target_logits || !aligned(target_logits, eb)) return fail(SPEC_ERR_INVALID_ARG, "target_logits null or misaligned");
     if (!parents || !node_tokens || !path_nodes || !path_len || !out_tokens || !dev_status)
         return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
-    if (N > INT_MAX / 16) return fail(SPEC_ERR_UNSUPPORTED, "N too large");
     const WsLayout wl = ws_layout(B, 0, N);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
@@ -350,10 +380,13 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     p.status = dev_status;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     p.ws_counter = reinterpret_cast<uint32_t *>(ws + wl.counter);
+    p.ws_first = reinterpret_cast<int32_t *>(ws + wl.first);
     p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
-    const int64_t units = static_cast<int64_t>(B) * N;
+    if (static_cast<int64_t>(B) * N > INT_MAX / 16) return fail(SPEC_ERR_UNSUPPORTED, "B * N too large");
+    p.n_units = B * N;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return eb == 4 ? launch<4, kTreeGreedy>(p, units, 1, 3 * N, s) : launch<2, kTreeGreedy>(p, units, 1, 3 * N, s);
+    // the last unit stages parents, node tokens and argmaxes (3 * N ints) in a stage buffer
+    return eb == 4 ? launch<4, kTreeGreedy>(p, 1, 12 * N, s) : launch<2, kTreeGreedy>(p, 1, 12 * N, s);
 }
 
 extern "C" const char *spec_status_string(spec_status status) {
