@@ -227,7 +227,7 @@ def run_ours(args):
                out_tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
                num_emitted=torch.empty(B, dtype=torch.int32, device=dev))
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = torch.zeros(sv.spec_workspace_bytes_linear(B, K), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(sv.spec_workspace_bytes_linear(B, K, V, torch.bfloat16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     h = ctypes.c_void_p(stream.cuda_stream)
     P = ctypes.c_void_p
@@ -333,7 +333,7 @@ def run_ours(args):
             "config": workload_config(w, bytes_per_step),
             "roofline": {"bound": "hbm", "achieved": gbps, "peak": peak, "unit": "GB/s", "frac": gbps / peak,
                          "peak_kind": peak_kind, "traffic": traffic,
-                         "kernel": "spec_unit_kernel<2, kLinearSample>"},
+                         "kernel": "spec_verify_kernel<2, kLinearSample>"},
             "e2e": {"value": world * B * e2e_steps / e2e_el, "unit": "seqs/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": args.steps,

@@ -38,13 +38,13 @@
  *     SPEC_DEV_* bits into *dev_status (which the caller zeroes); kernels never
  *     trap and never abort.
  *   - All arithmetic on the device is fp32 (bf16 inputs are widened exactly);
- *     cumulative sums for the inverse CDF are carried in fp64 above the level
- *     of one 16-byte group of logits.
- *   - Workspace: spec_verify_linear and spec_verify_tree need a caller-owned
- *     device workspace of spec_workspace_bytes_*() bytes, 16-byte aligned and
- *     zero-filled before its first use.  Every call leaves it zero-filled
- *     again, so one zeroing suffices for any number of calls, but one
- *     workspace must not be shared by calls that may run at the same time.
+ *     cumulative sums for the inverse CDF are exact int64 sums of the fp32
+ *     weights of 16-byte groups of logits, in units of 2^-52.
+ *   - Workspace: every entry point needs a caller-owned device workspace of
+ *     spec_workspace_bytes_*() bytes, 16-byte aligned and zero-filled before
+ *     its first use.  Every call leaves it zero-filled again, so one zeroing
+ *     suffices for any number of calls, but one workspace must not be shared
+ *     by calls that may run at the same time.
  *   - The functions keep no mutable global state apart from a per-thread copy
  *     of the last error message; they may be called from several host threads.
  */
@@ -79,11 +79,15 @@ typedef enum spec_dtype {
 #define SPEC_DEV_BAD_TREE     16u  /* parents[] not topological (0 <= parents[c] < c): edge ignored */
 #define SPEC_DEV_BAD_LENGTH   32u  /* spec_sample_bonus: accept_len[b] outside [0, K]; token -1 */
 
-/* Bytes of workspace spec_verify_linear needs for B sequences of K draft tokens. */
-size_t spec_workspace_bytes_linear(int B, int K);
+/* Bytes of workspace spec_verify_linear needs for B sequences of K draft
+ * tokens over a vocabulary of V logits of `dtype` (0 for invalid sizes). */
+size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype);
+
+/* Bytes of workspace spec_sample_bonus needs for B sequences. */
+size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype);
 
 /* Bytes of workspace spec_verify_tree needs for B sequences of N tree nodes. */
-size_t spec_workspace_bytes_tree(int B, int N);
+size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype);
 
 /*
  * Linear verify and (optionally) the extra token, in one launch.
@@ -124,12 +128,13 @@ spec_status spec_verify_linear(const void *target_logits, const void *draft_logi
  *   accept_len  [B] int32 (device, input); u_bonus [B] (ignored when greedy).
  *   bonus_token [B] int32 (device, output); -1 where accept_len[b] is out of
  *               range (and SPEC_DEV_BAD_LENGTH is set).
- * Needs no workspace.
+ *   workspace, workspace_bytes: spec_workspace_bytes_bonus(B, V, dtype) bytes.
  */
 spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits,
                               spec_dtype dtype, int B, int K, int V,
                               const int32_t *accept_len, const float *u_bonus, float temperature,
-                              int32_t *bonus_token, uint32_t *dev_status, void *stream);
+                              int32_t *bonus_token, uint32_t *dev_status,
+                              void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Greedy verify of a candidate tree ("Speculative-Decoding / Medusa" blog,

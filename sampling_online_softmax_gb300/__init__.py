@@ -64,13 +64,15 @@ def load_library():
                               "python -m sampling_online_softmax_gb300.build)")
         lib = ctypes.CDLL(LIB_PATH)
         P, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
-        lib.spec_workspace_bytes_linear.argtypes = [i32, i32]
+        lib.spec_workspace_bytes_linear.argtypes = [i32, i32, i32, i32]
         lib.spec_workspace_bytes_linear.restype = u64
-        lib.spec_workspace_bytes_tree.argtypes = [i32, i32]
+        lib.spec_workspace_bytes_bonus.argtypes = [i32, i32, i32]
+        lib.spec_workspace_bytes_bonus.restype = u64
+        lib.spec_workspace_bytes_tree.argtypes = [i32, i32, i32, i32]
         lib.spec_workspace_bytes_tree.restype = u64
         lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
         lib.spec_verify_linear.restype = i32
-        lib.spec_sample_bonus.argtypes = [P, P, i32, i32, i32, i32, P, P, f32, P, P, P]
+        lib.spec_sample_bonus.argtypes = [P, P, i32, i32, i32, i32, P, P, f32, P, P, P, u64, P]
         lib.spec_sample_bonus.restype = i32
         lib.spec_verify_tree.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, u64, P]
         lib.spec_verify_tree.restype = i32
@@ -140,12 +142,22 @@ def _workspace(device, stream, nbytes):
         return ws
 
 
-def spec_workspace_bytes_linear(B: int, K: int) -> int:
-    return int(load_library().spec_workspace_bytes_linear(int(B), int(K)))
+def _dtype_arg(dtype) -> int:
+    if isinstance(dtype, torch.dtype):
+        return SPEC_F32 if dtype == torch.float32 else SPEC_BF16
+    return int(dtype)
 
 
-def spec_workspace_bytes_tree(B: int, N: int) -> int:
-    return int(load_library().spec_workspace_bytes_tree(int(B), int(N)))
+def spec_workspace_bytes_linear(B: int, K: int, V: int, dtype) -> int:
+    return int(load_library().spec_workspace_bytes_linear(int(B), int(K), int(V), _dtype_arg(dtype)))
+
+
+def spec_workspace_bytes_bonus(B: int, V: int, dtype) -> int:
+    return int(load_library().spec_workspace_bytes_bonus(int(B), int(V), _dtype_arg(dtype)))
+
+
+def spec_workspace_bytes_tree(B: int, N: int, V: int, dtype) -> int:
+    return int(load_library().spec_workspace_bytes_tree(int(B), int(N), int(V), _dtype_arg(dtype)))
 
 
 def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperature, *,
@@ -182,7 +194,7 @@ def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperatu
         with torch.cuda.stream(s):
             status = torch.zeros(1, dtype=torch.int32, device=dev)
     out["status"] = status
-    nbytes = spec_workspace_bytes_linear(B, K)
+    nbytes = spec_workspace_bytes_linear(B, K, V, target.dtype)
     ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
     with torch.cuda.device(dev):
         st = lib.spec_verify_linear(
@@ -193,7 +205,8 @@ def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperatu
     return out
 
 
-def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status=None, out=None, stream=None):
+def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status=None, out=None, workspace=None,
+                      stream=None):
     """The extra token alone at row accept_len[b]; returns dict(bonus_token [B], status [1])."""
     lib = load_library()
     _cuda(target, "target")
@@ -209,9 +222,12 @@ def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status
     if status is None:
         with torch.cuda.stream(s):
             status = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = spec_workspace_bytes_bonus(B, V, target.dtype)
+    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
     with torch.cuda.device(dev):
         st = lib.spec_sample_bonus(_ptr(target), _ptr(draft), _dtype_code(target), B, K, V, _ptr(accept_len),
-                                   _ptr(u_bonus), float(temperature), _ptr(out), _ptr(status), h)
+                                   _ptr(u_bonus), float(temperature), _ptr(out), _ptr(status), _ptr(ws),
+                                   ws.numel(), h)
     _check(st)
     return dict(bonus_token=out, status=status)
 
@@ -235,7 +251,7 @@ def spec_verify_tree(target, parents, node_tokens, max_depth, *, status=None, ou
         with torch.cuda.stream(s):
             status = torch.zeros(1, dtype=torch.int32, device=dev)
     out["status"] = status
-    nbytes = spec_workspace_bytes_tree(B, N)
+    nbytes = spec_workspace_bytes_tree(B, N, V, target.dtype)
     ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
     with torch.cuda.device(dev):
         st = lib.spec_verify_tree(_ptr(target), _dtype_code(target), B, N, V, _ptr(parents), _ptr(node_tokens), D,

@@ -1,6 +1,6 @@
 // spec_verify.cu -- host side of libspecverify.so: the C ABI declared in
-// include/spec_verify.h (argument checks, workspace layout, cluster sizing and
-// launches of the kernels in verify_kernels.cuh).
+// include/spec_verify.h (argument checks, workspace layout, tile and ring
+// sizing, and the launches of the kernels in verify_kernels.cuh).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -31,17 +31,21 @@ spec_status fail(spec_status s, const char *fmt, ...) {
 }
 
 inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
+inline size_t round128(size_t n) { return (n + 127) / 128 * 128; }
 inline bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-// Stage sizing: about 32 KB of logits per CTA and unit, and a ring of stages
-// that lets two CTAs share an SM (the ring alone hides HBM latency).
-#ifndef SPEC_STAGE_TARGET
-#define SPEC_STAGE_TARGET (40 * 1024)
+// Tiling: about kSliceBytes of each row per tile; the ring of stages takes what
+// two CTAs per SM leave.
+#ifndef SPEC_SLICE_BYTES
+#define SPEC_SLICE_BYTES (16 * 1024)
 #endif
 #ifndef SPEC_SMEM_PER_CTA
 #define SPEC_SMEM_PER_CTA (110 * 1024)
 #endif
-constexpr size_t kStageTarget = SPEC_STAGE_TARGET;
+#ifndef SPEC_GRAB
+#define SPEC_GRAB 4
+#endif
+constexpr int kSliceBytes = SPEC_SLICE_BYTES;
 constexpr size_t kSmemPerCta = SPEC_SMEM_PER_CTA;
 constexpr int kMaxDevices = 64;
 
@@ -75,76 +79,64 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
     return SPEC_OK;
 }
 
+// Slices per row and slice length: a function of V and the element size only
+// (the workspace size depends on it).
+struct Slicing {
+    int S;  // slices (tiles) per unit
+    int L;  // elements per slice, a multiple of 16 / eb
+};
+Slicing slicing(int V, int eb) {
+    const int G = 16 / eb;
+    const long long row_bytes = static_cast<long long>(V) * eb;
+    int S = static_cast<int>(std::max<long long>(1, (row_bytes + kSliceBytes - 1) / kSliceBytes));
+    int L = (V + S - 1) / S;
+    L = (L + G - 1) / G * G;
+    S = (V + L - 1) / L;  // rounding L up may leave a last slice empty: drop it
+    return {S, L};
+}
+
 struct Shape {
-    int C;          // CTAs per cluster
-    int L;          // slice length (elements)
+    Slicing sl;
     int row_buf;    // bytes per row buffer
     int stage;      // bytes per stage
     int nstage;     // stages in the ring
+    int cpt;        // residual chunks per tile
+    size_t extra;   // bytes after the stages: residual chunk sums or tree scratch
     size_t dyn;     // dynamic shared memory per CTA
 };
 
-size_t round128(size_t n) { return (n + 127) / 128 * 128; }
-
-// Stage geometry for cluster size C (nstage left at 0).
-Shape stage_for(int C, int V, int eb, int rows_alloc, bool sample, int stage_min) {
+bool choose_shape(int V, int eb, int rows_alloc, bool sample, int tree_N, const DeviceInfo &di, Shape *out) {
     Shape s;
-    const int G = 16 / eb;
-    s.C = C;
-    int L = (V + C - 1) / C;
-    L = ((L + G - 1) / G) * G;
-    s.L = L;
-    s.row_buf = static_cast<int>(round128(static_cast<size_t>(L) * eb + 32));
-    s.stage = std::max(rows_alloc * s.row_buf, static_cast<int>(round128(static_cast<size_t>(stage_min))));
-    s.nstage = 0;
-    s.dyn = sample ? round128((static_cast<size_t>(L) * eb / 16 + 2) * 4) : 0;  // per-group weights
-    return s;
-}
-
-// Ring depth for a stage geometry within `budget` bytes of shared memory (0 if none fits).
-Shape with_stages(Shape s, size_t budget) {
-    const size_t extra = s.dyn;
-    int n = 0;
-    while (n < kMaxStages && extra + static_cast<size_t>(n + 1) * s.stage <= budget) ++n;
-    s.nstage = n;
-    s.dyn = extra + static_cast<size_t>(n) * s.stage;
-    return s;
-}
-
-// Cluster size: the smallest power of two whose stage holds about kStageTarget
-// bytes (16 if none); the ring takes what two CTAs per SM leave, else what one does.
-bool choose_shape(int V, int eb, int rows_alloc, bool sample, int stage_min, const DeviceInfo &di, Shape *out) {
-    int C = 16;
-    for (int c = 1; c <= 16; c *= 2)
-        if (static_cast<size_t>(stage_for(c, V, eb, rows_alloc, sample, stage_min).stage) <= kStageTarget) {
-            C = c;
-            break;
+    s.sl = slicing(V, eb);
+    s.row_buf = static_cast<int>(round128(static_cast<size_t>(s.sl.L) * eb + 32));
+    s.stage = rows_alloc * s.row_buf;
+    const int max_groups = s.sl.L * eb / 16 + 2;
+    s.cpt = (max_groups + kChunk - 1) / kChunk;
+    s.extra = sample ? round128(static_cast<size_t>(kMaxJobs) * s.sl.S * s.cpt * 8)
+                     : round128(static_cast<size_t>(tree_N) * 12);
+    for (size_t budget : {std::min(kSmemPerCta, di.max_dyn), di.max_dyn}) {
+        int n = 0;
+        while (n < kMaxStages && s.extra + static_cast<size_t>(n + 1) * s.stage <= budget) ++n;
+        if (n >= 2) {
+            s.nstage = n;
+            s.dyn = s.extra + static_cast<size_t>(n) * s.stage;
+            *out = s;
+            return true;
         }
-    Shape s = stage_for(C, V, eb, rows_alloc, sample, stage_min);
-    Shape two = with_stages(s, std::min(kSmemPerCta, di.max_dyn));
-    if (two.nstage >= 2) {
-        *out = two;
-        return true;
-    }
-    Shape one = with_stages(s, di.max_dyn);
-    if (one.nstage >= 1) {
-        *out = one;
-        return true;
     }
     return false;
 }
 
-// Clusters of this kernel and shape that can be resident at once (cached).
-int active_clusters(int dev, const void *kernel, const cudaLaunchConfig_t &cfg) {
+// Resident blocks per SM for this kernel and shared-memory size (cached).
+int blocks_per_sm(int dev, const void *kernel, size_t dyn) {
     static std::mutex mu;
-    static std::map<std::tuple<int, const void *, unsigned, size_t>, int> cache;
-    const auto key = std::make_tuple(dev, kernel, cfg.attrs[0].val.clusterDim.x, cfg.dynamicSmemBytes);
+    static std::map<std::tuple<int, const void *, size_t>, int> cache;
+    const auto key = std::make_tuple(dev, kernel, dyn);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-    if (e != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, dyn) != cudaSuccess) {
         cudaGetLastError();  // clear the (non-sticky) error
         n = 0;
     }
@@ -153,79 +145,79 @@ int active_clusters(int dev, const void *kernel, const cudaLaunchConfig_t &cfg) 
 }
 
 template <int EB, int MODE>
-spec_status launch(const Params &p0, int rows_alloc, int stage_min, cudaStream_t stream) {
+spec_status launch(const Params &p0, int rows_alloc, int tree_N, cudaStream_t stream) {
     DeviceInfo di;
     int dev = 0;
     spec_status st = device_info(&di, &dev);
     if (st != SPEC_OK) return st;
     constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
     Shape sh;
-    if (!choose_shape(p0.V, EB, rows_alloc, kSample, stage_min, di, &sh))
-        return fail(SPEC_ERR_UNSUPPORTED, "V=%d does not fit a 16-CTA cluster's shared memory", p0.V);
-
+    if (!choose_shape(p0.V, EB, rows_alloc, kSample, tree_N, di, &sh))
+        return fail(SPEC_ERR_UNSUPPORTED, "no ring of two stages fits shared memory (V=%d)", p0.V);
     auto kernel = spec_verify_kernel<EB, MODE>;
     {
-        // per device and kernel, once: allow the largest dynamic shared memory and 16-CTA clusters
+        // per device and kernel, once: allow the largest dynamic shared memory
         static bool configured[kMaxDevices] = {};
         std::lock_guard<std::mutex> lock(g_attr_mutex);
         if (!configured[dev]) {
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(di.max_dyn));
-            if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             configured[dev] = true;
         }
     }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // persistent grid: as many clusters as fit at once (a shape that cannot be
-    // placed at all is replaced by the next smaller cluster)
-    int nclusters = 0;
-    for (;;) {
-        attr[0].val.clusterDim.x = static_cast<unsigned>(sh.C);
-        cfg.gridDim = dim3(static_cast<unsigned>(sh.C), 1, 1);
-        cfg.dynamicSmemBytes = sh.dyn;
-        nclusters = active_clusters(dev, reinterpret_cast<const void *>(kernel), cfg);
-        if (nclusters > 0) break;
-        if (sh.C == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster shape fits (smem=%zu)", sh.dyn);
-        Shape smaller = with_stages(stage_for(sh.C / 2, p0.V, EB, rows_alloc, kSample, stage_min), di.max_dyn);
-        if (smaller.nstage < 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster shape fits V=%d", p0.V);
-        sh = smaller;
-    }
-    nclusters = std::min(nclusters, p0.n_units);
-    cfg.gridDim = dim3(static_cast<unsigned>(nclusters * sh.C), 1, 1);
+    const int per_sm = blocks_per_sm(dev, reinterpret_cast<const void *>(kernel), sh.dyn);
+    if (per_sm <= 0) return fail(SPEC_ERR_UNSUPPORTED, "kernel does not fit an SM (smem=%zu)", sh.dyn);
+    const long long tiles = static_cast<long long>(p0.n_units) * sh.sl.S;
+    const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * di.sms);
     Params p = p0;
-    p.slice_len = sh.L;
+    p.S = sh.sl.S;
+    p.slice_len = sh.sl.L;
     p.row_buf_bytes = sh.row_buf;
     p.stage_bytes = sh.stage;
     p.nstage = sh.nstage;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    p.cpt = sh.cpt;
+    p.grab = SPEC_GRAB;
+    spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, sh.dyn, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
-        return fail(SPEC_ERR_CUDA, "launch (C=%d, stages=%d, smem=%zu): %s", sh.C, sh.nstage, sh.dyn,
+        return fail(SPEC_ERR_CUDA, "launch (grid=%lld, stages=%d, smem=%zu): %s", grid, sh.nstage, sh.dyn,
                     cudaGetErrorString(e));
     return SPEC_OK;
 }
 
-// Workspace layout (16-byte aligned parts): [counter: B u32][first rejection: B i32]
-// [accept bits: B*K i32][values: B*U i32].
+// Workspace layout (16-byte aligned parts):
+//   [tile counter, CTAs finished: 2 u32][tiles done per unit: n_units u32]
+//   [units done per sequence: B u32][earliest rejection: B i32]
+//   [accept bits: B*K i32][candidate / argmax: B*U i32][partials: n_units*2*S uint2]
+//   [t(x), d(x): n_units float2]
 struct WsLayout {
-    size_t counter, first, acc, val, total;
+    size_t ctrl, unit_cnt, seq_cnt, first, acc, val, part, tx, total;
 };
-WsLayout ws_layout(int B, int K, int units_per_seq) {
+WsLayout ws_layout(int B, int K, int units_per_seq, int S) {
+    const size_t n_units = static_cast<size_t>(B) * units_per_seq;
     WsLayout w;
-    w.counter = 0;
-    w.first = align16(static_cast<size_t>(B) * 4);
+    w.ctrl = 0;
+    w.unit_cnt = 16;
+    w.seq_cnt = w.unit_cnt + align16(n_units * 4);
+    w.first = w.seq_cnt + align16(static_cast<size_t>(B) * 4);
     w.acc = w.first + align16(static_cast<size_t>(B) * 4);
     w.val = w.acc + align16(static_cast<size_t>(B) * K * 4);
-    w.total = w.val + align16(static_cast<size_t>(B) * units_per_seq * 4);
+    w.part = w.val + align16(n_units * 4);
+    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
+    w.total = w.tx + align16(n_units * 8);
     return w;
+}
+
+void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
+    p.ws_ctrl = reinterpret_cast<uint32_t *>(ws + wl.ctrl);
+    p.ws_unit_cnt = reinterpret_cast<uint32_t *>(ws + wl.unit_cnt);
+    p.ws_seq_cnt = reinterpret_cast<uint32_t *>(ws + wl.seq_cnt);
+    p.ws_first = reinterpret_cast<int32_t *>(ws + wl.first);
+    p.ws_acc = reinterpret_cast<int32_t *>(ws + wl.acc);
+    p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
+    p.ws_part = reinterpret_cast<uint2 *>(ws + wl.part);
+    p.ws_tx = reinterpret_cast<float2 *>(ws + wl.tx);
 }
 
 bool valid_temperature(float T, float *c_out) {
@@ -240,19 +232,27 @@ bool valid_temperature(float T, float *c_out) {
     return true;
 }
 
+int elt_bytes(spec_dtype dtype) { return dtype == SPEC_F32 ? 4 : 2; }
+bool valid_dtype(spec_dtype dtype) { return dtype == SPEC_F32 || dtype == SPEC_BF16; }
+
 }  // namespace
 }  // namespace spec
 
 using namespace spec;
 
-extern "C" size_t spec_workspace_bytes_linear(int B, int K) {
-    if (B <= 0 || K < 0) return 0;
-    return ws_layout(B, K, K + 1).total;
+extern "C" size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype) {
+    if (B <= 0 || K < 0 || V < 1 || !valid_dtype(dtype)) return 0;
+    return ws_layout(B, K, K + 1, slicing(V, elt_bytes(dtype)).S).total;
 }
 
-extern "C" size_t spec_workspace_bytes_tree(int B, int N) {
-    if (B <= 0 || N < 1) return 0;
-    return ws_layout(B, 0, N).total;
+extern "C" size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype) {
+    if (B <= 0 || V < 1 || !valid_dtype(dtype)) return 0;
+    return ws_layout(B, 0, 1, slicing(V, elt_bytes(dtype)).S).total;
+}
+
+extern "C" size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype) {
+    if (B <= 0 || N < 1 || V < 1 || !valid_dtype(dtype)) return 0;
+    return ws_layout(B, 0, N, slicing(V, elt_bytes(dtype)).S).total;
 }
 
 extern "C" spec_status spec_verify_linear(const void *target_logits, const void *draft_logits,
@@ -263,13 +263,13 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
                                           float *probs_out, uint32_t *dev_status, void *workspace,
                                           size_t workspace_bytes, void *stream) {
     g_last_error[0] = '\0';
-    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (!valid_dtype(dtype)) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 0 || K < 0 || V < 1) return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, K >= 0, V >= 1 (B=%d K=%d V=%d)", B, K, V);
     float c = 0.f;
     if (!valid_temperature(temperature, &c)) return fail(SPEC_ERR_INVALID_ARG, "temperature must be finite and >= 0");
     if (B == 0) return SPEC_OK;
     const bool sample = temperature > 0.0f;
-    const int eb = dtype == SPEC_F32 ? 4 : 2;
+    const int eb = elt_bytes(dtype);
     if (!target_logits || !aligned(target_logits, eb)) return fail(SPEC_ERR_INVALID_ARG, "target_logits null or misaligned");
     if (K > 0 && !draft_tokens) return fail(SPEC_ERR_INVALID_ARG, "draft_tokens is null");
     if (sample && K > 0) {
@@ -278,7 +278,8 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     }
     if (!accept_len || !num_emitted || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "an output pointer is null");
     if (u_bonus && !out_tokens) return fail(SPEC_ERR_INVALID_ARG, "out_tokens is required with u_bonus");
-    const WsLayout wl = ws_layout(B, K, K + 1);
+    if (static_cast<long long>(B) * (K + 1) > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B * (K + 1) too large");
+    const WsLayout wl = ws_layout(B, K, K + 1, slicing(V, eb).S);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
 
@@ -290,6 +291,7 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     p.V = V;
     p.t_rows = K + 1;
     p.units_per_seq = K + 1;
+    p.n_units = B * (K + 1);
     p.c = c;
     p.tokens = draft_tokens;
     p.u_accept = u_accept;
@@ -299,13 +301,7 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     p.num_emitted = num_emitted;
     p.probs = sample ? probs_out : nullptr;
     p.status = dev_status;
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    p.ws_counter = reinterpret_cast<uint32_t *>(ws + wl.counter);
-    p.ws_first = reinterpret_cast<int32_t *>(ws + wl.first);
-    p.ws_acc = reinterpret_cast<int32_t *>(ws + wl.acc);
-    p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
-    if (static_cast<int64_t>(B) * (K + 1) > INT_MAX / 16) return fail(SPEC_ERR_UNSUPPORTED, "B * (K + 1) too large");
-    p.n_units = B * (K + 1);
+    bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sample) return eb == 4 ? launch<4, kLinearSample>(p, 2, 0, s) : launch<2, kLinearSample>(p, 2, 0, s);
     return eb == 4 ? launch<4, kLinearGreedy>(p, 1, 0, s) : launch<2, kLinearGreedy>(p, 1, 0, s);
@@ -314,20 +310,24 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
 extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits, spec_dtype dtype,
                                          int B, int K, int V, const int32_t *accept_len, const float *u_bonus,
                                          float temperature, int32_t *bonus_token, uint32_t *dev_status,
-                                         void *stream) {
+                                         void *workspace, size_t workspace_bytes, void *stream) {
     g_last_error[0] = '\0';
-    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (!valid_dtype(dtype)) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 0 || K < 0 || V < 1) return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, K >= 0, V >= 1 (B=%d K=%d V=%d)", B, K, V);
     float c = 0.f;
     if (!valid_temperature(temperature, &c)) return fail(SPEC_ERR_INVALID_ARG, "temperature must be finite and >= 0");
     if (B == 0) return SPEC_OK;
     const bool sample = temperature > 0.0f;
-    const int eb = dtype == SPEC_F32 ? 4 : 2;
+    const int eb = elt_bytes(dtype);
     if (!target_logits || !aligned(target_logits, eb)) return fail(SPEC_ERR_INVALID_ARG, "target_logits null or misaligned");
     if (sample && K > 0 && (!draft_logits || !aligned(draft_logits, eb)))
         return fail(SPEC_ERR_INVALID_ARG, "draft_logits null or misaligned");
     if (sample && !u_bonus) return fail(SPEC_ERR_INVALID_ARG, "u_bonus is null");
     if (!accept_len || !bonus_token || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
+    if (B > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B too large");
+    const WsLayout wl = ws_layout(B, 0, 1, slicing(V, eb).S);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
+        return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
     Params p = {};
     p.target = static_cast<const unsigned char *>(target_logits);
     p.draft = static_cast<const unsigned char *>(draft_logits);
@@ -336,12 +336,13 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     p.V = V;
     p.t_rows = K + 1;
     p.units_per_seq = 1;
+    p.n_units = B;
     p.c = c;
     p.u_bonus = u_bonus;
     p.accept_len_in = accept_len;
     p.bonus_token = bonus_token;
     p.status = dev_status;
-    p.n_units = B;
+    bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sample) return eb == 4 ? launch<4, kBonusSample>(p, 2, 0, s) : launch<2, kBonusSample>(p, 2, 0, s);
     return eb == 4 ? launch<4, kBonusGreedy>(p, 1, 0, s) : launch<2, kBonusGreedy>(p, 1, 0, s);
@@ -353,15 +354,16 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
                                         uint32_t *dev_status, void *workspace, size_t workspace_bytes,
                                         void *stream) {
     g_last_error[0] = '\0';
-    if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (!valid_dtype(dtype)) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 0 || N < 1 || V < 1 || max_depth < 0)
         return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, N >= 1, V >= 1, max_depth >= 0");
     if (B == 0) return SPEC_OK;
-    const int eb = dtype == SPEC_F32 ? 4 : 2;
+    const int eb = elt_bytes(dtype);
     if (!target_logits || !aligned(target_logits, eb)) return fail(SPEC_ERR_INVALID_ARG, "target_logits null or misaligned");
     if (!parents || !node_tokens || !path_nodes || !path_len || !out_tokens || !dev_status)
         return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
-    const WsLayout wl = ws_layout(B, 0, N);
+    if (static_cast<long long>(B) * N > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B * N too large");
+    const WsLayout wl = ws_layout(B, 0, N, slicing(V, eb).S);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
     Params p = {};
@@ -371,6 +373,7 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     p.V = V;
     p.t_rows = N;
     p.units_per_seq = N;
+    p.n_units = B * N;
     p.tokens = node_tokens;
     p.parents = parents;
     p.max_depth = max_depth;
@@ -378,15 +381,10 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     p.out_tokens = out_tokens;
     p.path_nodes = path_nodes;
     p.status = dev_status;
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    p.ws_counter = reinterpret_cast<uint32_t *>(ws + wl.counter);
-    p.ws_first = reinterpret_cast<int32_t *>(ws + wl.first);
-    p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
-    if (static_cast<int64_t>(B) * N > INT_MAX / 16) return fail(SPEC_ERR_UNSUPPORTED, "B * N too large");
-    p.n_units = B * N;
+    bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the last unit stages parents, node tokens and argmaxes (3 * N ints) in a stage buffer
-    return eb == 4 ? launch<4, kTreeGreedy>(p, 1, 12 * N, s) : launch<2, kTreeGreedy>(p, 1, 12 * N, s);
+    // the last unit of a sequence stages parents, node tokens and argmaxes (3 * N ints)
+    return eb == 4 ? launch<4, kTreeGreedy>(p, 1, N, s) : launch<2, kTreeGreedy>(p, 1, N, s);
 }
 
 extern "C" const char *spec_status_string(spec_status status) {

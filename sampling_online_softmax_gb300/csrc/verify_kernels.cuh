@@ -10,36 +10,28 @@
 //   the first rejected position j, and one extra token drawn by inverse CDF
 //   from max(0, p_j - q_j) (j < K) or p_K (j == K), or argmax in greedy mode.
 //
-// How (GB300 design):
-//   * A "unit" is one (sequence, position): target row i together with draft
-//     row i for linear sampling, otherwise one target row.  Units are numbered
-//     position-major (every sequence's position 0, then position 1, ...), so
-//     when a position is processed the earlier positions of its sequence have
-//     usually finished.
-//   * Persistent thread-block clusters of C CTAs (grid = the clusters that fit
-//     at once); cluster g takes units g, g + G, g + 2G, ...  CTA r of a
-//     cluster owns the vocabulary slice [r*L, (r+1)*L) of every row.
-//   * Each CTA has a control warp (warp 0) and eight compute warps.  The
-//     control warp keeps a ring of NSTAGE shared-memory stages full: 1-D bulk
-//     copies (cp.async.bulk; one mbarrier per stage) of the CTA's slices of
-//     the unit NSTAGE-1 ahead, so HBM keeps streaming while the current unit
-//     is reduced and decided.  Slice ends that are not 16-byte aligned are
-//     loaded element-wise; padding is -inf.
-//   * Compute warps reduce their stage (max and exp2-sum per thread, or
-//     max / argmax); the control warp merges the warps, and the cluster's CTAs
-//     merge through distributed shared memory after one cluster barrier per
-//     unit (partials double-buffered by unit parity), so every CTA holds the
-//     same row statistics and takes the same decision.
-//   * A rejected position -- unless an earlier rejection of its sequence has
-//     already been published -- and the tail position draw their candidate
-//     extra token from the rows still resident in the cluster's shared memory:
-//     per-16-byte-group weights, exact int64 fixed-point sums (units of
-//     2^-52) scanned across the CTA and then across the cluster, and one
-//     thread walks its segment.  No second pass over HBM.
-//   * The publishing CTA's control warp writes the unit's result to the
-//     workspace and bumps a per-sequence counter (acq_rel atomic); the last
-//     unit of a sequence to finish emits the tokens (a warp ballot finds the
-//     first rejection) and zeroes the sequence's workspace entries.
+// How (GB300 design): a streaming reduction with no waiting between CTAs.
+//   * A "unit" is one (sequence, position): target row i with draft row i for
+//     linear sampling, otherwise one target row.  Each unit is cut into S
+//     vocabulary slices of about 16 KB per row; a "tile" is one slice of every
+//     row of one unit.  Tiles are numbered sequence-major, positions in order.
+//   * Persistent CTAs (a few per SM) take tiles dynamically from a global
+//     counter.  Each CTA has a control warp and eight compute warps.  The
+//     control warp keeps a ring of shared-memory stages full with 1-D bulk
+//     copies (cp.async.bulk, one mbarrier per stage; unaligned slice ends
+//     element-wise, padding -inf); the compute warps reduce each stage (max
+//     and exp2-sum per row, or max/argmax) and hand the per-warp results back
+//     through a second mbarrier.
+//   * The control warp writes the tile's partial to the workspace and bumps
+//     the unit's tile counter (acq_rel atomic).  The CTA that completes a unit
+//     merges its S partials, takes the acceptance decision, and -- for the
+//     first rejection (or the tail when nothing earlier rejected) -- draws the
+//     candidate extra token itself: it re-streams the unit's slices (from L2,
+//     they were just read) as residual tiles whose compute warps produce exact
+//     int64 fixed-point weight sums (units of 2^-52) per 64-group chunk, then
+//     locates the chunk by a prefix over those sums and rescans that one chunk.
+//   * The CTA that completes a sequence's last unit emits its tokens (a warp
+//     ballot finds the first rejection) and zeroes its workspace entries.
 //   * No tensor cores (nothing here is a contraction).  Every wait is bounded
 //     and reports SPEC_DEV_TIMEOUT instead of trapping.
 #pragma once
@@ -57,9 +49,9 @@ constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kThreads = kComputeThreads + 32;  // warp 0 controls, warps 1..8 compute
 constexpr int kMaxRows = 2;                     // rows per unit: target, draft
 constexpr int kMaxStages = 4;
+constexpr int kMaxJobs = kMaxStages + 1;        // pending extra-token draws per CTA
+constexpr int kChunk = 64;                      // 16-byte groups per residual chunk
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kBarStageFree = 1;                // compute warps hand a stage back to the control warp
-constexpr int kBarCompute = 2;                  // barrier among the compute warps only
 
 enum Mode : int {
     kLinearSample = 0,
@@ -69,13 +61,22 @@ enum Mode : int {
     kBonusGreedy = 4,
 };
 
+enum TileKind : int { kTileEnd = 0, kTileStats = 1, kTileResid = 2 };
+
 struct Params {
     const unsigned char *target;   // [B, t_rows, V]
     const unsigned char *draft;    // [B, K, V] (sampling) or null
     int B, K, V;
     int t_rows;                    // target rows per sequence: K+1 (linear), N (tree)
     int units_per_seq;             // K+1 (linear), N (tree), 1 (extra token alone)
-    int n_units;                   // B * units_per_seq
+    int n_units;
+    int S;                         // tiles (slices) per unit
+    int slice_len;                 // elements per slice (multiple of 16/eb)
+    int row_buf_bytes;             // shared bytes per row buffer in a stage
+    int stage_bytes;               // shared bytes per stage
+    int nstage;                    // stages in the ring (2..kMaxStages)
+    int cpt;                       // residual chunks per tile
+    int grab;                      // tiles taken per visit to the global counter
     float c;                       // log2(e) / T  (sampling modes)
     const int32_t *tokens;         // [B, K] draft tokens, or [B, N] node tokens
     const float *u_accept;         // [B, K]
@@ -90,49 +91,43 @@ struct Params {
     int32_t *path_nodes;           // [B, max_depth+1]
     int32_t *bonus_token;          // [B]
     uint32_t *status;              // [1]
-    uint32_t *ws_counter;          // [B]   units finished per sequence
-    int32_t *ws_first;             // [B]   K + 1 - (earliest published rejection), 0 if none
+    uint32_t *ws_ctrl;             // [0] next tile, [1] CTAs finished
+    uint32_t *ws_unit_cnt;         // [n_units] tiles finished per unit
+    uint32_t *ws_seq_cnt;          // [B] units finished per sequence
+    int32_t *ws_first;             // [B] K + 1 - (earliest published rejection), 0 if none
     int32_t *ws_acc;               // [B*K] accept bits
     int32_t *ws_val;               // [B*units_per_seq] candidate token / argmax
-    int slice_len;                 // elements per CTA slice (multiple of 16/eb)
-    int row_buf_bytes;             // shared bytes per row buffer in a stage
-    int stage_bytes;               // shared bytes per stage
-    int nstage;                    // stages in the ring (1..kMaxStages)
+    uint2 *ws_part;                // [n_units * 2 * S] per-tile partials
+    float2 *ws_tx;                 // [n_units] target and draft logit of the draft token
+};
+
+struct StageMeta {
+    int kind;                      // TileKind
+    int unit, k, b, pos, nrows;
+    int job, tailw;                // residual tiles: job slot, weights of p instead of max(0, p - q)
+    float Mt, invSt, Md, invSd;    // residual tiles: row statistics
+};
+
+struct Job {                       // a pending extra-token draw, private to one CTA
+    int unit, b, pos, nrows, tailw, next_k, done_k, fin;
+    float Mt, invSt, Md, invSd, ub;
 };
 
 struct __align__(16) Ctl {
-    unsigned long long full[kMaxStages];
-    long long incl[kComputeThreads];     // inclusive scan of per-thread segment weights
-    long long warp_tot[kComputeWarps];
-    long long part_w[2];                 // CTA weight total, by unit parity (read by the cluster)
-    long long tlocal;                    // target cumulative weight inside the owner CTA
-    float warp_m[kMaxRows][kComputeWarps];
-    float warp_s[kMaxRows][kComputeWarps];
-    int warp_i[kMaxRows][kComputeWarps];
-    float part_m[2][kMaxRows];           // CTA partial statistics, by unit parity (read by the cluster)
-    float part_s[2][kMaxRows];
-    int part_i[2][kMaxRows];
-    int part_flag[2];
-    float M[kMaxRows];                   // merged statistics, identical in every CTA
-    float S[kMaxRows];
-    int A[kMaxRows];
-    float px, qx, thr;
-    int accept, do_resid, tail_weights, retry, owner_rank, publisher;
-    int warp_first[kComputeWarps];
-    int cand;
+    unsigned long long full[kMaxStages];   // stage loaded (control -> compute)
+    unsigned long long done[kMaxStages];   // stage reduced (compute -> control)
+    StageMeta meta[kMaxStages];
+    float wm[kMaxStages][kMaxRows][kComputeWarps];
+    float wsum[kMaxStages][kMaxRows][kComputeWarps];
+    int wi[kMaxStages][kMaxRows][kComputeWarps];
+    float2 xval[kMaxStages];              // t(x), d(x) when the draft token lies in the stage's slice
+    int xhas[kMaxStages];
+    Job jobs[kMaxJobs];
     int timed_out;
-    uint32_t flags;
-    int st_b[kMaxStages], st_pos[kMaxStages], st_nrows[kMaxStages];
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-__device__ __forceinline__ void bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void bar_arrive(int id, int n) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -153,13 +148,19 @@ __device__ __forceinline__ int ld_relaxed(const int32_t *p) {
 // conversion rounds only weights below 2^-29.
 __device__ __forceinline__ long long fixq(float w) { return __float2ll_rn(w * 4503599627370496.0f); }
 
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
 // ---------------------------------------------------------------- elements
 template <int EB>
 struct Elt;
 
 template <>
 struct Elt<4> {
-    static constexpr int G = 4;  // elements per 16-byte granule
+    static constexpr int G = 4;  // elements per 16-byte group
     __device__ __forceinline__ static void unpack(const uint4 &w, float (&v)[G]) {
         v[0] = __uint_as_float(w.x);
         v[1] = __uint_as_float(w.y);
@@ -169,13 +170,16 @@ struct Elt<4> {
     __device__ __forceinline__ static float load(const unsigned char *p) {
         return *reinterpret_cast<const float *>(p);
     }
+    __device__ __forceinline__ static float gload(const unsigned char *p) {
+        return __uint_as_float(__ldg(reinterpret_cast<const unsigned int *>(p)));
+    }
     __device__ __forceinline__ static void store_neg_inf(unsigned char *p) {
         *reinterpret_cast<uint32_t *>(p) = 0xff800000u;
     }
     __device__ __forceinline__ static void copy(unsigned char *dst, const unsigned char *src) {
         *reinterpret_cast<uint32_t *>(dst) = __ldg(reinterpret_cast<const uint32_t *>(src));
     }
-    __device__ __forceinline__ static float granule_max(const unsigned char *buf, int g0, int g1, int step) {
+    __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1, int step) {
         float m = neg_inf();
         for (int g = g0; g < g1; g += step) {
             const uint4 w = *reinterpret_cast<const uint4 *>(buf + 16 * g);
@@ -202,13 +206,16 @@ struct Elt<2> {
     __device__ __forceinline__ static float load(const unsigned char *p) {
         return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16);
     }
+    __device__ __forceinline__ static float gload(const unsigned char *p) {
+        return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p))) << 16);
+    }
     __device__ __forceinline__ static void store_neg_inf(unsigned char *p) {
         *reinterpret_cast<uint16_t *>(p) = 0xff80u;
     }
     __device__ __forceinline__ static void copy(unsigned char *dst, const unsigned char *src) {
         *reinterpret_cast<uint16_t *>(dst) = __ldg(reinterpret_cast<const unsigned short *>(src));
     }
-    __device__ __forceinline__ static float granule_max(const unsigned char *buf, int g0, int g1, int step) {
+    __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1, int step) {
         uint32_t m = 0xff80ff80u;  // (-inf, -inf)
         for (int g = g0; g < g1; g += step) {
             const uint4 w = *reinterpret_cast<const uint4 *>(buf + 16 * g);
@@ -219,16 +226,16 @@ struct Elt<2> {
 };
 
 // ------------------------------------------------------------ row geometry
-// A CTA's slice [s0, s1) of one row, mirrored in shared memory granule by
-// granule: buffer byte k holds global byte (glo + k), glo = 16-byte floor of
-// the slice start.  Granules [hg, hg + nfull) arrive by bulk copy; partial
-// granules at either end are filled element-wise, with -inf outside the slice.
+// A slice [s0, s1) of one row, mirrored in shared memory 16-byte group by
+// group: buffer byte k holds global byte (glo + k), glo = 16-byte floor of the
+// slice start.  Groups [hg, hg + nfull) arrive by bulk copy; partial groups at
+// either end are filled element-wise, with -inf outside the slice.
 struct RowGeo {
     const unsigned char *glo;  // global address of buffer byte 0
     unsigned char *buf;        // shared buffer (generic pointer)
-    int ngran;                 // granules in the buffer
-    int hg;                    // 1 if granule 0 is partial (and there are full granules)
-    int nfull;                 // granules copied in bulk
+    int ngran;                 // 16-byte groups in the buffer
+    int hg;                    // 1 if group 0 is partial (and there are full groups)
+    int nfull;                 // groups copied in bulk
     int vbase;                 // element index of buffer byte 0 (may be negative)
     int a0off, a1off;          // byte offsets of the slice's first / one-past-last element
 };
@@ -259,12 +266,6 @@ __device__ __forceinline__ RowGeo make_geo(const unsigned char *row, int s0, int
     return g;
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it)
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
 // ------------------------------------------------------- softmax merging
 // (m, s) represents sum exp2((x - m) * c) over a set; merge two such sets.
 __device__ __forceinline__ void merge_ms(float &m, float &s, float m2, float s2, float c) {
@@ -284,87 +285,93 @@ __device__ __forceinline__ void merge_vi(float &v, int &i, float v2, int i2) {
 }
 
 // ------------------------------------------------------ extra-token weights
-// Weights of the G elements of target granule g:
-//   pair (residual):  max(0, p_v - q_v) = max(0, 2^((t-Mt)c)/St - 2^((d-Md)c)/Sd)
-//   tail:             p_v = 2^((t - Mt) c) / St
-// Explicit _rn intrinsics keep the two evaluations of a weight bit-identical.
+// Weight of one element: pair (residual) max(0, p_v - q_v) with
+// p_v = 2^((t - Mt) c) / St and q_v = 2^((d - Md) c) / Sd; tail p_v.  The
+// explicit _rn intrinsics keep every evaluation of a weight bit-identical.
+__device__ __forceinline__ float elem_weight(float t, float d, bool pair, float Mt, float Md, float invSt,
+                                             float invSd, float c) {
+    const float pv = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(t, Mt), c)), invSt);
+    if (!pair) return pv;
+    const float qv = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(d, Md), c)), invSd);
+    return fmaxf(0.0f, __fsub_rn(pv, qv));
+}
+
+// fp32 sum of one 16-byte group's weights, in element order (the order every
+// consumer of a group sum repeats).
 template <int EB>
-__device__ __forceinline__ void granule_weights(const RowGeo &gt, const RowGeo &gd, bool pair, bool same_phase,
-                                                int g, int s0, int s1, float Mt, float Md, float invSt,
-                                                float invSd, float c, float (&w)[Elt<EB>::G]) {
+__device__ __forceinline__ float group_weight(const RowGeo &gt, const RowGeo &gd, bool pair, bool same_phase,
+                                              int g, int s0, int s1, float Mt, float Md, float invSt, float invSd,
+                                              float c) {
     constexpr int G = Elt<EB>::G;
-    float t[G];
+    float t[G], d[G];
     Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(gt.buf + 16 * g), t);
-    if (!pair) {
+    if (pair) {
+        if (same_phase) {
+            Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(gd.buf + 16 * g), d);
+        } else {
 #pragma unroll
-        for (int k = 0; k < G; ++k) w[k] = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(t[k], Mt), c)), invSt);
-        return;
-    }
-    float d[G];
-    if (same_phase) {
-        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(gd.buf + 16 * g), d);
-    } else {
-#pragma unroll
-        for (int k = 0; k < G; ++k) {
-            const int v = gt.vbase + g * G + k;
-            d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(gd.buf + (v - gd.vbase) * EB) : neg_inf();
+            for (int k = 0; k < G; ++k) {
+                const int v = gt.vbase + g * G + k;
+                d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(gd.buf + (v - gd.vbase) * EB) : neg_inf();
+            }
         }
     }
+    float sw = 0.f;
 #pragma unroll
-    for (int k = 0; k < G; ++k) {
-        const float pv = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(t[k], Mt), c)), invSt);
-        const float qv = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(d[k], Md), c)), invSd);
-        w[k] = fmaxf(0.0f, __fsub_rn(pv, qv));
-    }
+    for (int k = 0; k < G; ++k) sw += elem_weight(t[k], pair ? d[k] : 0.f, pair, Mt, Md, invSt, invSd, c);
+    return sw;
 }
 
 // ---------------------------------------------------------- unit layout
 struct UnitRows {
-    int nrows;
+    int b, pos, nrows;
     const unsigned char *row[kMaxRows];
 };
 
-// Rows of unit (b, pos); pos < 0 marks an invalid unit (no rows).
+// Unit u: (sequence b, position pos) and its rows; pos < 0 marks an invalid
+// unit of the extra-token-alone mode (no rows).
 template <int EB, int MODE>
-__device__ __forceinline__ UnitRows unit_rows(const Params &p, int b, int pos) {
+__device__ __forceinline__ UnitRows unit_rows(const Params &p, int u) {
     constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
+    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
     UnitRows ur;
-    ur.nrows = (pos < 0) ? 0 : ((kSample && pos < p.K) ? 2 : 1);
+    if (kBonus) {
+        ur.b = u;
+        ur.pos = p.accept_len_in[u];
+        if (ur.pos < 0 || ur.pos > p.K) ur.pos = -1;
+    } else {
+        ur.b = u / p.units_per_seq;
+        ur.pos = u - ur.b * p.units_per_seq;
+    }
+    ur.nrows = (ur.pos < 0) ? 0 : ((kSample && ur.pos < p.K) ? 2 : 1);
     const size_t row_bytes = static_cast<size_t>(p.V) * EB;
     ur.row[0] = p.target;
-    if (ur.nrows >= 1) ur.row[0] = p.target + (static_cast<size_t>(b) * p.t_rows + pos) * row_bytes;
+    if (ur.nrows >= 1) ur.row[0] = p.target + (static_cast<size_t>(ur.b) * p.t_rows + ur.pos) * row_bytes;
     ur.row[1] = ur.row[0];
-    if (ur.nrows == 2) ur.row[1] = p.draft + (static_cast<size_t>(b) * p.K + pos) * row_bytes;
+    if (ur.nrows == 2) ur.row[1] = p.draft + (static_cast<size_t>(ur.b) * p.K + ur.pos) * row_bytes;
     return ur;
 }
 
-// Control warp: fill stage `s` with this CTA's slices of unit u (position-major:
-// u = pos * B + b; the extra-token-alone mode reads pos from accept_len).
+// ====================================================== control-warp side
+// The control warp fills stage s with slice k of unit u's rows (all 32 lanes call it).
 template <int EB, int MODE>
-__device__ void prefetch_unit(const Params &p, Ctl &ctl, unsigned char *dsm, int s, int u, int s0, int s1,
-                              int lane) {
-    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
-    int pos = u / p.B;
-    const int b = u - pos * p.B;
-    if (kBonus) {
-        pos = p.accept_len_in[b];
-        if (pos < 0 || pos > p.K) pos = -1;  // invalid: no rows; the publisher reports it
-    }
-    const UnitRows ur = unit_rows<EB, MODE>(p, b, pos);
+__device__ void fill_stage(const Params &p, Ctl &ctl, unsigned char *dsm, int s, const StageMeta &m,
+                           const UnitRows &ur, int lane) {
     unsigned char *stage = dsm + static_cast<size_t>(s) * p.stage_bytes;
     const uint32_t bar = ptx::smem_addr(&ctl.full[s]);
+    const int s0 = min(p.V, m.k * p.slice_len);
+    const int s1 = min(p.V, s0 + p.slice_len);
     RowGeo geo[kMaxRows];
 #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) geo[r] = make_geo<EB>(ur.row[r], s0, s1, stage + r * p.row_buf_bytes);
     if (lane == 0) {
-        ctl.st_b[s] = b;
-        ctl.st_pos[s] = pos;
-        ctl.st_nrows[s] = ur.nrows;
+        ctl.meta[s] = m;
         uint32_t bytes = 0;
 #pragma unroll
         for (int r = 0; r < kMaxRows; ++r)
             if (r < ur.nrows) bytes += static_cast<uint32_t>(geo[r].nfull) * 16u;
-        fence_proxy_async();  // earlier generic reads of this stage come before the async writes
+        // the compute warps' reads of this stage are ordered before this point by
+        // the stage's done-mbarrier, which the control warp waited on
         ptx::mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
         for (int r = 0; r < kMaxRows; ++r) {
@@ -374,7 +381,7 @@ __device__ void prefetch_unit(const Params &p, Ctl &ctl, unsigned char *dsm, int
                           static_cast<uint32_t>(geo[r].nfull) * 16u, bar);
         }
     }
-    // ragged ends element-wise (at most 16 slots per row): lanes 0..15 row 0, 16..31 row 1
+    // unaligned ends element-wise (at most 16 slots per row): lanes 0..15 row 0, 16..31 row 1
     {
         const int r = lane >> 4;
         const int e = lane & 15;
@@ -396,42 +403,11 @@ __device__ void prefetch_unit(const Params &p, Ctl &ctl, unsigned char *dsm, int
     if (lane == 0) mbar_arrive(bar);  // second arrival: the element-wise part is in place
 }
 
-// Control warp of the publishing CTA: write the unit's result, count the unit,
-// and if it was the sequence's last one, emit the sequence.
+// Emit sequence b (its last unit just finished) and zero its workspace entries.
 template <int EB, int MODE>
-__device__ void publish(const Params &p, Ctl &ctl, int s, unsigned char *stage, int lane) {
-    constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
-    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
-    const int b = ctl.st_b[s];
-    const int pos = ctl.st_pos[s];
+__device__ void emit_sequence(const Params &p, int b, long long *stage_ints, int lane) {
     const int K = p.K;
     const int U = p.units_per_seq;
-    int last = 0;
-    if (lane == 0) {
-        uint32_t fl = ctl.flags;
-        if (MODE == kLinearSample) {
-            if (pos < K) {
-                p.ws_acc[static_cast<size_t>(b) * K + pos] = ctl.accept;
-                if (p.probs) {
-                    float *pr = p.probs + (static_cast<size_t>(b) * K + pos) * 3;
-                    pr[0] = ctl.px;
-                    pr[1] = ctl.qx;
-                    pr[2] = ctl.thr;
-                }
-            }
-            if (ctl.do_resid) p.ws_val[static_cast<size_t>(b) * U + pos] = ctl.cand;
-        } else if (MODE == kLinearGreedy || MODE == kTreeGreedy) {
-            p.ws_val[static_cast<size_t>(b) * U + pos] = ctl.A[0];
-        } else {
-            if (pos < 0) fl |= SPEC_DEV_BAD_LENGTH;
-            p.bonus_token[b] = (pos < 0) ? -1 : (kSample ? ctl.cand : ctl.A[0]);
-        }
-        if (fl) atomicOr(p.status, fl);
-        if (!kBonus) last = (atom_add_acq_rel(&p.ws_counter[b], 1u) == static_cast<unsigned>(U - 1)) ? 1 : 0;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __syncwarp();
     if (MODE == kLinearSample || MODE == kLinearGreedy) {
         const bool has_bonus = p.u_bonus != nullptr;
         int j = K;
@@ -460,20 +436,19 @@ __device__ void publish(const Params &p, Ctl &ctl, int s, unsigned char *stage, 
             p.accept_len[b] = j;
             p.num_emitted[b] = j + (has_bonus ? 1 : 0);
         }
-        // leave this sequence's workspace entries zero for the next call,
-        // whatever (B, K) that call uses the workspace with
+        // leave this sequence's workspace entries zero for the next call
         __syncwarp();
         if (MODE == kLinearSample)
             for (int i = lane; i < K; i += 32) p.ws_acc[static_cast<size_t>(b) * K + i] = 0;
         for (int i = lane; i < U; i += 32) p.ws_val[static_cast<size_t>(b) * U + i] = 0;
         if (lane == 0) {
             p.ws_first[b] = 0;
-            p.ws_counter[b] = 0u;
+            p.ws_seq_cnt[b] = 0u;
         }
     } else if (MODE == kTreeGreedy) {
-        // stage the tree of this sequence in the current stage buffer (no longer read)
+        // stage the tree of this sequence in the control warp's scratch area
         const int N = U;
-        int *par_s = reinterpret_cast<int *>(stage);
+        int *par_s = reinterpret_cast<int *>(stage_ints);
         int *tok_s = par_s + N;
         int *am_s = tok_s + N;
         for (int cidx = lane; cidx < N; cidx += 32) {
@@ -518,7 +493,7 @@ __device__ void publish(const Params &p, Ctl &ctl, int s, unsigned char *stage, 
             pn[0] = 0;
             ot[depth] = am_s[cur];
             p.accept_len[b] = depth;
-            p.ws_counter[b] = 0u;
+            p.ws_seq_cnt[b] = 0u;
         }
         for (int i = depth + 1 + lane; i <= D; i += 32) {
             ot[i] = -1;
@@ -528,11 +503,256 @@ __device__ void publish(const Params &p, Ctl &ctl, int s, unsigned char *stage, 
     }
 }
 
-// ================================================================ kernel
+// One more unit of sequence b is finished; emit the sequence if it was the last.
 template <int EB, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) spec_verify_kernel(const Params p) {
+__device__ void unit_finished(const Params &p, int b, long long *scratch, int lane) {
+    int last = 0;
+    if (lane == 0)
+        last = (atom_add_acq_rel(&p.ws_seq_cnt[b], 1u) == static_cast<unsigned>(p.units_per_seq - 1)) ? 1 : 0;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+        __syncwarp();
+        emit_sequence<EB, MODE>(p, b, scratch, lane);
+    }
+}
+
+// Extra-token draw finished: record the token.
+template <int EB, int MODE>
+__device__ void token_drawn(const Params &p, const Job &jb, int token, long long *scratch, int lane) {
+    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
+    if (kBonus) {
+        if (lane == 0) p.bonus_token[jb.b] = token;
+        return;
+    }
+    if (lane == 0) p.ws_val[static_cast<size_t>(jb.b) * p.units_per_seq + jb.pos] = token;
+    __syncwarp();
+    unit_finished<EB, MODE>(p, jb.b, scratch, lane);
+}
+
+// All residual tiles of job `jb` are reduced: locate the token.  Returns -1
+// when the weights summed to zero (the caller then retries with p alone).
+template <int EB, int MODE>
+__device__ int select_token(const Params &p, const Job &jb, const long long *csum, int lane) {
+    constexpr int G = Elt<EB>::G;
+    const int n = p.S * p.cpt;
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    long long mine = 0;
+    for (int i = lo; i < hi; ++i) mine += csum[i];
+    long long incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const long long tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (tot <= 0) return -1;
+    const long long target = static_cast<long long>(static_cast<double>(jb.ub) * static_cast<double>(tot));
+    // the chunk holding the target: first lane, then first chunk in that lane's block
+    const unsigned bl = __ballot_sync(0xffffffffu, incl > target);
+    const int ol = __ffs(bl) - 1;
+    long long acc = __shfl_sync(0xffffffffu, incl - mine, ol);
+    int chunk = -1;
+    if (lane == ol) {
+        long long a = acc;
+        for (int i = lo; i < hi; ++i) {
+            if (a + csum[i] > target) {
+                chunk = i;
+                break;
+            }
+            a += csum[i];
+        }
+        acc = a;
+    }
+    chunk = __shfl_sync(0xffffffffu, chunk, ol);
+    acc = __shfl_sync(0xffffffffu, acc, ol);
+    const long long rem = target - acc;  // 0 <= rem < csum[chunk]
+    // rescan that chunk from global memory, element by element, with the same weights
+    const int k = chunk / p.cpt;
+    const int cc = chunk - k * p.cpt;
+    const int s0 = min(p.V, k * p.slice_len);
+    const int s1 = min(p.V, s0 + p.slice_len);
+    const UnitRows ur = unit_rows<EB, MODE>(p, jb.unit);
+    const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, nullptr);
+    const bool pair = !jb.tailw;
+    long long q[2];
+    float w[2][G];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int g = cc * kChunk + h * 32 + lane;
+        float sw = 0.f;
+#pragma unroll
+        for (int e = 0; e < G; ++e) {
+            const int v = gt.vbase + g * G + e;
+            float we = 0.f;
+            if (g < gt.ngran && v >= s0 && v < s1) {
+                const float t = Elt<EB>::gload(ur.row[0] + static_cast<size_t>(v) * EB);
+                const float d = pair ? Elt<EB>::gload(ur.row[1] + static_cast<size_t>(v) * EB) : 0.f;
+                we = elem_weight(t, d, pair, jb.Mt, jb.Md, jb.invSt, jb.invSd, p.c);
+            }
+            w[h][e] = we;
+            sw += we;
+        }
+        q[h] = fixq(sw);
+    }
+    // inclusive prefix over the chunk's 64 groups (first half, then second half)
+    long long i0 = q[0], i1 = q[1];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long y0 = __shfl_up_sync(0xffffffffu, i0, off);
+        const long long y1 = __shfl_up_sync(0xffffffffu, i1, off);
+        if (lane >= off) {
+            i0 += y0;
+            i1 += y1;
+        }
+    }
+    const long long t0 = __shfl_sync(0xffffffffu, i0, 31);
+    i1 += t0;
+    unsigned bh = __ballot_sync(0xffffffffu, i0 > rem);
+    int half = 0;
+    if (!bh) {
+        bh = __ballot_sync(0xffffffffu, i1 > rem);
+        half = 1;
+    }
+    int token = -1;
+    if (bh) {
+        const int gl = __ffs(bh) - 1;
+        const long long excl = __shfl_sync(0xffffffffu, half ? (i1 - q[1]) : (i0 - q[0]), gl);
+        if (lane == gl) {
+            const int g = cc * kChunk + half * 32 + lane;
+            // the same weights, summed in the same order as the group sum
+            float cum = 0.f;
+            int esel = -1;
+#pragma unroll
+            for (int e = 0; e < G; ++e) {
+                cum += half ? w[1][e] : w[0][e];
+                if (esel < 0 && excl + fixq(cum) > rem) esel = e;
+            }
+            token = gt.vbase + g * G + (esel < 0 ? G - 1 : esel);
+        }
+        token = __shfl_sync(0xffffffffu, token, gl);
+    }
+    return token < 0 ? 0 : token;
+}
+
+// ====================================================== compute-warp side
+template <int EB, int MODE>
+__device__ void compute_stats(const Params &p, Ctl &ctl, unsigned char *stage, const StageMeta &m, int s,
+                              int ct, int cw, int lane) {
     constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
     constexpr int G = Elt<EB>::G;
+    const UnitRows ur = unit_rows<EB, MODE>(p, m.unit);
+    const int s0 = min(p.V, m.k * p.slice_len);
+    const int s1 = min(p.V, s0 + p.slice_len);
+    const float c = p.c;
+    // the draft token of a pair unit: its two logits are read here if this slice holds it
+    int x = -1;
+    if (MODE == kLinearSample && m.nrows == 2 && ct == 0) x = p.tokens[static_cast<size_t>(m.b) * p.K + m.pos];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+        if (r >= m.nrows) continue;
+        const RowGeo g = make_geo<EB>(ur.row[r], s0, s1, stage + r * p.row_buf_bytes);
+        if (kSample) {
+            const float mp = Elt<EB>::group_max(g.buf, ct, g.ngran, kComputeThreads);
+            float sa = 0.f, sb = 0.f;
+            if (mp != neg_inf()) {
+                int gg = ct;
+                for (; gg + kComputeThreads < g.ngran; gg += 2 * kComputeThreads) {
+                    float va[G], vb[G];
+                    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
+                    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * (gg + kComputeThreads)), vb);
+#pragma unroll
+                    for (int k = 0; k < G; ++k) {
+                        sa += ptx::ex2((va[k] - mp) * c);
+                        sb += ptx::ex2((vb[k] - mp) * c);
+                    }
+                }
+                if (gg < g.ngran) {
+                    float va[G];
+                    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
+#pragma unroll
+                    for (int k = 0; k < G; ++k) sa += ptx::ex2((va[k] - mp) * c);
+                }
+            }
+            // warp: the max first, then one rescale per lane and a plain sum
+            float wmax = mp;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
+            float sum = sa + sb;
+            if (mp != wmax) sum *= ptx::ex2((mp - wmax) * c);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) {
+                ctl.wm[s][r][cw] = wmax;
+                ctl.wsum[s][r][cw] = sum;
+            }
+        } else {
+            float bv = neg_inf();
+            int bi = INT_MAX;
+            for (int gg = ct; gg < g.ngran; gg += kComputeThreads) {
+                float va[G];
+                Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
+#pragma unroll
+                for (int k = 0; k < G; ++k)
+                    if (va[k] > bv) {
+                        bv = va[k];
+                        bi = g.vbase + gg * G + k;
+                    }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                merge_vi(bv, bi, __shfl_xor_sync(0xffffffffu, bv, off), __shfl_xor_sync(0xffffffffu, bi, off));
+            if (lane == 0) {
+                ctl.wm[s][r][cw] = bv;
+                ctl.wi[s][r][cw] = bi;
+            }
+        }
+    }
+    if (MODE == kLinearSample && ct == 0) {
+        int has = 0;
+        float2 xv = make_float2(0.f, 0.f);
+        if (m.nrows == 2 && x >= s0 && x < s1) {
+            const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, stage);
+            const RowGeo gd = make_geo<EB>(ur.row[1], s0, s1, stage + p.row_buf_bytes);
+            xv = make_float2(Elt<EB>::load(gt.buf + (x - gt.vbase) * EB), Elt<EB>::load(gd.buf + (x - gd.vbase) * EB));
+            has = 1;
+        }
+        ctl.xval[s] = xv;
+        ctl.xhas[s] = has;
+    }
+}
+
+// Residual tile: exact int64 weight sums per chunk of 64 groups.
+template <int EB, int MODE>
+__device__ void compute_resid(const Params &p, unsigned char *stage, const StageMeta &m, long long *csum, int cw,
+                              int lane) {
+    const UnitRows ur = unit_rows<EB, MODE>(p, m.unit);
+    const int s0 = min(p.V, m.k * p.slice_len);
+    const int s1 = min(p.V, s0 + p.slice_len);
+    const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, stage);
+    const RowGeo gd = make_geo<EB>(ur.row[1], s0, s1, stage + p.row_buf_bytes);
+    const bool pair = !m.tailw;
+    const bool same_phase =
+        ((reinterpret_cast<uintptr_t>(ur.row[0]) - reinterpret_cast<uintptr_t>(ur.row[1])) & 15u) == 0;
+    for (int ch = cw; ch < p.cpt; ch += kComputeWarps) {
+        long long q = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int g = ch * kChunk + h * 32 + lane;
+            if (g < gt.ngran)
+                q += fixq(group_weight<EB>(gt, gd, pair, same_phase, g, s0, s1, m.Mt, m.Md, m.invSt, m.invSd, p.c));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
+        if (lane == 0) csum[m.k * p.cpt + ch] = q;
+    }
+}
+
+// ================================================================ kernel
+template <int EB, int MODE>
+__global__ void __maxnreg__(112) spec_verify_kernel(const Params p) {
+    constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
+    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
 
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ Ctl ctl;
@@ -540,390 +760,455 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_kernel(const Params p
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const bool is_ctrl = (warp == 0);
-    const int ct = tid - 32;  // compute-thread index (compute warps only)
-    const int cw = warp - 1;  // compute-warp index
-    const uint32_t crank = ptx::cluster_ctarank();
-    const uint32_t csize = ptx::cluster_nctarank();
-    const int cid = static_cast<int>(ptx::cluster_id_x());
-    const int ncl = static_cast<int>(gridDim.x / csize);
-    const int V = p.V, K = p.K;
-    const float c = p.c;
     const int nstage = p.nstage;
-    const int n_my = (p.n_units > cid) ? (p.n_units - cid + ncl - 1) / ncl : 0;
-    const int s0 = min(V, static_cast<int>(crank) * p.slice_len);
-    const int s1 = min(V, s0 + p.slice_len);
-    float *wgs = reinterpret_cast<float *>(dsm + static_cast<size_t>(nstage) * p.stage_bytes);
+    // after the stages: per-job residual chunk sums (sampling), or the tree-walk scratch
+    long long *extra = reinterpret_cast<long long *>(dsm + static_cast<size_t>(nstage) * p.stage_bytes);
+    const int job_stride = p.S * p.cpt;
 
     if (tid == 0) {
-        for (int s = 0; s < nstage; ++s) ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 2);
+        for (int s = 0; s < nstage; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 2);
+            ptx::mbar_init(ptx::smem_addr(&ctl.done[s]), kComputeWarps);
+        }
         ptx::fence_mbar_init();
-        ctl.flags = 0;
         ctl.timed_out = 0;
     }
     __syncthreads();
-    if (is_ctrl)
-        for (int it = 0; it < nstage - 1 && it < n_my; ++it)
-            prefetch_unit<EB, MODE>(p, ctl, dsm, it % nstage, cid + it * ncl, s0, s1, lane);
 
-    for (int it = 0; it < n_my; ++it) {
-        const int s = it % nstage;
-        const uint32_t ph = static_cast<uint32_t>(it / nstage) & 1u;
-        const int slot = it & 1;
-        unsigned char *stage = dsm + static_cast<size_t>(s) * p.stage_bytes;
-
-        // ---- control warp: refill the ring, fetch this unit's scalars
-        int x = -1;
-        float tx = 0.f, dx = 0.f, ua = 0.f, ubv = 0.f;
-        int early_seen = 0;
-        if (is_ctrl) {
-            const int ahead = it + nstage - 1;
-            if (ahead < n_my) {
-                if (it >= 1) bar_sync(kBarStageFree, kThreads);  // compute warps are done with that stage
-                prefetch_unit<EB, MODE>(p, ctl, dsm, ahead % nstage, cid + ahead * ncl, s0, s1, lane);
+    if (warp != 0) {
+        // ===================== compute warps: reduce the stages in ring order
+        const int ct = tid - 32;
+        const int cw = warp - 1;
+        for (int it = 0;; ++it) {
+            const int s = it % nstage;
+            if (!wait_bar(ptx::smem_addr(&ctl.full[s]), static_cast<uint32_t>(it / nstage) & 1u)) {
+                ctl.timed_out = 1;
+                break;
             }
-            if (lane == 0) {
-                const int b = ctl.st_b[s];
-                const int pos = ctl.st_pos[s];
-                if (MODE == kLinearSample && pos < K) {
-                    const UnitRows ur = unit_rows<EB, MODE>(p, b, pos);
+            const StageMeta m = ctl.meta[s];
+            if (m.kind == kTileEnd) break;
+            unsigned char *stage = dsm + static_cast<size_t>(s) * p.stage_bytes;
+            if (m.kind == kTileStats)
+                compute_stats<EB, MODE>(p, ctl, stage, m, s, ct, cw, lane);
+            else if (kSample)
+                compute_resid<EB, MODE>(p, stage, m, extra + static_cast<size_t>(m.job) * job_stride, cw, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ptx::smem_addr(&ctl.done[s]));
+        }
+        return;
+    }
+
+    // ========================= control warp: stream tiles, publish, finalize
+    const long long total = static_cast<long long>(p.n_units) * p.S;
+    // tile indices from the global counter; lane 0's copies are authoritative.
+    // The next batch is requested one batch ahead, so its latency is hidden.
+    long long grab_next = 0, grab_end = 0;
+    unsigned grab_ahead = 0;
+    if (lane == 0) grab_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(p.grab));
+    bool exhausted = false;
+    int job_head = 0, job_count = 0;  // FIFO of pending draws (lane 0)
+    int handled = 0, filled = 0;      // tiles handled / tiles handed to the ring
+    bool timed_out = false;
+    // the last published run's counter increment, consumed later
+    unsigned pend_old = 0;
+    int pend_cnt = 0;
+    bool pend_valid = false;
+    StageMeta pend_m = {};
+    // the run of consecutive stats tiles of one unit merged in this CTA (lane 0)
+    int run_unit = -1, run_k0 = 0, run_cnt = 0, run_hasx = 0;
+    uint2 run_part[kMaxRows] = {};
+    float2 run_x = make_float2(0.f, 0.f);
+    StageMeta run_m = {};
+
+    // the next tile of this CTA's stream: pending draws first, then fresh tiles
+    auto next_tile = [&](StageMeta &m) -> bool {
+        int found = 0;
+        if (lane == 0) {
+            for (int q = 0; q < job_count && !found; ++q) {
+                Job &jb = ctl.jobs[(job_head + q) % kMaxJobs];
+                if (!jb.fin && jb.next_k < p.S) {
+                    m.kind = kTileResid;
+                    m.unit = jb.unit;
+                    m.k = jb.next_k++;
+                    m.job = (job_head + q) % kMaxJobs;
+                    m.tailw = jb.tailw;
+                    m.Mt = jb.Mt;
+                    m.invSt = jb.invSt;
+                    m.Md = jb.Md;
+                    m.invSd = jb.invSd;
+                    found = 1;
+                }
+            }
+            if (!found && !exhausted) {
+                if (grab_next >= grab_end) {
+                    grab_next = grab_ahead;
+                    grab_end = grab_next + p.grab;
+                    if (grab_next < total)
+                        grab_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(p.grab));
+                }
+                if (grab_next < total) {
+                    const long long t = grab_next++;
+                    m.kind = kTileStats;
+                    m.unit = static_cast<int>(t / p.S);
+                    m.k = static_cast<int>(t - static_cast<long long>(m.unit) * p.S);
+                    m.job = -1;
+                    m.tailw = 0;
+                    found = 1;
+                } else {
+                    exhausted = true;
+                }
+            }
+        }
+        found = __shfl_sync(0xffffffffu, found, 0);
+        if (!found) return false;
+        m.kind = __shfl_sync(0xffffffffu, m.kind, 0);
+        m.unit = __shfl_sync(0xffffffffu, m.unit, 0);
+        m.k = __shfl_sync(0xffffffffu, m.k, 0);
+        m.job = __shfl_sync(0xffffffffu, m.job, 0);
+        m.tailw = __shfl_sync(0xffffffffu, m.tailw, 0);
+        m.Mt = __shfl_sync(0xffffffffu, m.Mt, 0);
+        m.invSt = __shfl_sync(0xffffffffu, m.invSt, 0);
+        m.Md = __shfl_sync(0xffffffffu, m.Md, 0);
+        m.invSd = __shfl_sync(0xffffffffu, m.invSd, 0);
+        return true;
+    };
+    auto fill_more = [&]() {
+        while (filled < handled + nstage) {
+            StageMeta m;
+            if (!next_tile(m)) break;
+            const UnitRows ur = unit_rows<EB, MODE>(p, m.unit);
+            m.b = ur.b;
+            m.pos = ur.pos;
+            m.nrows = ur.nrows;
+            fill_stage<EB, MODE>(p, ctl, dsm, filled % nstage, m, ur, lane);
+            ++filled;
+        }
+    };
+    auto push_job = [&](const Job &jb) {
+        if (lane == 0) {
+            if (job_count < kMaxJobs) {
+                ctl.jobs[(job_head + job_count) % kMaxJobs] = jb;
+                ++job_count;
+            } else {
+                atomicOr(p.status, SPEC_DEV_TIMEOUT);  // cannot happen: at most nstage + 1 draws pend
+            }
+        }
+        __syncwarp();
+    };
+
+    // ---- this CTA finished unit m.unit: merge its S partials, decide, maybe queue a draw
+    auto finalize_unit = [&](const StageMeta &m) {
+        const int b = m.b, pos = m.pos, K = p.K;
+        // one round of loads: every partial, t(x) / d(x), the draft token and uniforms
+        float v0 = neg_inf(), s0_ = 0.f, v1 = neg_inf(), s1_ = 0.f;
+        int i0 = INT_MAX, i1 = INT_MAX;
+        for (int l = lane; l < p.S; l += 32) {
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) {
+                if (r >= m.nrows) continue;
+                uint2 *slot = &p.ws_part[(static_cast<size_t>(m.unit) * 2 + r) * p.S + l];
+                const uint2 e = __ldcg(slot);
+                if (e.y == 0u) continue;  // no run started at this slice
+                *slot = make_uint2(0u, 0u);
+                float &v = r ? v1 : v0;
+                float &sm = r ? s1_ : s0_;
+                int &ii = r ? i1 : i0;
+                if (kSample)
+                    merge_ms(v, sm, __uint_as_float(e.x), __uint_as_float(e.y), p.c);
+                else
+                    merge_vi(v, ii, __uint_as_float(e.x), static_cast<int>(e.y) - 1);
+            }
+        }
+        int x = -1, enc = 0;
+        float ua = 0.f, ub = 0.f;
+        float2 txv = make_float2(0.f, 0.f);
+        if (lane == 0) {
+            if (MODE == kLinearSample) {
+                enc = ld_relaxed(&p.ws_first[b]);
+                if (p.u_bonus) ub = p.u_bonus[b];
+                if (pos < K) {
                     x = p.tokens[static_cast<size_t>(b) * K + pos];
                     ua = p.u_accept[static_cast<size_t>(b) * K + pos];
-                    if (x >= 0 && x < V) {
-                        tx = Elt<EB>::load(ur.row[0] + static_cast<size_t>(x) * EB);
-                        dx = Elt<EB>::load(ur.row[1] + static_cast<size_t>(x) * EB);
-                    }
+                    txv = __ldcg(&p.ws_tx[m.unit]);
+                    p.ws_tx[m.unit] = make_float2(0.f, 0.f);
                 }
-                if (kSample && p.u_bonus && pos >= 0) ubv = p.u_bonus[b];
-                if (MODE == kLinearSample) {
-                    const int enc = ld_relaxed(&p.ws_first[b]);
-                    early_seen = (enc != 0 && (K + 1 - enc) < pos) ? 1 : 0;
-                }
+            } else if (MODE == kBonusSample) {
+                if (pos >= 0) ub = p.u_bonus[b];
             }
+            p.ws_unit_cnt[m.unit] = 0u;
         }
-
-        // ---- compute warps: row statistics of the stage
-        if (!is_ctrl) {
-            if (!wait_bar(ptx::smem_addr(&ctl.full[s]), ph)) ctl.timed_out = 1;
-            const int nrows = ctl.st_nrows[s];
-            const UnitRows ur = unit_rows<EB, MODE>(p, ctl.st_b[s], ctl.st_pos[s]);
+        float Mr[kMaxRows], Sr[kMaxRows];
+        int Ar[kMaxRows];
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r >= nrows) continue;
-                const RowGeo g = make_geo<EB>(ur.row[r], s0, s1, stage + r * p.row_buf_bytes);
-                if (kSample) {
-                    const float mp = Elt<EB>::granule_max(g.buf, ct, g.ngran, kComputeThreads);
-                    float sa = 0.f, sb = 0.f;
-                    if (mp != neg_inf()) {
-                        int gg = ct;
-                        for (; gg + kComputeThreads < g.ngran; gg += 2 * kComputeThreads) {
-                            float va[G], vb[G];
-                            Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
-                            Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * (gg + kComputeThreads)), vb);
+        for (int r = 0; r < kMaxRows; ++r) {
+            float v = r ? v1 : v0, sm = r ? s1_ : s0_;
+            int ii = r ? i1 : i0;
+            if (kSample) {
+                float wmax = v;
 #pragma unroll
-                            for (int k = 0; k < G; ++k) {
-                                sa += ptx::ex2((va[k] - mp) * c);
-                                sb += ptx::ex2((vb[k] - mp) * c);
-                            }
-                        }
-                        if (gg < g.ngran) {
-                            float va[G];
-                            Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
+                for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
+                if (v != wmax) sm *= ptx::ex2((v - wmax) * p.c);
 #pragma unroll
-                            for (int k = 0; k < G; ++k) sa += ptx::ex2((va[k] - mp) * c);
-                        }
+                for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
+                v = wmax;
+            } else {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    merge_vi(v, ii, __shfl_xor_sync(0xffffffffu, v, off), __shfl_xor_sync(0xffffffffu, ii, off));
+            }
+            Mr[r] = v;
+            Sr[r] = sm;
+            Ar[r] = ii;
+        }
+        uint32_t fl = 0;
+        bool finite = true;
+        if (kSample) {
+            for (int r = 0; r < m.nrows; ++r)
+                if (!(isfinite(Mr[r]) && isfinite(Sr[r]) && Sr[r] > 0.f)) finite = false;
+            if (!finite) fl |= SPEC_DEV_NONFINITE;
+        } else if (m.nrows > 0 && Ar[0] == INT_MAX) {
+            fl |= SPEC_DEV_NONFINITE;  // no element above -inf
+            Ar[0] = 0;
+        }
+        Job jb;
+        jb.unit = m.unit;
+        jb.b = b;
+        jb.pos = pos;
+        jb.nrows = m.nrows;
+        jb.next_k = 0;
+        jb.done_k = 0;
+        jb.fin = 0;
+        jb.Mt = Mr[0];
+        jb.invSt = 1.0f / Sr[0];
+        jb.Md = Mr[1];
+        jb.invSd = (m.nrows == 2) ? 1.0f / Sr[1] : 0.f;
+        jb.tailw = (m.nrows == 2) ? 0 : 1;
+        jb.ub = __shfl_sync(0xffffffffu, ub, 0);
+        int draw = 0;
+        if (lane == 0) {
+            if (MODE == kLinearSample) {
+                const int early = (enc != 0 && (K + 1 - enc) < pos) ? 1 : 0;
+                if (pos < K) {
+                    float px = 0.f, qx = 0.f, thr = 0.f;
+                    int accept = 0;
+                    if (x < 0 || x >= p.V) {
+                        fl |= SPEC_DEV_BAD_TOKEN;
+                    } else {
+                        const float tx = txv.x, dx = txv.y;
+                        px = ptx::ex2((tx - Mr[0]) * p.c) / Sr[0];
+                        qx = ptx::ex2((dx - Mr[1]) * p.c) / Sr[1];
+                        const float ratio = ptx::ex2(((tx - Mr[0]) - (dx - Mr[1])) * p.c) * (Sr[1] / Sr[0]);
+                        thr = fminf(1.0f, ratio);
+                        accept = (ua < thr) ? 1 : 0;
                     }
-                    float m = mp, sum = sa + sb;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        merge_ms(m, sum, __shfl_xor_sync(0xffffffffu, m, off),
-                                 __shfl_xor_sync(0xffffffffu, sum, off), c);
-                    if (lane == 0) {
-                        ctl.warp_m[r][cw] = m;
-                        ctl.warp_s[r][cw] = sum;
+                    p.ws_acc[static_cast<size_t>(b) * K + pos] = accept;
+                    if (p.probs) {
+                        float *pr = p.probs + (static_cast<size_t>(b) * K + pos) * 3;
+                        pr[0] = px;
+                        pr[1] = qx;
+                        pr[2] = thr;
                     }
+                    if (!accept) atomicMax(&p.ws_first[b], K + 1 - pos);
+                    draw = (!accept && p.u_bonus != nullptr && !early) ? 1 : 0;
                 } else {
-                    float bv = neg_inf();
-                    int bi = INT_MAX;
-                    for (int gg = ct; gg < g.ngran; gg += kComputeThreads) {
-                        float va[G];
-                        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
-#pragma unroll
-                        for (int k = 0; k < G; ++k)
-                            if (va[k] > bv) {
-                                bv = va[k];
-                                bi = g.vbase + gg * G + k;
-                            }
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        merge_vi(bv, bi, __shfl_xor_sync(0xffffffffu, bv, off), __shfl_xor_sync(0xffffffffu, bi, off));
-                    if (lane == 0) {
-                        ctl.warp_m[r][cw] = bv;
-                        ctl.warp_i[r][cw] = bi;
-                    }
+                    draw = (p.u_bonus != nullptr && !early) ? 1 : 0;  // tail: p_K
                 }
+                if (!finite) draw = 0;
+            } else if (MODE == kBonusSample) {
+                draw = (pos >= 0 && finite) ? 1 : 0;
+                if (pos < 0) fl |= SPEC_DEV_BAD_LENGTH;
             }
+            if (fl) atomicOr(p.status, fl);
         }
-        __syncthreads();
+        draw = __shfl_sync(0xffffffffu, draw, 0);
+        if (draw) {
+            push_job(jb);
+        } else if (MODE == kLinearGreedy || MODE == kTreeGreedy) {
+            if (lane == 0) p.ws_val[static_cast<size_t>(b) * p.units_per_seq + pos] = Ar[0];
+            __syncwarp();
+            unit_finished<EB, MODE>(p, b, extra, lane);
+        } else if (MODE == kBonusGreedy) {
+            if (lane == 0) {
+                if (pos < 0) atomicOr(p.status, SPEC_DEV_BAD_LENGTH);
+                p.bonus_token[b] = (pos < 0) ? -1 : Ar[0];
+            }
+        } else if (MODE == kBonusSample) {
+            if (lane == 0) p.bonus_token[b] = (pos < 0) ? -1 : 0;
+        } else {  // linear sampling without a draw here
+            unit_finished<EB, MODE>(p, b, extra, lane);
+        }
+    };
+    // consume the previous stats tile's counter increment (issued a tile ago)
+    auto resolve_pending = [&]() {
+        if (!pend_valid) return;
+        pend_valid = false;
+        const int last =
+            __shfl_sync(0xffffffffu, (pend_old + static_cast<unsigned>(pend_cnt) == static_cast<unsigned>(p.S)) ? 1 : 0, 0);
+        if (last) {
+            __syncwarp();
+            finalize_unit(pend_m);
+        }
+    };
 
-        // ---- control warp: CTA partial; cluster merge; decision
-        const int nrows_u = ctl.st_nrows[s];
-        if (is_ctrl) {
+    // write the current run's merged partial, count its tiles (the increment is consumed later)
+    auto publish_run = [&]() {
+        const int have = __shfl_sync(0xffffffffu, run_unit, 0);
+        if (have < 0) return;
+        resolve_pending();
+        const StageMeta rm = run_m;
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r)
+                if (r < rm.nrows) p.ws_part[(static_cast<size_t>(run_unit) * 2 + r) * p.S + run_k0] = run_part[r];
+            if (run_hasx) p.ws_tx[run_unit] = run_x;
+            pend_old = atom_add_acq_rel(&p.ws_unit_cnt[run_unit], static_cast<unsigned>(run_cnt));
+            pend_cnt = run_cnt;
+            run_unit = -1;
+        }
+        pend_valid = true;
+        pend_m = rm;
+    };
+
+    fill_more();
+    for (;;) {
+        if (filled == handled) {
+            publish_run();
+            resolve_pending();
+            fill_more();
+            if (filled == handled) break;  // nothing in flight and nothing left
+        }
+        const int s = handled % nstage;
+        if (!wait_bar(ptx::smem_addr(&ctl.done[s]), static_cast<uint32_t>(handled / nstage) & 1u)) {
+            timed_out = true;
+            break;
+        }
+        const StageMeta m = ctl.meta[s];
+        ++handled;
+        if (m.kind != kTileStats) {
+            publish_run();
+            resolve_pending();
+        }
+        if (m.kind == kTileStats) {
+            // ---- CTA partial of this tile -> workspace (the max first, then one rescale per warp)
+            uint2 part[kMaxRows];
 #pragma unroll
             for (int r = 0; r < kMaxRows; ++r) {
-                if (r >= nrows_u) continue;
-                float m = lane < kComputeWarps ? ctl.warp_m[r][lane] : neg_inf();
+                if (r >= m.nrows) continue;
+                float v = lane < kComputeWarps ? ctl.wm[s][r][lane] : neg_inf();
                 if (kSample) {
-                    float sum = lane < kComputeWarps ? ctl.warp_s[r][lane] : 0.f;
+                    float sum = lane < kComputeWarps ? ctl.wsum[s][r][lane] : 0.f;
+                    float wmax = v;
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        merge_ms(m, sum, __shfl_xor_sync(0xffffffffu, m, off),
-                                 __shfl_xor_sync(0xffffffffu, sum, off), c);
-                    if (lane == 0) {
-                        ctl.part_m[slot][r] = m;
-                        ctl.part_s[slot][r] = sum;
-                    }
+                    for (int off = 4; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
+                    if (v != wmax) sum *= ptx::ex2((v - wmax) * p.c);
+#pragma unroll
+                    for (int off = 4; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                    part[r] = make_uint2(__float_as_uint(wmax), __float_as_uint(sum));
                 } else {
-                    int i = lane < kComputeWarps ? ctl.warp_i[r][lane] : INT_MAX;
+                    int i = lane < kComputeWarps ? ctl.wi[s][r][lane] : INT_MAX;
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        merge_vi(m, i, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, i, off));
-                    if (lane == 0) {
-                        ctl.part_m[slot][r] = m;
-                        ctl.part_i[slot][r] = i;
-                    }
+                    for (int off = 4; off > 0; off >>= 1)
+                        merge_vi(v, i, __shfl_xor_sync(0xffffffffu, v, off), __shfl_xor_sync(0xffffffffu, i, off));
+                    part[r] = make_uint2(__float_as_uint(v), static_cast<unsigned>(i) + 1u);  // +1: never 0
                 }
             }
-            if (lane == 0) ctl.part_flag[slot] = early_seen;
-        }
-        ptx::cluster_sync();
-        if (is_ctrl) {
-            int early = 0;
-            if (lane < static_cast<int>(csize))
-                early = ptx::ld_dsmem_s32(ptx::mapa(ptx::smem_addr(&ctl.part_flag[slot]), lane));
-            early = __any_sync(0xffffffffu, early != 0) ? 1 : 0;
+            const int has_x = (MODE == kLinearSample) ? ctl.xhas[s] : 0;
+            const float2 xv = ctl.xval[s];
+            fill_more();  // refill first: the publication below waits on its own stores
+            const int same = __shfl_sync(0xffffffffu, (run_unit == m.unit && run_k0 + run_cnt == m.k) ? 1 : 0, 0);
+            if (!same) publish_run();
+            if (lane == 0) {
+                if (!same) {
+                    run_unit = m.unit;
+                    run_k0 = m.k;
+                    run_cnt = 0;
+                    run_hasx = 0;
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r >= nrows_u) continue;
-                float m = neg_inf(), sum = 0.f;
-                int i = INT_MAX;
-                if (lane < static_cast<int>(csize)) {
-                    m = ptx::ld_dsmem_f32(ptx::mapa(ptx::smem_addr(&ctl.part_m[slot][r]), lane));
-                    if (kSample)
-                        sum = ptx::ld_dsmem_f32(ptx::mapa(ptx::smem_addr(&ctl.part_s[slot][r]), lane));
-                    else
-                        i = ptx::ld_dsmem_s32(ptx::mapa(ptx::smem_addr(&ctl.part_i[slot][r]), lane));
-                }
+                    for (int r = 0; r < kMaxRows; ++r) run_part[r] = part[r];
+                } else {
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    if (kSample)
-                        merge_ms(m, sum, __shfl_xor_sync(0xffffffffu, m, off),
-                                 __shfl_xor_sync(0xffffffffu, sum, off), c);
-                    else
-                        merge_vi(m, i, __shfl_xor_sync(0xffffffffu, m, off), __shfl_xor_sync(0xffffffffu, i, off));
+                    for (int r = 0; r < kMaxRows; ++r) {
+                        if (r >= m.nrows) continue;
+                        float v = __uint_as_float(run_part[r].x);
+                        if (kSample) {
+                            float sm = __uint_as_float(run_part[r].y);
+                            merge_ms(v, sm, __uint_as_float(part[r].x), __uint_as_float(part[r].y), p.c);
+                            run_part[r] = make_uint2(__float_as_uint(v), __float_as_uint(sm));
+                        } else {
+                            int ii = static_cast<int>(run_part[r].y) - 1;
+                            merge_vi(v, ii, __uint_as_float(part[r].x), static_cast<int>(part[r].y) - 1);
+                            run_part[r] = make_uint2(__float_as_uint(v), static_cast<unsigned>(ii) + 1u);
+                        }
+                    }
                 }
+                run_cnt += 1;
+                if (has_x) {
+                    run_hasx = 1;
+                    run_x = xv;
+                }
+            }
+            if (!same) run_m = m;
+        } else if (kSample) {
+            // ---- a residual tile of a pending draw is reduced
+            Job jb = ctl.jobs[m.job];
+            __syncwarp();
+            int finished = 0;
+            if (lane == 0) {
+                ctl.jobs[m.job].done_k += 1;
+                finished = (ctl.jobs[m.job].done_k == p.S) ? 1 : 0;
+            }
+            finished = __shfl_sync(0xffffffffu, finished, 0);
+            if (!finished) {
+                fill_more();
+                continue;
+            }
+            __syncwarp();
+            const int token = select_token<EB, MODE>(p, jb, extra + static_cast<size_t>(m.job) * job_stride, lane);
+            if (token < 0 && !jb.tailw) {
+                // the residual vanished through rounding: draw from p_j instead
                 if (lane == 0) {
-                    ctl.M[r] = m;
-                    ctl.S[r] = sum;
-                    ctl.A[r] = i;
+                    atomicOr(p.status, SPEC_DEV_ZERO_RESIDUAL);
+                    ctl.jobs[m.job].tailw = 1;
+                    ctl.jobs[m.job].next_k = 0;
+                    ctl.jobs[m.job].done_k = 0;
+                }
+                __syncwarp();
+                fill_more();
+                continue;
+            }
+            // the draw is done; drop finished draws from the head of the FIFO
+            if (lane == 0) {
+                ctl.jobs[m.job].fin = 1;
+                while (job_count > 0 && ctl.jobs[job_head].fin) {
+                    job_head = (job_head + 1) % kMaxJobs;
+                    --job_count;
                 }
             }
             __syncwarp();
-            if (lane == 0) {
-                const int pos = ctl.st_pos[s];
-                const int b = ctl.st_b[s];
-                uint32_t fl = 0;
-                int do_resid = 0, accept = 1, tailw = 0;
-                bool finite = true;
-                if (kSample) {
-                    for (int r = 0; r < nrows_u; ++r)
-                        if (!(isfinite(ctl.M[r]) && isfinite(ctl.S[r]) && ctl.S[r] > 0.f)) finite = false;
-                    if (!finite) fl |= SPEC_DEV_NONFINITE;
-                } else if (nrows_u > 0 && ctl.A[0] == INT_MAX) {
-                    fl |= SPEC_DEV_NONFINITE;  // no element above -inf
-                    ctl.A[0] = 0;
-                }
-                if (MODE == kLinearSample) {
-                    if (pos < K) {
-                        float px = 0.f, qx = 0.f, thr = 0.f;
-                        if (x < 0 || x >= V) {
-                            fl |= SPEC_DEV_BAD_TOKEN;
-                            accept = 0;
-                        } else {
-                            const float Mt = ctl.M[0], St = ctl.S[0], Md = ctl.M[1], Sd = ctl.S[1];
-                            px = ptx::ex2((tx - Mt) * c) / St;
-                            qx = ptx::ex2((dx - Md) * c) / Sd;
-                            const float ratio = ptx::ex2(((tx - Mt) - (dx - Md)) * c) * (Sd / St);
-                            thr = fminf(1.0f, ratio);
-                            accept = (ua < thr) ? 1 : 0;
-                        }
-                        ctl.px = px;
-                        ctl.qx = qx;
-                        ctl.thr = thr;
-                        // later positions of this sequence may skip drawing a candidate
-                        if (!accept && crank == 0) atomicMax(&p.ws_first[b], K + 1 - pos);
-                        do_resid = (!accept && p.u_bonus != nullptr && !early) ? 1 : 0;
-                    } else {
-                        do_resid = (p.u_bonus != nullptr && !early) ? 1 : 0;
-                        tailw = 1;
-                    }
-                } else if (MODE == kBonusSample) {
-                    do_resid = (pos >= 0) ? 1 : 0;
-                    tailw = (pos == K) ? 1 : 0;
-                }
-                if (!finite) do_resid = 0;
-                ctl.do_resid = do_resid;
-                ctl.tail_weights = tailw;
-                ctl.accept = accept;
-                ctl.flags = fl;
-                ctl.publisher = 0;
-                ctl.cand = 0;
-            }
-        }
-        __syncthreads();
-
-        if (kSample && ctl.do_resid) {
-            // ================= extra token from the resident rows =================
-            const UnitRows ur = unit_rows<EB, MODE>(p, ctl.st_b[s], ctl.st_pos[s]);
-            const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, stage);
-            const RowGeo gd = make_geo<EB>(ur.row[1], s0, s1, stage + p.row_buf_bytes);
-            const bool same_phase =
-                ((reinterpret_cast<uintptr_t>(ur.row[0]) - reinterpret_cast<uintptr_t>(ur.row[1])) & 15u) == 0;
-            const float Mt = ctl.M[0], Md = ctl.M[1];
-            const float invSt = 1.0f / ctl.S[0];
-            const float invSd = (nrows_u == 2) ? 1.0f / ctl.S[1] : 0.f;
-            const int ngran = gt.ngran;
-            const int seg = (ngran + kComputeThreads - 1) / kComputeThreads;
-            const int sg0 = min(ngran, max(ct, 0) * seg);
-            const int sg1 = min(ngran, sg0 + seg);
-            long long segq = 0, incl = 0;
-            for (;;) {
-                const bool pair = (ctl.tail_weights == 0);
-                if (!is_ctrl) {
-                    // weights per 16-byte group, then exact per-thread segment sums in element order
-                    for (int g = ct; g < ngran; g += kComputeThreads) {
-                        float w[G];
-                        granule_weights<EB>(gt, gd, pair, same_phase, g, s0, s1, Mt, Md, invSt, invSd, c, w);
-                        float sw = 0.f;
-#pragma unroll
-                        for (int k = 0; k < G; ++k) sw += w[k];
-                        wgs[g] = sw;
-                    }
-                    bar_sync(kBarCompute, kComputeThreads);
-                    segq = 0;
-                    for (int g = sg0; g < sg1; ++g) segq += fixq(wgs[g]);
-                    long long xs = segq;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const long long y = __shfl_up_sync(0xffffffffu, xs, off);
-                        if (lane >= off) xs += y;
-                    }
-                    if (lane == 31) ctl.warp_tot[cw] = xs;
-                    bar_sync(kBarCompute, kComputeThreads);
-                    long long offs = 0;
-                    for (int w2 = 0; w2 < cw; ++w2) offs += ctl.warp_tot[w2];
-                    incl = offs + xs;
-                    ctl.incl[ct] = incl;
-                    if (ct == kComputeThreads - 1) ctl.part_w[slot] = incl;
-                }
-                __syncthreads();
-                ptx::cluster_sync();
-                if (is_ctrl) {
-                    // cluster-wide cumulative weight, rank by rank (exact integers)
-                    const long long wk = (lane < static_cast<int>(csize))
-                                             ? ptx::ld_dsmem_s64(ptx::mapa(ptx::smem_addr(&ctl.part_w[slot]), lane))
-                                             : 0;
-                    long long tot = 0;
-                    for (int k = 0; k < static_cast<int>(csize); ++k) tot += __shfl_sync(0xffffffffu, wk, k);
-                    const float ub = __shfl_sync(0xffffffffu, ubv, 0);
-                    const long long target = static_cast<long long>(static_cast<double>(ub) * static_cast<double>(tot));
-                    long long acc = 0, pre = 0;
-                    int owner = -1;
-                    for (int k = 0; k < static_cast<int>(csize); ++k) {
-                        const long long w = __shfl_sync(0xffffffffu, wk, k);
-                        if (owner < 0 && acc + w > target) {
-                            owner = k;
-                            pre = acc;
-                        }
-                        acc += w;
-                    }
-                    if (lane == 0) {
-                        const int retry = (tot <= 0 && ctl.tail_weights == 0) ? 1 : 0;
-                        ctl.retry = retry;
-                        if (retry) {  // the residual vanished through rounding: draw from p_j instead
-                            ctl.tail_weights = 1;
-                            ctl.flags |= SPEC_DEV_ZERO_RESIDUAL;
-                        }
-                        ctl.owner_rank = owner;
-                        ctl.tlocal = target - pre;
-                        ctl.publisher = owner < 0 ? 0 : owner;
-                    }
-                }
-                __syncthreads();
-                if (!ctl.retry) break;
-                ptx::cluster_sync();  // every CTA has read this parity's part_w before it is rewritten
-            }
-            const bool pair = (ctl.tail_weights == 0);
-            if (static_cast<int>(crank) == ctl.owner_rank) {
-                if (!is_ctrl) {
-                    // the first thread whose inclusive weight exceeds the target owns the token
-                    const long long tl = ctl.tlocal;
-                    const unsigned bal = __ballot_sync(0xffffffffu, segq > 0 && incl > tl);
-                    if (lane == 0) ctl.warp_first[cw] = bal ? __ffs(bal) - 1 : 32;
-                    bar_sync(kBarCompute, kComputeThreads);
-                    int owner_t = -1;
-                    for (int w2 = 0; w2 < kComputeWarps && owner_t < 0; ++w2)
-                        if (ctl.warp_first[w2] < 32) owner_t = w2 * 32 + ctl.warp_first[w2];
-                    if (ct == owner_t) {
-                        long long acc = (ct == 0) ? 0 : ctl.incl[ct - 1];
-                        int gsel = -1;
-                        for (int g = sg0; g < sg1; ++g) {
-                            const long long q = fixq(wgs[g]);
-                            if (q > 0 && acc + q > tl) {
-                                gsel = g;
-                                break;
-                            }
-                            acc += q;
-                        }
-                        int token = 0;
-                        if (gsel >= 0) {
-                            // same weights, same fp32 summation order as the group sum
-                            float w[G];
-                            granule_weights<EB>(gt, gd, pair, same_phase, gsel, s0, s1, Mt, Md, invSt, invSd, c, w);
-                            float cum = 0.f;
-                            int ksel = G - 1;
-                            for (int k = 0; k < G; ++k) {
-                                cum += w[k];
-                                if (acc + fixq(cum) > tl) {
-                                    ksel = k;
-                                    break;
-                                }
-                            }
-                            token = gt.vbase + gsel * G + ksel;
-                        }
-                        ctl.cand = token;
-                    }
-                }
-                __syncthreads();
-            }
-        }
-
-        // ---- the compute warps are done with this stage; publish
-        if (!is_ctrl && it + nstage < n_my) bar_arrive(kBarStageFree, kThreads);
-        if (is_ctrl && static_cast<int>(crank) == ctl.publisher) publish<EB, MODE>(p, ctl, s, stage, lane);
-    }
-
-    // no CTA leaves while a peer may still read its control block
-    ptx::cluster_sync();
-    if (tid == 0 && ctl.timed_out) {
-        atomicOr(p.status, SPEC_DEV_TIMEOUT);
-        // wait (bounded) for copies that may still be in flight into any stage
-        for (int s = 0; s < nstage && s < n_my; ++s) {
-            const int last_it = s + ((n_my - 1 - s) / nstage) * nstage;
-            wait_bar(ptx::smem_addr(&ctl.full[s]), static_cast<uint32_t>(last_it / nstage) & 1u);
+            token_drawn<EB, MODE>(p, jb, token < 0 ? 0 : token, extra, lane);
+            fill_more();
         }
     }
+
+    // ---- end of the stream: release the compute warps, account for the CTA
+    if (!timed_out) {
+        const int s = filled % nstage;
+        if (lane == 0) {
+            StageMeta e{};
+            e.kind = kTileEnd;
+            ctl.meta[s] = e;
+            mbar_arrive(ptx::smem_addr(&ctl.full[s]));
+            mbar_arrive(ptx::smem_addr(&ctl.full[s]));
+        }
+    }
+    if (lane == 0) {
+        if (timed_out || ctl.timed_out) atomicOr(p.status, SPEC_DEV_TIMEOUT);
+        if (atom_add_acq_rel(&p.ws_ctrl[1], 1u) == gridDim.x - 1) {
+            p.ws_ctrl[0] = 0u;  // the last CTA leaves the tile counter zeroed
+            p.ws_ctrl[1] = 0u;
+        }
+    }
+    (void)kBonus;
 }
 
 }  // namespace spec

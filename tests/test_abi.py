@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("spec_verify_linear", "spec_sample_bonus", "spec_verify_tree", "spec_status_string",
-              "spec_last_error", "spec_workspace_bytes_linear", "spec_workspace_bytes_tree"):
+              "spec_last_error", "spec_workspace_bytes_linear", "spec_workspace_bytes_bonus",
+              "spec_workspace_bytes_tree"):
         assert n in names
 
 
@@ -45,13 +46,19 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    assert sv.spec_workspace_bytes_linear(0, 4) == 0
-    a = sv.spec_workspace_bytes_linear(64, 4)
-    assert a >= 64 * 4 + 64 * 4 * 4 + 64 * 5 * 4 and a % 16 == 0
-    assert sv.spec_workspace_bytes_linear(128, 4) > a
-    t = sv.spec_workspace_bytes_tree(16, 64)
-    assert t >= 16 * 4 + 16 * 64 * 4
-    assert sv.spec_workspace_bytes_tree(16, 0) == 0
+    assert sv.spec_workspace_bytes_linear(0, 4, 1000, sv.SPEC_F32) == 0
+    assert sv.spec_workspace_bytes_linear(4, 4, 0, sv.SPEC_F32) == 0
+    assert sv.spec_workspace_bytes_linear(4, 4, 1000, 9) == 0
+    a = sv.spec_workspace_bytes_linear(64, 4, 128256, sv.SPEC_BF16)
+    # counters, accept bits, values, and 8-byte partials for 16 KB slices of every row
+    slices = -(-128256 * 2 // 16384)
+    assert a >= 64 * 5 * 4 + 64 * 4 * 4 + 64 * 5 * 4 + 64 * 5 * 2 * slices * 8 and a % 16 == 0
+    assert sv.spec_workspace_bytes_linear(128, 4, 128256, sv.SPEC_BF16) > a
+    assert sv.spec_workspace_bytes_linear(64, 4, 128256, sv.SPEC_F32) > a      # twice the slices
+    t = sv.spec_workspace_bytes_tree(16, 64, 32000, sv.SPEC_F32)
+    assert t >= 16 * 64 * 4 * 2
+    assert sv.spec_workspace_bytes_tree(16, 0, 32000, sv.SPEC_F32) == 0
+    assert sv.spec_workspace_bytes_bonus(8, 1000, sv.SPEC_BF16) > 0
 
 
 FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every case below fails on the host
@@ -101,10 +108,12 @@ def test_greedy_needs_no_draft(lib):
 
 def test_bonus_and_tree_host_validation(lib):
     f = lib.spec_sample_bonus
-    assert f(FAKE, FAKE, 1, -1, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, 1, 2, 2, 10, None, FAKE, 1.0, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, 1, 2, 2, 10, FAKE, None, 1.0, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
-    assert f(FAKE, FAKE, 1, 0, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, None) == sv.SPEC_OK
+    W = 1 << 20
+    assert f(FAKE, FAKE, 1, -1, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 2, 2, 10, None, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 2, 2, 10, FAKE, None, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 2, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, None, W, None) == sv.SPEC_ERR_WORKSPACE
+    assert f(FAKE, FAKE, 1, 0, 2, 10, FAKE, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_OK
     t = lib.spec_verify_tree
     assert t(FAKE, 0, 2, 0, 10, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
     assert t(FAKE, 0, 2, 5, 10, FAKE, FAKE, -1, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG

@@ -159,7 +159,7 @@ def test_non_default_stream_and_repeat_calls_are_identical():
 
 def test_workspace_left_zeroed():
     d = rand_linear(5, 3, 3000, "f32", seed=7)
-    ws = torch.zeros(sv.spec_workspace_bytes_linear(5, 3), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(sv.spec_workspace_bytes_linear(5, 3, 3000, torch.float32), dtype=torch.uint8, device="cuda")
     sv.spec_verify_linear(d["target"], d["draft"], d["draft_tokens"], d["u_accept"], d["u_bonus"], 1.0,
                           workspace=ws)
     torch.cuda.synchronize()
