@@ -61,7 +61,7 @@ extern "C" {
 typedef enum spec_status {
     SPEC_OK = 0,
     SPEC_ERR_INVALID_ARG = 1, /* a null, misaligned or out-of-range argument */
-    SPEC_ERR_UNSUPPORTED = 2, /* valid, but beyond what this build handles (e.g. V too large) */
+    SPEC_ERR_UNSUPPORTED = 2, /* valid, but beyond what this library handles (e.g. V too large) */
     SPEC_ERR_CUDA = 3,        /* the CUDA runtime reported an error; see spec_last_error() */
     SPEC_ERR_WORKSPACE = 4    /* workspace missing, too small or misaligned */
 } spec_status;

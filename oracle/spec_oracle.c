@@ -25,7 +25,7 @@
  *     node's candidate children, and verification continues along the child
  *     that matches, until no child matches.
  *
- * Readings taken where the pages are silent (all restated in the design doc):
+ * Readings taken where the pages are silent:
  *   - accept draft token x_i iff u_i < min(1, p_i(x_i) / q_i(x_i)) (strict),
  *     with p_i = softmax(target_i / T) and q_i = softmax(draft_i / T); for
  *     finite logits both are positive, and the quotient is evaluated as
