@@ -40,7 +40,8 @@
  *   - All arithmetic on the device is fp32 (bf16 inputs are widened exactly);
  *     cumulative sums for the inverse CDF are exact int64 sums of the fp32
  *     weights of 16-byte groups of logits, in units of 2^-52.
- *   - Workspace: every entry point needs a caller-owned device workspace of
+ *   - Workspace: every entry point except spec_verify_linear_static needs a
+ *     caller-owned device workspace of
  *     spec_workspace_bytes_*() bytes, 16-byte aligned and zero-filled before
  *     its first use.  Every call leaves it zero-filled again, so one zeroing
  *     suffices for any number of calls, but one workspace must not be shared
@@ -157,6 +158,44 @@ spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B,
                              int32_t *path_nodes, int32_t *path_len, int32_t *out_tokens,
                              uint32_t *dev_status, void *workspace, size_t workspace_bytes,
                              void *stream);
+
+/*
+ * spec_verify_linear with the library's own workspace.  The pages describe no
+ * such call: it exists for callers that cannot allocate device memory at the
+ * point where they verify -- e.g. a host program embedded in an inference
+ * engine whose memory pool already owns the device, or a decode loop that must
+ * not call cudaMalloc / cudaFree between steps because cudaFree synchronises
+ * the whole device.  It allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).
+ *
+ * The workspace is one statically sized array per device, compiled into the
+ * library: SPEC_STATIC_WORKSPACE_BYTES bytes.  Shapes whose
+ * spec_workspace_bytes_linear(B, K, V, dtype) exceeds that are rejected with
+ * SPEC_ERR_WORKSPACE (spec_last_error() gives both sizes); use
+ * spec_verify_linear with a workspace of your own for those.
+ *
+ * First call on each device: it looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current; this may also load the
+ * library's kernels onto the device).  Make one call on every device you will
+ * use before you begin any stream capture on it.
+ *
+ * Every call clears the part of the array it uses with cudaMemsetAsync on
+ * `stream` before its kernel, so no earlier call's leftovers matter.  There is
+ * ONE array per device and process: calls that may overlap in time (different
+ * streams, or host threads without ordering) race on it and give wrong
+ * results.  Issue them on one stream, or use spec_verify_linear.
+ *
+ * Arguments, outputs and errors are those of spec_verify_linear, without
+ * `workspace` and `workspace_bytes`.
+ */
+#define SPEC_STATIC_WORKSPACE_BYTES (16u << 20)
+
+spec_status spec_verify_linear_static(const void *target_logits, const void *draft_logits,
+                                      spec_dtype dtype, int B, int K, int V,
+                                      const int32_t *draft_tokens, const float *u_accept,
+                                      const float *u_bonus, float temperature,
+                                      int32_t *accept_len, int32_t *out_tokens, int32_t *num_emitted,
+                                      float *probs_out, uint32_t *dev_status, void *stream);
 
 /* Static text for a status code. */
 const char *spec_status_string(spec_status status);

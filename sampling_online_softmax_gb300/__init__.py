@@ -72,6 +72,8 @@ def load_library():
         lib.spec_workspace_bytes_tree.restype = u64
         lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
         lib.spec_verify_linear.restype = i32
+        lib.spec_verify_linear_static.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P]
+        lib.spec_verify_linear_static.restype = i32
         lib.spec_sample_bonus.argtypes = [P, P, i32, i32, i32, i32, P, P, f32, P, P, P, u64, P]
         lib.spec_sample_bonus.restype = i32
         lib.spec_verify_tree.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, u64, P]
@@ -202,6 +204,44 @@ def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperatu
             _ptr(u_bonus), float(temperature), _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
             _ptr(out["num_emitted"]), _ptr(out.get("probs")), _ptr(status), _ptr(ws), ws.numel(), h)
     _check(st)
+    return out
+
+
+def spec_verify_linear_static(target, draft, draft_tokens, u_accept, u_bonus, temperature, *, out, status,
+                              stream=None):
+    """spec_verify_linear on the library's built-in per-device workspace.
+
+    For callers that must not allocate device memory during the step: nothing
+    is allocated here either, so `out` (accept_len, out_tokens, num_emitted and
+    optionally probs, as returned by spec_verify_linear) and `status` (int32 [1],
+    zeroed by the caller) must be passed in.  Calls that may overlap in time
+    share the one workspace and race; keep them on one stream.
+    """
+    lib = load_library()
+    _cuda(target, "target")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    _cuda(draft, "draft")
+    _cuda(draft_tokens, "draft_tokens", torch.int32)
+    _cuda(u_accept, "u_accept", torch.float32)
+    _cuda(u_bonus, "u_bonus", torch.float32)
+    if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
+        raise ValueError("draft must match target's dtype with shape [B, K, V]")
+    if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
+        raise ValueError("draft_tokens must be [B, K]")
+    for name in ("accept_len", "out_tokens", "num_emitted"):
+        _cuda(out[name], name, torch.int32)
+    _cuda(out.get("probs"), "probs", torch.float32)
+    _cuda(status, "status", torch.int32)
+    h, _ = _stream_handle(dev, stream)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_linear_static(
+            _ptr(target), _ptr(draft), _dtype_code(target), B, K, V, _ptr(draft_tokens), _ptr(u_accept),
+            _ptr(u_bonus), float(temperature), _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+            _ptr(out["num_emitted"]), _ptr(out.get("probs")), _ptr(status), h)
+    _check(st)
+    out["status"] = status
     return out
 
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -385,6 +386,73 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the last unit of a sequence stages parents, node tokens and argmaxes (3 * N ints)
     return eb == 4 ? launch<4, kTreeGreedy>(p, 1, N, s) : launch<2, kTreeGreedy>(p, 1, N, s);
+}
+
+// ---- spec_verify_linear_static: spec_verify_linear on a workspace compiled
+// into the library, one array per device, so the call allocates nothing.
+namespace spec {
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_ws[SPEC_STATIC_WORKSPACE_BYTES];
+
+std::atomic<void *> g_static_addr[kMaxDevices];
+std::mutex g_static_mutex;
+
+// Device address of the current device's array; looked up once per device,
+// with that device current.
+spec_status static_workspace(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_UNSUPPORTED, "device index %d", dev);
+    void *a = g_static_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        std::lock_guard<std::mutex> lock(g_static_mutex);
+        a = g_static_addr[dev].load(std::memory_order_relaxed);
+        if (!a) {
+            e = cudaGetSymbolAddress(&a, g_static_ws);
+            if (e != cudaSuccess || !a)
+                return fail(SPEC_ERR_CUDA, "cudaGetSymbolAddress of the static workspace on device %d: %s", dev,
+                            cudaGetErrorString(e));
+            g_static_addr[dev].store(a, std::memory_order_release);
+        }
+    }
+    *out = a;
+    return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace spec
+
+extern "C" spec_status spec_verify_linear_static(const void *target_logits, const void *draft_logits,
+                                                 spec_dtype dtype, int B, int K, int V,
+                                                 const int32_t *draft_tokens, const float *u_accept,
+                                                 const float *u_bonus, float temperature, int32_t *accept_len,
+                                                 int32_t *out_tokens, int32_t *num_emitted, float *probs_out,
+                                                 uint32_t *dev_status, void *stream) {
+    // Argument checks first: spec_verify_linear without a workspace enqueues
+    // nothing and reports either an argument error, SPEC_OK for an empty batch,
+    // or the missing workspace.
+    spec_status st = spec_verify_linear(target_logits, draft_logits, dtype, B, K, V, draft_tokens, u_accept, u_bonus,
+                                        temperature, accept_len, out_tokens, num_emitted, probs_out, dev_status,
+                                        nullptr, 0, stream);
+    if (st != SPEC_ERR_WORKSPACE) return st;
+    g_last_error[0] = '\0';
+    const size_t need = spec_workspace_bytes_linear(B, K, V, dtype);
+    if (need == 0 || need > static_cast<size_t>(SPEC_STATIC_WORKSPACE_BYTES))
+        return fail(SPEC_ERR_WORKSPACE,
+                    "B=%d K=%d V=%d needs %zu workspace bytes; the static workspace holds %zu "
+                    "(use spec_verify_linear with a workspace of your own)",
+                    B, K, V, need, static_cast<size_t>(SPEC_STATIC_WORKSPACE_BYTES));
+    void *ws = nullptr;
+    st = static_workspace(&ws);
+    if (st != SPEC_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(ws, 0, need, s);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaMemsetAsync of the static workspace: %s", cudaGetErrorString(e));
+    return spec_verify_linear(target_logits, draft_logits, dtype, B, K, V, draft_tokens, u_accept, u_bonus,
+                              temperature, accept_len, out_tokens, num_emitted, probs_out, dev_status, ws,
+                              static_cast<size_t>(SPEC_STATIC_WORKSPACE_BYTES), stream);
 }
 
 extern "C" const char *spec_status_string(spec_status status) {
