@@ -1,6 +1,6 @@
 // spec_verify.cu -- host side of libspecverify.so: the C ABI declared in
-// include/spec_verify.h (argument checks, workspace layout, tile and ring
-// sizing, and the launches of the kernels in verify_kernels.cuh).
+// include/spec_verify.h (argument checks, workspace layout, tiling and launch
+// shape, and the launches of the kernel in verify_kernels.cuh).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,22 +32,8 @@ spec_status fail(spec_status s, const char *fmt, ...) {
 }
 
 inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
-inline size_t round128(size_t n) { return (n + 127) / 128 * 128; }
 inline bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
-// Tiling: about kSliceBytes of each row per tile; the ring of stages takes what
-// two CTAs per SM leave.
-#ifndef SPEC_SLICE_BYTES
-#define SPEC_SLICE_BYTES (16 * 1024)
-#endif
-#ifndef SPEC_SMEM_PER_CTA
-#define SPEC_SMEM_PER_CTA (110 * 1024)
-#endif
-#ifndef SPEC_GRAB
-#define SPEC_GRAB 4
-#endif
-constexpr int kSliceBytes = SPEC_SLICE_BYTES;
-constexpr size_t kSmemPerCta = SPEC_SMEM_PER_CTA;
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -69,8 +55,8 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         g_dev[dev].sms = sms;
-        g_dev[dev].max_dyn = static_cast<size_t>(smem) > sizeof(Ctl) + 1024
-                                 ? static_cast<size_t>(smem) - sizeof(Ctl) - 1024
+        g_dev[dev].max_dyn = static_cast<size_t>(smem) > sizeof(WarpCtl) * kWarps + 1024
+                                 ? static_cast<size_t>(smem) - sizeof(WarpCtl) * kWarps - 1024
                                  : 0;
     });
     *out = g_dev[dev];
@@ -80,52 +66,78 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
     return SPEC_OK;
 }
 
-// Slices per row and slice length: a function of V and the element size only
-// (the workspace size depends on it).
+// Stats tiling: a row is read as kTileBytes windows on the 16-byte grid of
+// global memory; every row gets the same number of tiles (the count for the
+// worst alignment; a spare last window is empty).
+int stats_tiles_per_row(int V, int eb) {
+    return static_cast<int>((static_cast<long long>(V) * eb + 30 + kTileBytes - 1) / kTileBytes);
+}
+
+// Residual slices of a row: at most kResidSliceBytes each, a whole number of
+// 16-byte groups long, none empty.  A function of V and the element size only.
 struct Slicing {
-    int S;  // slices (tiles) per unit
-    int L;  // elements per slice, a multiple of 16 / eb
+    int S;  // slices per row
+    int L;  // elements per slice
 };
-Slicing slicing(int V, int eb) {
+Slicing resid_slicing(int V, int eb) {
     const int G = 16 / eb;
     const long long row_bytes = static_cast<long long>(V) * eb;
-    int S = static_cast<int>(std::max<long long>(1, (row_bytes + kSliceBytes - 1) / kSliceBytes));
+    int S = static_cast<int>(std::max<long long>(1, (row_bytes + kResidSliceBytes - 1) / kResidSliceBytes));
     int L = (V + S - 1) / S;
-    L = (L + G - 1) / G * G;
-    S = (V + L - 1) / L;  // rounding L up may leave a last slice empty: drop it
+    L = (L + G - 1) / G * G;  // still <= kResidSliceBytes / eb, a multiple of G
+    S = (V + L - 1) / L;
     return {S, L};
 }
 
-struct Shape {
-    Slicing sl;
-    int row_buf;    // bytes per row buffer
-    int stage;      // bytes per stage
-    int nstage;     // stages in the ring
-    int cpt;        // residual chunks per tile
-    size_t extra;   // bytes after the stages: residual chunk sums or tree scratch
-    size_t dyn;     // dynamic shared memory per CTA
+// Workspace layout (16-byte aligned parts):
+//   [counters: 4 u32][stats tiles per unit: n_units u32][units per sequence: B u32]
+//   [accept bits: B*K i32][argmax: n_units i32][run partials: n_units*2*S uint2]
+//   [t(x), d(x): n_units float2][draw statistics: n_units float4]
+//   [draw entries: B u32][residual tiles per entry: B u32][chunk sums: B*Sr*kCpt i64]
+struct WsLayout {
+    size_t ctrl, unit_cnt, seq_cnt, acc, val, part, tx, stats, rq, res_cnt, csum, total;
 };
+WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, bool draws) {
+    const size_t n_units = static_cast<size_t>(B) * units_per_seq;
+    WsLayout w;
+    w.ctrl = 0;
+    w.unit_cnt = 16;
+    w.seq_cnt = w.unit_cnt + align16(n_units * 4);
+    w.acc = w.seq_cnt + align16(static_cast<size_t>(B) * 4);
+    w.val = w.acc + align16(static_cast<size_t>(B) * K * 4);
+    w.part = w.val + align16(n_units * 4);
+    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
+    w.stats = w.tx + align16(n_units * 8);
+    const size_t entries = draws ? static_cast<size_t>(B) : 0;
+    w.rq = w.stats + (draws ? align16(n_units * 16) : 0);
+    w.res_cnt = w.rq + align16(entries * 4);
+    w.csum = w.res_cnt + align16(entries * 4);
+    w.total = w.csum + align16(entries * static_cast<size_t>(Sr) * kCpt * 8);
+    return w;
+}
 
-bool choose_shape(int V, int eb, int rows_alloc, bool sample, int tree_N, const DeviceInfo &di, Shape *out) {
-    Shape s;
-    s.sl = slicing(V, eb);
-    s.row_buf = static_cast<int>(round128(static_cast<size_t>(s.sl.L) * eb + 32));
-    s.stage = rows_alloc * s.row_buf;
-    const int max_groups = s.sl.L * eb / 16 + 2;
-    s.cpt = (max_groups + kChunk - 1) / kChunk;
-    s.extra = sample ? round128(static_cast<size_t>(kMaxJobs) * s.sl.S * s.cpt * 8)
-                     : round128(static_cast<size_t>(tree_N) * 12);
-    for (size_t budget : {std::min(kSmemPerCta, di.max_dyn), di.max_dyn}) {
-        int n = 0;
-        while (n < kMaxStages && s.extra + static_cast<size_t>(n + 1) * s.stage <= budget) ++n;
-        if (n >= 2) {
-            s.nstage = n;
-            s.dyn = s.extra + static_cast<size_t>(n) * s.stage;
-            *out = s;
-            return true;
-        }
-    }
-    return false;
+void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
+    p.ws_ctrl = reinterpret_cast<uint32_t *>(ws + wl.ctrl);
+    p.ws_unit_cnt = reinterpret_cast<uint32_t *>(ws + wl.unit_cnt);
+    p.ws_seq_cnt = reinterpret_cast<uint32_t *>(ws + wl.seq_cnt);
+    p.ws_acc = reinterpret_cast<int32_t *>(ws + wl.acc);
+    p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
+    p.ws_part = reinterpret_cast<uint2 *>(ws + wl.part);
+    p.ws_tx = reinterpret_cast<float2 *>(ws + wl.tx);
+    p.ws_stats = reinterpret_cast<float4 *>(ws + wl.stats);
+    p.ws_rq = reinterpret_cast<uint32_t *>(ws + wl.rq);
+    p.ws_res_cnt = reinterpret_cast<uint32_t *>(ws + wl.res_cnt);
+    p.ws_csum = reinterpret_cast<long long *>(ws + wl.csum);
+}
+
+WsLayout layout_linear(int B, int K, int V, int eb) {
+    return ws_layout(B, K, K + 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
+}
+WsLayout layout_bonus(int B, int V, int eb) {
+    return ws_layout(B, 0, 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
+}
+WsLayout layout_tree(int B, int N, int V, int eb) {
+    return ws_layout(B, 0, N, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, false);
 }
 
 // Resident blocks per SM for this kernel and shared-memory size (cached).
@@ -145,16 +157,14 @@ int blocks_per_sm(int dev, const void *kernel, size_t dyn) {
     return n;
 }
 
+// Fill in the tiling of p0 (rows_per_seq and the problem sizes already set),
+// choose the ring depth and grid, and launch.
 template <int EB, int MODE>
-spec_status launch(const Params &p0, int rows_alloc, int tree_N, cudaStream_t stream) {
+spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     DeviceInfo di;
     int dev = 0;
     spec_status st = device_info(&di, &dev);
     if (st != SPEC_OK) return st;
-    constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
-    Shape sh;
-    if (!choose_shape(p0.V, EB, rows_alloc, kSample, tree_N, di, &sh))
-        return fail(SPEC_ERR_UNSUPPORTED, "no ring of two stages fits shared memory (V=%d)", p0.V);
     auto kernel = spec_verify_kernel<EB, MODE>;
     {
         // per device and kernel, once: allow the largest dynamic shared memory
@@ -167,58 +177,42 @@ spec_status launch(const Params &p0, int rows_alloc, int tree_N, cudaStream_t st
             configured[dev] = true;
         }
     }
-    const int per_sm = blocks_per_sm(dev, reinterpret_cast<const void *>(kernel), sh.dyn);
-    if (per_sm <= 0) return fail(SPEC_ERR_UNSUPPORTED, "kernel does not fit an SM (smem=%zu)", sh.dyn);
-    const long long tiles = static_cast<long long>(p0.n_units) * sh.sl.S;
-    const long long grid = std::min<long long>(tiles, static_cast<long long>(per_sm) * di.sms);
     Params p = p0;
-    p.S = sh.sl.S;
-    p.slice_len = sh.sl.L;
-    p.row_buf_bytes = sh.row_buf;
-    p.stage_bytes = sh.stage;
-    p.nstage = sh.nstage;
-    p.cpt = sh.cpt;
-    p.grab = SPEC_GRAB;
-    spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, sh.dyn, stream>>>(p);
+    const Slicing rs = resid_slicing(p.V, EB);
+    p.S = stats_tiles_per_row(p.V, EB);
+    p.Sr = rs.S;
+    p.Lr = rs.L;
+    p.stats_tiles = static_cast<long long>(p.B) * p.rows_per_seq * p.S;
+    p.res_tiles = draws ? static_cast<long long>(p.B) * p.Sr : 0;
+    // ring depth: the deepest ring that keeps kMinCtas CTAs on an SM
+    const size_t scratch = (MODE == kTreeGreedy) ? static_cast<size_t>(kWarps) * 3 * p.units_per_seq * 4 : 0;
+    int ns = 0, per_sm = 0;
+    size_t dyn = 0;
+    for (int cand : {3, 2}) {
+        const size_t d = static_cast<size_t>(kWarps) * cand * kStageBytes + scratch;
+        if (d > di.max_dyn) continue;
+        const int b = blocks_per_sm(dev, reinterpret_cast<const void *>(kernel), d);
+        if (b >= kMinCtas || (cand == 2 && b >= 1)) {
+            ns = cand;
+            per_sm = b;
+            dyn = d;
+            break;
+        }
+    }
+    if (per_sm <= 0) return fail(SPEC_ERR_UNSUPPORTED, "kernel does not fit an SM (N=%d)", p.units_per_seq);
+    p.nstage = ns;
+    // enough CTAs for every warp to get a tile, at most what is resident at once
+    const long long want = std::max<long long>(1, (p.stats_tiles + kWarps - 1) / kWarps);
+    const long long grid = std::min<long long>(want, static_cast<long long>(per_sm) * di.sms);
+    const long long warps = grid * kWarps;
+    if (p.stats_tiles + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxGrab >= (1ll << 31))
+        return fail(SPEC_ERR_UNSUPPORTED, "too many tiles (B=%d, V=%d)", p.B, p.V);
+    spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, dyn, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
-        return fail(SPEC_ERR_CUDA, "launch (grid=%lld, stages=%d, smem=%zu): %s", grid, sh.nstage, sh.dyn,
+        return fail(SPEC_ERR_CUDA, "launch (grid=%lld, stages=%d, smem=%zu): %s", grid, ns, dyn,
                     cudaGetErrorString(e));
     return SPEC_OK;
-}
-
-// Workspace layout (16-byte aligned parts):
-//   [tile counter, CTAs finished: 2 u32][tiles done per unit: n_units u32]
-//   [units done per sequence: B u32][earliest rejection: B i32]
-//   [accept bits: B*K i32][candidate / argmax: B*U i32][partials: n_units*2*S uint2]
-//   [t(x), d(x): n_units float2]
-struct WsLayout {
-    size_t ctrl, unit_cnt, seq_cnt, first, acc, val, part, tx, total;
-};
-WsLayout ws_layout(int B, int K, int units_per_seq, int S) {
-    const size_t n_units = static_cast<size_t>(B) * units_per_seq;
-    WsLayout w;
-    w.ctrl = 0;
-    w.unit_cnt = 16;
-    w.seq_cnt = w.unit_cnt + align16(n_units * 4);
-    w.first = w.seq_cnt + align16(static_cast<size_t>(B) * 4);
-    w.acc = w.first + align16(static_cast<size_t>(B) * 4);
-    w.val = w.acc + align16(static_cast<size_t>(B) * K * 4);
-    w.part = w.val + align16(n_units * 4);
-    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
-    w.total = w.tx + align16(n_units * 8);
-    return w;
-}
-
-void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
-    p.ws_ctrl = reinterpret_cast<uint32_t *>(ws + wl.ctrl);
-    p.ws_unit_cnt = reinterpret_cast<uint32_t *>(ws + wl.unit_cnt);
-    p.ws_seq_cnt = reinterpret_cast<uint32_t *>(ws + wl.seq_cnt);
-    p.ws_first = reinterpret_cast<int32_t *>(ws + wl.first);
-    p.ws_acc = reinterpret_cast<int32_t *>(ws + wl.acc);
-    p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
-    p.ws_part = reinterpret_cast<uint2 *>(ws + wl.part);
-    p.ws_tx = reinterpret_cast<float2 *>(ws + wl.tx);
 }
 
 bool valid_temperature(float T, float *c_out) {
@@ -243,17 +237,17 @@ using namespace spec;
 
 extern "C" size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype) {
     if (B <= 0 || K < 0 || V < 1 || !valid_dtype(dtype)) return 0;
-    return ws_layout(B, K, K + 1, slicing(V, elt_bytes(dtype)).S).total;
+    return layout_linear(B, K, V, elt_bytes(dtype)).total;
 }
 
 extern "C" size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype) {
     if (B <= 0 || V < 1 || !valid_dtype(dtype)) return 0;
-    return ws_layout(B, 0, 1, slicing(V, elt_bytes(dtype)).S).total;
+    return layout_bonus(B, V, elt_bytes(dtype)).total;
 }
 
 extern "C" size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype) {
     if (B <= 0 || N < 1 || V < 1 || !valid_dtype(dtype)) return 0;
-    return ws_layout(B, 0, N, slicing(V, elt_bytes(dtype)).S).total;
+    return layout_tree(B, N, V, elt_bytes(dtype)).total;
 }
 
 extern "C" spec_status spec_verify_linear(const void *target_logits, const void *draft_logits,
@@ -279,19 +273,23 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     }
     if (!accept_len || !num_emitted || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "an output pointer is null");
     if (u_bonus && !out_tokens) return fail(SPEC_ERR_INVALID_ARG, "out_tokens is required with u_bonus");
-    if (static_cast<long long>(B) * (K + 1) > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B * (K + 1) too large");
-    const WsLayout wl = ws_layout(B, K, K + 1, slicing(V, eb).S);
+    if (static_cast<long long>(B) * (2 * K + 1) > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B * (K + 1) too large");
+    const WsLayout wl = layout_linear(B, K, V, eb);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
 
     Params p = {};
+    const size_t row_bytes = static_cast<size_t>(V) * eb;
     p.target = static_cast<const unsigned char *>(target_logits);
+    p.t_end = p.target + static_cast<size_t>(B) * (K + 1) * row_bytes;
     p.draft = static_cast<const unsigned char *>(draft_logits);
+    p.d_end = p.draft ? p.draft + static_cast<size_t>(B) * K * row_bytes : nullptr;
     p.B = B;
     p.K = K;
     p.V = V;
     p.t_rows = K + 1;
     p.units_per_seq = K + 1;
+    p.rows_per_seq = sample ? 2 * K + 1 : K + 1;
     p.n_units = B * (K + 1);
     p.c = c;
     p.tokens = draft_tokens;
@@ -304,8 +302,9 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     p.status = dev_status;
     bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sample) return eb == 4 ? launch<4, kLinearSample>(p, 2, 0, s) : launch<2, kLinearSample>(p, 2, 0, s);
-    return eb == 4 ? launch<4, kLinearGreedy>(p, 1, 0, s) : launch<2, kLinearGreedy>(p, 1, 0, s);
+    const bool draws = sample && u_bonus != nullptr;
+    if (sample) return eb == 4 ? launch<4, kLinearSample>(p, draws, s) : launch<2, kLinearSample>(p, draws, s);
+    return eb == 4 ? launch<4, kLinearGreedy>(p, false, s) : launch<2, kLinearGreedy>(p, false, s);
 }
 
 extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits, spec_dtype dtype,
@@ -314,7 +313,7 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
                                          void *workspace, size_t workspace_bytes, void *stream) {
     g_last_error[0] = '\0';
     if (!valid_dtype(dtype)) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if (B < 0 || K < 0 || V < 1) return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, K >= 0, V >= 1 (B=%d K=%d V=%d)", B, K, V);
+    if (B < 0 || K < 0 || V < 1) return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, K >= 0, V >= 1");
     float c = 0.f;
     if (!valid_temperature(temperature, &c)) return fail(SPEC_ERR_INVALID_ARG, "temperature must be finite and >= 0");
     if (B == 0) return SPEC_OK;
@@ -326,17 +325,21 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     if (sample && !u_bonus) return fail(SPEC_ERR_INVALID_ARG, "u_bonus is null");
     if (!accept_len || !bonus_token || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
     if (B > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B too large");
-    const WsLayout wl = ws_layout(B, 0, 1, slicing(V, eb).S);
+    const WsLayout wl = layout_bonus(B, V, eb);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
     Params p = {};
+    const size_t row_bytes = static_cast<size_t>(V) * eb;
     p.target = static_cast<const unsigned char *>(target_logits);
+    p.t_end = p.target + static_cast<size_t>(B) * (K + 1) * row_bytes;
     p.draft = static_cast<const unsigned char *>(draft_logits);
+    p.d_end = p.draft ? p.draft + static_cast<size_t>(B) * K * row_bytes : nullptr;
     p.B = B;
     p.K = K;
     p.V = V;
     p.t_rows = K + 1;
     p.units_per_seq = 1;
+    p.rows_per_seq = sample ? 2 : 1;
     p.n_units = B;
     p.c = c;
     p.u_bonus = u_bonus;
@@ -345,8 +348,8 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     p.status = dev_status;
     bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sample) return eb == 4 ? launch<4, kBonusSample>(p, 2, 0, s) : launch<2, kBonusSample>(p, 2, 0, s);
-    return eb == 4 ? launch<4, kBonusGreedy>(p, 1, 0, s) : launch<2, kBonusGreedy>(p, 1, 0, s);
+    if (sample) return eb == 4 ? launch<4, kBonusSample>(p, true, s) : launch<2, kBonusSample>(p, true, s);
+    return eb == 4 ? launch<4, kBonusGreedy>(p, false, s) : launch<2, kBonusGreedy>(p, false, s);
 }
 
 extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B, int N, int V,
@@ -364,16 +367,18 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     if (!parents || !node_tokens || !path_nodes || !path_len || !out_tokens || !dev_status)
         return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
     if (static_cast<long long>(B) * N > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B * N too large");
-    const WsLayout wl = ws_layout(B, 0, N, slicing(V, eb).S);
+    const WsLayout wl = layout_tree(B, N, V, eb);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
         return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
     Params p = {};
     p.target = static_cast<const unsigned char *>(target_logits);
+    p.t_end = p.target + static_cast<size_t>(B) * N * static_cast<size_t>(V) * eb;
     p.B = B;
     p.K = N;
     p.V = V;
     p.t_rows = N;
     p.units_per_seq = N;
+    p.rows_per_seq = N;
     p.n_units = B * N;
     p.tokens = node_tokens;
     p.parents = parents;
@@ -384,8 +389,8 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     p.status = dev_status;
     bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the last unit of a sequence stages parents, node tokens and argmaxes (3 * N ints)
-    return eb == 4 ? launch<4, kTreeGreedy>(p, 1, N, s) : launch<2, kTreeGreedy>(p, 1, N, s);
+    // the warp that finishes a sequence stages parents, node tokens and argmaxes (3 * N ints)
+    return eb == 4 ? launch<4, kTreeGreedy>(p, false, s) : launch<2, kTreeGreedy>(p, false, s);
 }
 
 // ---- spec_verify_linear_static: spec_verify_linear on a workspace compiled
@@ -459,7 +464,7 @@ extern "C" const char *spec_status_string(spec_status status) {
     switch (status) {
         case SPEC_OK: return "SPEC_OK";
         case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG: invalid argument";
-        case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED: valid but not supported by this build";
+        case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED: valid but not supported by this library";
         case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA: CUDA runtime error";
         case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE: workspace missing, too small or misaligned";
     }

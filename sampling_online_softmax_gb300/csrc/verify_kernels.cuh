@@ -10,30 +10,38 @@
 //   the first rejected position j, and one extra token drawn by inverse CDF
 //   from max(0, p_j - q_j) (j < K) or p_K (j == K), or argmax in greedy mode.
 //
-// How (GB300 design): a streaming reduction with no waiting between CTAs.
+// How (GB300 design): a streaming reduction in which every warp runs its own
+// pipeline and no warp waits on another while it holds unpublished work.
 //   * A "unit" is one (sequence, position): target row i with draft row i for
-//     linear sampling, otherwise one target row.  Each unit is cut into S
-//     vocabulary slices of about 16 KB per row; a "tile" is one slice of every
-//     row of one unit.  Tiles are numbered sequence-major, positions in order.
-//   * Persistent CTAs (a few per SM) take tiles dynamically from a global
-//     counter.  Each CTA has a control warp and eight compute warps.  The
-//     control warp keeps a ring of shared-memory stages full with 1-D bulk
-//     copies (cp.async.bulk, one mbarrier per stage; unaligned slice ends
-//     element-wise, padding -inf); the compute warps reduce each stage (max
-//     and exp2-sum per row, or max/argmax) and hand the per-warp results back
-//     through a second mbarrier.
-//   * The control warp writes the tile's partial to the workspace and bumps
-//     the unit's tile counter (acq_rel atomic).  The CTA that completes a unit
-//     merges its S partials, takes the acceptance decision, and -- for the
-//     first rejection (or the tail when nothing earlier rejected) -- draws the
-//     candidate extra token itself: it re-streams the unit's slices (from L2,
-//     they were just read) as residual tiles whose compute warps produce exact
-//     int64 fixed-point weight sums (units of 2^-52) per 64-group chunk, then
-//     locates the chunk by a prefix over those sums and rescans that one chunk.
-//   * The CTA that completes a sequence's last unit emits its tokens (a warp
-//     ballot finds the first rejection) and zeroes its workspace entries.
-//   * No tensor cores (nothing here is a contraction).  Every wait is bounded
-//     and reports SPEC_DEV_TIMEOUT instead of trapping.
+//     linear sampling, otherwise one target row.  Every row is cut into S
+//     tiles: 4 KB windows on the 16-byte grid of global memory, so only a
+//     row's first and last tile can hold bytes of a neighbouring row.  A batch
+//     is up to `grab` consecutive tiles of one row.
+//   * Persistent CTAs of eight warps, two per SM.  Each warp takes batches
+//     from a global counter (the next batch is requested one batch ahead) and
+//     keeps a ring of shared-memory stages filled with 1-D bulk copies
+//     (cp.async.bulk, one mbarrier per stage, a 16-byte descriptor per stage).
+//   * Row statistics live in the log2-scaled domain: every lane keeps a
+//     running (mc, s) over its logits of the batch, mc = fl(max(l) * c) and
+//     s = sum 2^(fma(l, c, -mc)), c = log2(e) / T; the inner loop is packed
+//     fp32x2 FMA/ADD plus one MUFU ex2 per logit.  Greedy lanes keep (max,
+//     lowest argmax).  The warp merges its lanes once per batch.
+//   * A warp publishes each batch's partial and adds one to the unit's batch
+//     counter with an acq_rel atomic whose result it looks at one tile later.
+//     The warp that completes a unit merges the partials and decides it; the
+//     warp that completes a sequence finds the first rejection and emits the
+//     sequence, or, when an extra token is drawn, publishes a draw entry.
+//   * A draw entry names one row pair (or the tail row) and is cut into Sr
+//     residual tiles of at most 2 KB per row.  Any warp may claim residual
+//     tiles (a second global counter); they take precedence over stats tiles,
+//     so rows are re-read while they are still in L2.  A residual tile sums
+//     the fp32 weights max(0, p - q) (or p) of every 16-byte group exactly in
+//     int64 fixed point (units of 2^-52) per 64-group chunk.  The warp that
+//     completes an entry's residual locates the token (a prefix over the
+//     chunk sums, then a rescan of one chunk) and emits the sequence.
+//   * No tensor cores (nothing here is a contraction).  A warp waits on other
+//     warps only with an empty ring and nothing unpublished; every wait is
+//     bounded and reports SPEC_DEV_TIMEOUT instead of trapping.
 #pragma once
 
 #include <climits>
@@ -44,14 +52,28 @@
 
 namespace spec {
 
-constexpr int kComputeWarps = 8;
-constexpr int kComputeThreads = kComputeWarps * 32;
-constexpr int kThreads = kComputeThreads + 32;  // warp 0 controls, warps 1..8 compute
-constexpr int kMaxRows = 2;                     // rows per unit: target, draft
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxStages = 4;
-constexpr int kMaxJobs = kMaxStages + 1;        // pending extra-token draws per CTA
-constexpr int kChunk = 64;                      // 16-byte groups per residual chunk
+#ifndef SPEC_TILE_KB
+#define SPEC_TILE_KB 8
+#endif
+#ifndef SPEC_MIN_CTAS
+#define SPEC_MIN_CTAS 1
+#endif
+constexpr int kMinCtas = SPEC_MIN_CTAS;              // CTAs resident per SM
+constexpr int kTileBytes = SPEC_TILE_KB * 1024;      // stats tile: a window of one row on the 16-byte grid
+constexpr int kResidSliceBytes = kTileBytes / 2;     // at most this many bytes of each row per residual tile
+constexpr int kRowBuf = kResidSliceBytes + 64;       // residual row buffer: a slice plus its ragged groups
+constexpr int kStageBytes = 2 * kRowBuf;
+constexpr int kChunk = 64;                           // 16-byte groups per residual chunk
+constexpr int kCpt = (kResidSliceBytes / 16 + 2 + kChunk - 1) / kChunk;  // residual chunks per tile
+static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout");
+constexpr int kMaxGrab = 32;            // stats tiles taken from the global counter at once (at most)
+constexpr int kMaxClaim = 8;            // residual tiles claimed at once (at most)
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kSpinLimit = 1u << 21;
+constexpr unsigned kFull = 0xffffffffu;
 
 enum Mode : int {
     kLinearSample = 0,
@@ -61,22 +83,28 @@ enum Mode : int {
     kBonusGreedy = 4,
 };
 
-enum TileKind : int { kTileEnd = 0, kTileStats = 1, kTileResid = 2 };
+enum TileKind : int { kTileNone = 0, kTileStats = 1, kTileResid = 2 };
+
+// A draw entry: (unit + 1) | pair | skip.
+constexpr uint32_t kRecUnit = (1u << 30) - 1;
+constexpr uint32_t kRecPair = 1u << 30;  // weights max(0, p - q); else p
+constexpr uint32_t kRecSkip = 1u << 31;  // nothing to draw (non-finite row, bad length)
 
 struct Params {
     const unsigned char *target;   // [B, t_rows, V]
     const unsigned char *draft;    // [B, K, V] (sampling) or null
+    const unsigned char *t_end;    // one past the last byte of target
+    const unsigned char *d_end;    // one past the last byte of draft
     int B, K, V;
     int t_rows;                    // target rows per sequence: K+1 (linear), N (tree)
+    int rows_per_seq;              // row slots per sequence in the stats tiling
     int units_per_seq;             // K+1 (linear), N (tree), 1 (extra token alone)
     int n_units;
-    int S;                         // tiles (slices) per unit
-    int slice_len;                 // elements per slice (multiple of 16/eb)
-    int row_buf_bytes;             // shared bytes per row buffer in a stage
-    int stage_bytes;               // shared bytes per stage
-    int nstage;                    // stages in the ring (2..kMaxStages)
-    int cpt;                       // residual chunks per tile
-    int grab;                      // tiles taken per visit to the global counter
+    int S;                         // stats tiles per row (windows of kTileBytes on the 16-byte grid)
+    int Sr, Lr;                    // residual slices per entry, elements per slice
+    int nstage;                    // stages per warp ring (2..kMaxStages)
+    long long stats_tiles;         // B * rows_per_seq * S
+    long long res_tiles;           // (draw entries: B or 0) * Sr
     float c;                       // log2(e) / T  (sampling modes)
     const int32_t *tokens;         // [B, K] draft tokens, or [B, N] node tokens
     const float *u_accept;         // [B, K]
@@ -91,58 +119,55 @@ struct Params {
     int32_t *path_nodes;           // [B, max_depth+1]
     int32_t *bonus_token;          // [B]
     uint32_t *status;              // [1]
-    uint32_t *ws_ctrl;             // [0] next tile, [1] CTAs finished
-    uint32_t *ws_unit_cnt;         // [n_units] tiles finished per unit
-    uint32_t *ws_seq_cnt;          // [B] units finished per sequence
-    int32_t *ws_first;             // [B] K + 1 - (earliest published rejection), 0 if none
+    uint32_t *ws_ctrl;             // [0] stats tiles taken, [1] CTAs finished, [2] draw entries, [3] residual tiles taken
+    uint32_t *ws_unit_cnt;         // [n_units] stats tiles published per unit
+    uint32_t *ws_seq_cnt;          // [B] units decided per sequence
     int32_t *ws_acc;               // [B*K] accept bits
-    int32_t *ws_val;               // [B*units_per_seq] candidate token / argmax
-    uint2 *ws_part;                // [n_units * 2 * S] per-tile partials
+    int32_t *ws_val;               // [B*units_per_seq] argmax per unit (greedy)
+    uint2 *ws_part;                // [n_units * 2 * S] run partials (slot = the run's first tile)
     float2 *ws_tx;                 // [n_units] target and draft logit of the draft token
+    float4 *ws_stats;              // [n_units] (MCt, 1/St, MCd, 1/Sd) of units that may draw
+    uint32_t *ws_rq;               // [B] draw entries
+    uint32_t *ws_res_cnt;          // [B] residual tiles finished per entry
+    long long *ws_csum;            // [B * Sr * kCpt] residual chunk sums
 };
 
-struct StageMeta {
-    int kind;                      // TileKind
-    int unit, k, b, pos, nrows;
-    int job, tailw;                // residual tiles: job slot, weights of p instead of max(0, p - q)
-    float Mt, invSt, Md, invSd;    // residual tiles: row statistics
-};
-
-struct Job {                       // a pending extra-token draw, private to one CTA
-    int unit, b, pos, nrows, tailw, next_k, done_k, fin;
-    float Mt, invSt, Md, invSd, ub;
-};
-
-struct __align__(16) Ctl {
-    unsigned long long full[kMaxStages];   // stage loaded (control -> compute)
-    unsigned long long done[kMaxStages];   // stage reduced (compute -> control)
-    StageMeta meta[kMaxStages];
-    float wm[kMaxStages][kMaxRows][kComputeWarps];
-    float wsum[kMaxStages][kMaxRows][kComputeWarps];
-    int wi[kMaxStages][kMaxRows][kComputeWarps];
-    float2 xval[kMaxStages];              // t(x), d(x) when the draft token lies in the stage's slice
-    int xhas[kMaxStages];
-    Job jobs[kMaxJobs];
-    int timed_out;
+// One stage's tile: {kTileStats, tile} or {kTileResid, residual tile, entry record}.
+struct __align__(16) WarpCtl {
+    unsigned long long full[kMaxStages];
+    int4 desc[kMaxStages];
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ unsigned atom_add_acq_rel(uint32_t *p, unsigned v) {
     unsigned old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
-__device__ __forceinline__ int ld_relaxed(const int32_t *p) {
-    int v;
-    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Release only: the returned count is looked at later, and only the thread
+// that completes a count takes an acquire fence before reading what it guards.
+__device__ __forceinline__ unsigned atom_add_release(uint32_t *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_relaxed(const uint32_t *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+__device__ __forceinline__ unsigned ld_acquire(const uint32_t *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // A weight in units of 2^-52: the power-of-two scaling is exact; the
 // conversion rounds only weights below 2^-29.
@@ -154,6 +179,34 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
     return false;
 }
 
+// ---- packed fp32 pairs (sm_100+ fma/add .f32x2)
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// sum + (2^x.lo, 2^x.hi) with x = fma(v, c, -mc)
+__device__ __forceinline__ unsigned long long exp_acc(unsigned long long sum, unsigned long long v,
+                                                      unsigned long long c2, unsigned long long nmc2) {
+    float a, b;
+    f2unpack(f2fma(v, c2, nmc2), a, b);
+    return f2add(sum, f2pack(ptx::ex2(a), ptx::ex2(b)));
+}
+
 // ---------------------------------------------------------------- elements
 template <int EB>
 struct Elt;
@@ -161,11 +214,16 @@ struct Elt;
 template <>
 struct Elt<4> {
     static constexpr int G = 4;  // elements per 16-byte group
+    static constexpr int P = 2;  // packed pairs per group
     __device__ __forceinline__ static void unpack(const uint4 &w, float (&v)[G]) {
         v[0] = __uint_as_float(w.x);
         v[1] = __uint_as_float(w.y);
         v[2] = __uint_as_float(w.z);
         v[3] = __uint_as_float(w.w);
+    }
+    __device__ __forceinline__ static void pairs(const uint4 &w, unsigned long long (&q)[P]) {
+        q[0] = f2pack(__uint_as_float(w.x), __uint_as_float(w.y));
+        q[1] = f2pack(__uint_as_float(w.z), __uint_as_float(w.w));
     }
     __device__ __forceinline__ static float load(const unsigned char *p) {
         return *reinterpret_cast<const float *>(p);
@@ -179,9 +237,10 @@ struct Elt<4> {
     __device__ __forceinline__ static void copy(unsigned char *dst, const unsigned char *src) {
         *reinterpret_cast<uint32_t *>(dst) = __ldg(reinterpret_cast<const uint32_t *>(src));
     }
-    __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1, int step) {
+    __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1) {
         float m = neg_inf();
-        for (int g = g0; g < g1; g += step) {
+#pragma unroll 4
+        for (int g = g0; g < g1; g += 32) {
             const uint4 w = *reinterpret_cast<const uint4 *>(buf + 16 * g);
             m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
                                fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
@@ -193,6 +252,7 @@ struct Elt<4> {
 template <>
 struct Elt<2> {
     static constexpr int G = 8;
+    static constexpr int P = 4;
     __device__ __forceinline__ static void unpack(const uint4 &w, float (&v)[G]) {
         v[0] = __uint_as_float(w.x << 16);
         v[1] = __uint_as_float(w.x & 0xffff0000u);
@@ -202,6 +262,12 @@ struct Elt<2> {
         v[5] = __uint_as_float(w.z & 0xffff0000u);
         v[6] = __uint_as_float(w.w << 16);
         v[7] = __uint_as_float(w.w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static void pairs(const uint4 &w, unsigned long long (&q)[P]) {
+        q[0] = f2pack(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+        q[1] = f2pack(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+        q[2] = f2pack(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+        q[3] = f2pack(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
     }
     __device__ __forceinline__ static float load(const unsigned char *p) {
         return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16);
@@ -215,9 +281,10 @@ struct Elt<2> {
     __device__ __forceinline__ static void copy(unsigned char *dst, const unsigned char *src) {
         *reinterpret_cast<uint16_t *>(dst) = __ldg(reinterpret_cast<const unsigned short *>(src));
     }
-    __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1, int step) {
+    __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1) {
         uint32_t m = 0xff80ff80u;  // (-inf, -inf)
-        for (int g = g0; g < g1; g += step) {
+#pragma unroll 4
+        for (int g = g0; g < g1; g += 32) {
             const uint4 w = *reinterpret_cast<const uint4 *>(buf + 16 * g);
             m = ptx::bmax2(m, ptx::bmax2(ptx::bmax2(w.x, w.y), ptx::bmax2(w.z, w.w)));
         }
@@ -226,52 +293,68 @@ struct Elt<2> {
 };
 
 // ------------------------------------------------------------ row geometry
-// A slice [s0, s1) of one row, mirrored in shared memory 16-byte group by
-// group: buffer byte k holds global byte (glo + k), glo = 16-byte floor of the
-// slice start.  Groups [hg, hg + nfull) arrive by bulk copy; partial groups at
-// either end are filled element-wise, with -inf outside the slice.
-struct RowGeo {
-    const unsigned char *glo;  // global address of buffer byte 0
-    unsigned char *buf;        // shared buffer (generic pointer)
-    int ngran;                 // 16-byte groups in the buffer
-    int hg;                    // 1 if group 0 is partial (and there are full groups)
-    int nfull;                 // groups copied in bulk
-    int vbase;                 // element index of buffer byte 0 (may be negative)
-    int a0off, a1off;          // byte offsets of the slice's first / one-past-last element
+// A slice [s0, s1) of one row is mirrored in a shared buffer 16-byte group by
+// group: buffer byte k holds global byte glo + k, glo = 16-byte floor of the
+// slice start.  The bulk copy covers [c0, c1) (offsets from glo), the part of
+// the window inside the tensor's 16-byte-aligned interior; window bytes
+// outside the slice, or slice bytes outside [c0, c1), are fixed afterwards.
+struct Geo {
+    const unsigned char *glo;
+    int ngran;   // 16-byte groups in the window
+    int c0, c1;  // bulk-copied bytes
+    int a0, a1;  // the slice's bytes
+    int vbase;   // element index of buffer byte 0 (may be negative)
+    bool patch;  // some window byte needs fixing
 };
 
 template <int EB>
-__device__ __forceinline__ RowGeo make_geo(const unsigned char *row, int s0, int s1, unsigned char *buf) {
-    RowGeo g;
-    const uintptr_t A = reinterpret_cast<uintptr_t>(row);
-    const uintptr_t a0 = A + static_cast<uintptr_t>(s0) * EB;
-    const uintptr_t a1 = A + static_cast<uintptr_t>(s1) * EB;
+__device__ __forceinline__ Geo make_geo(const unsigned char *row, int s0, int s1, const unsigned char *lo,
+                                        const unsigned char *hi) {
+    Geo g;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(s0) * EB;
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(s1) * EB;
     const uintptr_t glo = a0 & ~uintptr_t(15);
     const uintptr_t ghi = (a1 + 15) & ~uintptr_t(15);
-    const uintptr_t flo = (a0 + 15) & ~uintptr_t(15);
-    const uintptr_t fhi = a1 & ~uintptr_t(15);
+    const uintptr_t safe_lo = (reinterpret_cast<uintptr_t>(lo) + 15) & ~uintptr_t(15);
+    const uintptr_t safe_hi = reinterpret_cast<uintptr_t>(hi) & ~uintptr_t(15);
+    uintptr_t c0 = glo > safe_lo ? glo : safe_lo;
+    uintptr_t c1 = ghi < safe_hi ? ghi : safe_hi;
+    if (c0 > ghi) c0 = ghi;
+    if (c1 < c0) c1 = c0;
     g.glo = reinterpret_cast<const unsigned char *>(glo);
-    g.buf = buf;
     g.ngran = static_cast<int>((ghi - glo) >> 4);
-    if (flo < fhi) {
-        g.hg = static_cast<int>((flo - glo) >> 4);
-        g.nfull = static_cast<int>((fhi - flo) >> 4);
-    } else {
-        g.hg = 0;
-        g.nfull = 0;
-    }
-    g.vbase = static_cast<int>((static_cast<long long>(glo) - static_cast<long long>(A)) / EB);
-    g.a0off = static_cast<int>(a0 - glo);
-    g.a1off = static_cast<int>(a1 - glo);
+    g.c0 = static_cast<int>(c0 - glo);
+    g.c1 = static_cast<int>(c1 - glo);
+    g.a0 = static_cast<int>(a0 - glo);
+    g.a1 = static_cast<int>(a1 - glo);
+    g.vbase = s0 - g.a0 / EB;
+    g.patch = (a0 != glo) || (a1 != ghi) || (c0 != glo) || (c1 != ghi);
     return g;
 }
 
-// ------------------------------------------------------- softmax merging
-// (m, s) represents sum exp2((x - m) * c) over a set; merge two such sets.
-__device__ __forceinline__ void merge_ms(float &m, float &s, float m2, float s2, float c) {
+// Fix the edge groups of one row buffer after its bulk copy has landed:
+// window bytes outside the slice become -inf, slice bytes outside the copied
+// range are loaded element by element.  16 lanes: 0..7 the first group,
+// 8..15 the last group.
+template <int EB>
+__device__ __forceinline__ void patch_row(unsigned char *buf, const Geo &g, int l16) {
+    constexpr int G = 16 / EB;
+    const int e = l16 & 7;
+    if (e >= G) return;
+    const int grp = (l16 < 8) ? 0 : g.ngran - 1;
+    const int off = grp * 16 + e * EB;
+    if (off < g.a0 || off >= g.a1)
+        Elt<EB>::store_neg_inf(buf + off);
+    else if (off < g.c0 || off >= g.c1)
+        Elt<EB>::copy(buf + off, g.glo + off);
+}
+
+// ------------------------------------------------------- partial merging
+// (mc, s) represents sum 2^(l*c - mc) over a set of logits l (scaled domain).
+__device__ __forceinline__ void merge_sc(float &m, float &s, float m2, float s2) {
     const float mm = fmaxf(m, m2);
-    const float a = (m == mm) ? s : s * ptx::ex2((m - mm) * c);
-    const float b = (m2 == mm) ? s2 : s2 * ptx::ex2((m2 - mm) * c);
+    const float a = (m == mm) ? s : s * ptx::ex2(m - mm);
+    const float b = (m2 == mm) ? s2 : s2 * ptx::ex2(m2 - mm);
     m = mm;
     s = a + b;
 }
@@ -284,175 +367,546 @@ __device__ __forceinline__ void merge_vi(float &v, int &i, float v2, int i2) {
     }
 }
 
+// Warp-wide merge of the lanes' (mc, s): the max first, then one rescale per
+// lane and a plain sum.  Every lane ends with the result.
+__device__ __forceinline__ void warp_merge_sc(float &m, float &s) {
+    float mm = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(kFull, mm, off));
+    if (m != mm) s *= ptx::ex2(m - mm);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+    m = mm;
+}
+
+__device__ __forceinline__ void warp_merge_vi(float &v, int &i) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        merge_vi(v, i, __shfl_xor_sync(kFull, v, off), __shfl_xor_sync(kFull, i, off));
+}
+
+__device__ __forceinline__ long long warp_sum64(long long q) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(kFull, q, off);
+    return q;
+}
+
 // ------------------------------------------------------ extra-token weights
 // Weight of one element: pair (residual) max(0, p_v - q_v) with
-// p_v = 2^((t - Mt) c) / St and q_v = 2^((d - Md) c) / Sd; tail p_v.  The
-// explicit _rn intrinsics keep every evaluation of a weight bit-identical.
-__device__ __forceinline__ float elem_weight(float t, float d, bool pair, float Mt, float Md, float invSt,
-                                             float invSd, float c) {
-    const float pv = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(t, Mt), c)), invSt);
+// p_v = 2^(t c - MCt) / St and q_v = 2^(d c - MCd) / Sd; tail p_v.
+// js = (MCt, 1/St, MCd, 1/Sd).  The explicit _rn intrinsics keep every
+// evaluation of a weight bit-identical (no contraction into an FMA).
+__device__ __forceinline__ float elem_weight(float t, float d, bool pair, const float4 &js, float c) {
+    const float pv = __fmul_rn(ptx::ex2(__fmaf_rn(t, c, -js.x)), js.y);
     if (!pair) return pv;
-    const float qv = __fmul_rn(ptx::ex2(__fmul_rn(__fsub_rn(d, Md), c)), invSd);
+    const float qv = __fmul_rn(ptx::ex2(__fmaf_rn(d, c, -js.z)), js.w);
     return fmaxf(0.0f, __fsub_rn(pv, qv));
 }
 
-// fp32 sum of one 16-byte group's weights, in element order (the order every
-// consumer of a group sum repeats).
+// ---------------------------------------------------------- tile reductions
+// Sum of 2^(fma(l, c, -mc)) over this lane's logits of one stats tile (the
+// 16-byte groups lane, lane + 32, ...): packed FMA/ADD, one ex2 per logit.
 template <int EB>
-__device__ __forceinline__ float group_weight(const RowGeo &gt, const RowGeo &gd, bool pair, bool same_phase,
-                                              int g, int s0, int s1, float Mt, float Md, float invSt, float invSd,
-                                              float c) {
-    constexpr int G = Elt<EB>::G;
-    float t[G], d[G];
-    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(gt.buf + 16 * g), t);
-    if (pair) {
-        if (same_phase) {
-            Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(gd.buf + 16 * g), d);
-        } else {
+__device__ __forceinline__ float lane_tile_sum(const unsigned char *buf, int ngran, int lane, float c, float mc) {
+    constexpr int P = Elt<EB>::P;
+    const unsigned long long c2 = f2pack(c, c), nmc2 = f2pack(-mc, -mc);
+    unsigned long long acc[P];
 #pragma unroll
-            for (int k = 0; k < G; ++k) {
-                const int v = gt.vbase + g * G + k;
-                d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(gd.buf + (v - gd.vbase) * EB) : neg_inf();
-            }
+    for (int q = 0; q < P; ++q) acc[q] = 0ull;
+#pragma unroll 4
+    for (int g = lane; g < ngran; g += 32) {
+        unsigned long long v[P];
+        Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(buf + 16 * g), v);
+#pragma unroll
+        for (int q = 0; q < P; ++q) acc[q] = exp_acc(acc[q], v[q], c2, nmc2);
+    }
+#pragma unroll
+    for (int q = 1; q < P; ++q) acc[0] = f2add(acc[0], acc[q]);
+    float a, b;
+    f2unpack(acc[0], a, b);
+    return a + b;
+}
+
+// Add one stats tile to this lane's running (mc, sum), sum = sum 2^(l c - mc).
+// The offset mc need not be the max: the lane's max is taken only to start,
+// or when a tile's terms grow past 2^64 (a new, much larger max); so every
+// term stays below 2^64 and nothing overflows.
+template <int EB>
+__device__ __forceinline__ void lane_sum(const unsigned char *buf, int ngran, float c, int lane, float &mc,
+                                         float &sum) {
+    if (mc > neg_inf()) {
+        const float t = lane_tile_sum<EB>(buf, ngran, lane, c, mc);
+        if (t < 18446744073709551616.0f) {  // 2^64 (false for NaN and inf: redone below)
+            sum += t;
+            return;
         }
     }
-    float sw = 0.f;
+    const float mx = Elt<EB>::group_max(buf, lane, ngran);
+    if (!(mx > neg_inf())) {        // no logit above -inf in this lane's part
+        if (mx != mx) sum = mx;     // all NaN: poison the sum so the row is flagged
+        return;
+    }
+    const float mn = mx * c;        // fl(max * c): the largest fl(l * c) of these logits
+    if (mn > mc) {
+        sum *= ptx::ex2(mc - mn);   // 0 while mc is still -inf
+        mc = mn;
+    }
+    sum += lane_tile_sum<EB>(buf, ngran, lane, c, mc);
+}
+
+// Add one stats tile to this lane's running (max, lowest index of the max).
+template <int EB>
+__device__ __forceinline__ void lane_argmax(const unsigned char *buf, int ngran, int vbase, int lane, float &bv,
+                                            int &bi) {
+    constexpr int G = Elt<EB>::G;
+    for (int g = lane; g < ngran; g += 32) {
+        float va[G];
+        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(buf + 16 * g), va);
 #pragma unroll
-    for (int k = 0; k < G; ++k) sw += elem_weight(t[k], pair ? d[k] : 0.f, pair, Mt, Md, invSt, invSd, c);
-    return sw;
+        for (int k = 0; k < G; ++k)
+            if (va[k] > bv) {
+                bv = va[k];
+                bi = vbase + g * G + k;
+            }
+    }
+}
+
+// Exact weight sums of one residual tile per chunk of 64 groups (every lane
+// ends with them).  Groups follow the target row's window; `same` when both
+// row buffers share the 16-byte phase.
+template <int EB>
+__device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, int vbase0, int vbase1, int s0,
+                                           int s1, bool pair, bool same, const float4 &js, float c, int lane,
+                                           long long (&q)[kCpt]) {
+    constexpr int G = Elt<EB>::G;
+    const unsigned char *bt = buf;
+    const unsigned char *bd = buf + kRowBuf;
+#pragma unroll
+    for (int ch = 0; ch < kCpt; ++ch) q[ch] = 0;
+    for (int g = lane; g < ngran; g += 32) {
+        float t[G], d[G];
+        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(bt + 16 * g), t);
+        if (pair) {
+            if (same) {
+                Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(bd + 16 * g), d);
+            } else {
+#pragma unroll
+                for (int k = 0; k < G; ++k) {
+                    const int v = vbase0 + g * G + k;
+                    d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(bd + (v - vbase1) * EB) : neg_inf();
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < G; ++k) d[k] = 0.f;
+        }
+        float sw = 0.f;
+#pragma unroll
+        for (int k = 0; k < G; ++k) sw += elem_weight(t[k], d[k], pair, js, c);
+        const long long qq = fixq(sw);
+        const int chunk = g >> 6;
+#pragma unroll
+        for (int ch = 0; ch < kCpt; ++ch)
+            if (chunk == ch) q[ch] += qq;
+    }
+#pragma unroll
+    for (int ch = 0; ch < kCpt; ++ch) q[ch] = warp_sum64(q[ch]);
 }
 
 // ---------------------------------------------------------- unit layout
-struct UnitRows {
-    int b, pos, nrows;
-    const unsigned char *row[kMaxRows];
+template <int MODE>
+struct Traits {
+    static constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
+    static constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
 };
 
-// Unit u: (sequence b, position pos) and its rows; pos < 0 marks an invalid
-// unit of the extra-token-alone mode (no rows).
-template <int EB, int MODE>
-__device__ __forceinline__ UnitRows unit_rows(const Params &p, int u) {
-    constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
-    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
-    UnitRows ur;
-    if (kBonus) {
-        ur.b = u;
-        ur.pos = p.accept_len_in[u];
-        if (ur.pos < 0 || ur.pos > p.K) ur.pos = -1;
-    } else {
-        ur.b = u / p.units_per_seq;
-        ur.pos = u - ur.b * p.units_per_seq;
-    }
-    ur.nrows = (ur.pos < 0) ? 0 : ((kSample && ur.pos < p.K) ? 2 : 1);
-    const size_t row_bytes = static_cast<size_t>(p.V) * EB;
-    ur.row[0] = p.target;
-    if (ur.nrows >= 1) ur.row[0] = p.target + (static_cast<size_t>(ur.b) * p.t_rows + ur.pos) * row_bytes;
-    ur.row[1] = ur.row[0];
-    if (ur.nrows == 2) ur.row[1] = p.draft + (static_cast<size_t>(ur.b) * p.K + ur.pos) * row_bytes;
-    return ur;
+template <int EB>
+__device__ __forceinline__ const unsigned char *row_ptr(const Params &p, int b, int pos, int r) {
+    const size_t rb = static_cast<size_t>(p.V) * EB;
+    if (r == 0) return p.target + (static_cast<size_t>(b) * p.t_rows + pos) * rb;
+    return p.draft + (static_cast<size_t>(b) * p.K + pos) * rb;
 }
 
-// ====================================================== control-warp side
-// The control warp fills stage s with slice k of unit u's rows (all 32 lanes call it).
-template <int EB, int MODE>
-__device__ void fill_stage(const Params &p, Ctl &ctl, unsigned char *dsm, int s, const StageMeta &m,
-                           const UnitRows &ur, int lane) {
-    unsigned char *stage = dsm + static_cast<size_t>(s) * p.stage_bytes;
-    const uint32_t bar = ptx::smem_addr(&ctl.full[s]);
-    const int s0 = min(p.V, m.k * p.slice_len);
-    const int s1 = min(p.V, s0 + p.slice_len);
-    RowGeo geo[kMaxRows];
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) geo[r] = make_geo<EB>(ur.row[r], s0, s1, stage + r * p.row_buf_bytes);
-    if (lane == 0) {
-        ctl.meta[s] = m;
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r)
-            if (r < ur.nrows) bytes += static_cast<uint32_t>(geo[r].nfull) * 16u;
-        // the compute warps' reads of this stage are ordered before this point by
-        // the stage's done-mbarrier, which the control warp waited on
-        ptx::mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-            if (r >= ur.nrows || geo[r].nfull == 0) continue;
-            const int off = 16 * geo[r].hg;
-            ptx::bulk_g2s(ptx::smem_addr(geo[r].buf + off), geo[r].glo + off,
-                          static_cast<uint32_t>(geo[r].nfull) * 16u, bar);
-        }
+// Position of sequence b's unit in the extra-token-alone modes; -1 if invalid.
+__device__ __forceinline__ int bonus_pos(const Params &p, int b) {
+    const int j = __ldg(&p.accept_len_in[b]);
+    return (j < 0 || j > p.K) ? -1 : j;
+}
+
+// Rows of the unit at position pos (-1: an invalid length, one unused row).
+template <int MODE>
+__device__ __forceinline__ int unit_nrows(const Params &p, int pos) {
+    return (Traits<MODE>::kSample && pos >= 0 && pos < p.K) ? 2 : 1;
+}
+
+// Row slot rs of a sequence in the stats tiling: its position, its row within
+// the unit, and whether it exists (bpos: the extra-token position, if any).
+template <int MODE>
+__device__ __forceinline__ bool row_slot(const Params &p, int rs, int bpos, int &pos, int &r) {
+    if (MODE == kLinearSample) {
+        pos = rs >> 1;
+        r = rs & 1;
+        return true;
     }
-    // unaligned ends element-wise (at most 16 slots per row): lanes 0..15 row 0, 16..31 row 1
-    {
-        const int r = lane >> 4;
-        const int e = lane & 15;
-        if (r < ur.nrows) {
-            const RowGeo g = (r == 0) ? geo[0] : geo[1];
-            const int head_slots = g.hg * 16 / EB;
-            const int tail_first = (g.hg + g.nfull) * 16;
-            const int tail_slots = (g.ngran * 16 - tail_first) / EB;
-            if (e < head_slots + tail_slots) {
-                const int off = (e < head_slots) ? e * EB : tail_first + (e - head_slots) * EB;
-                if (off >= g.a0off && off < g.a1off)
-                    Elt<EB>::copy(g.buf + off, g.glo + off);
-                else
-                    Elt<EB>::store_neg_inf(g.buf + off);
-            }
-        }
+    if (MODE == kBonusSample || MODE == kBonusGreedy) {
+        pos = bpos < 0 ? 0 : bpos;  // an invalid length still reads one row, so its unit completes
+        r = rs;
+        return r == 0 || (MODE == kBonusSample && bpos >= 0 && bpos < p.K);
+    }
+    pos = rs;
+    r = 0;
+    return true;
+}
+
+// =================================================================== kernel
+template <int EB, int MODE>
+__global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const Params p) {
+    using T = Traits<MODE>;
+    constexpr int G = Elt<EB>::G;
+
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ WarpCtl wctl[kWarps];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    WarpCtl &wc = wctl[warp];
+    const int NS = p.nstage;
+    unsigned char *ring = dsm + static_cast<size_t>(warp) * NS * kStageBytes;
+    int *tscratch = reinterpret_cast<int *>(dsm + static_cast<size_t>(kWarps) * NS * kStageBytes) +
+                    static_cast<size_t>(warp) * 3 * p.units_per_seq;
+
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) ptx::mbar_init(ptx::smem_addr(&wc.full[s]), 1);
+        ptx::fence_mbar_init();
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar);  // second arrival: the element-wise part is in place
-}
 
-// Emit sequence b (its last unit just finished) and zero its workspace entries.
-template <int EB, int MODE>
-__device__ void emit_sequence(const Params &p, int b, long long *stage_ints, int lane) {
-    const int K = p.K;
-    const int U = p.units_per_seq;
-    if (MODE == kLinearSample || MODE == kLinearGreedy) {
-        const bool has_bonus = p.u_bonus != nullptr;
-        int j = K;
-        for (int base = 0; base < K; base += 32) {
-            const int i = base + lane;
-            bool rej = false;
-            if (i < K) {
-                if (MODE == kLinearSample)
-                    rej = __ldcg(&p.ws_acc[static_cast<size_t>(b) * K + i]) == 0;
-                else
-                    rej = p.tokens[static_cast<size_t>(b) * K + i] != __ldcg(&p.ws_val[static_cast<size_t>(b) * U + i]);
-            }
-            const unsigned m = __ballot_sync(0xffffffffu, rej);
-            if (m) {
-                j = base + __ffs(m) - 1;
-                break;
+    const long long ST = p.stats_tiles;
+    const long long RT = p.res_tiles;
+    const int S = p.S;
+    const size_t row_bytes = static_cast<size_t>(p.V) * EB;
+    const bool draws = T::kSample && (T::kBonus || p.u_bonus != nullptr);
+    const long long nwarps = static_cast<long long>(gridDim.x) * kWarps;
+    bool timed_out = false;
+
+    // A row of the stats tiling: row slot rs of sequence b.
+    struct Row {
+        int id;                        // b * rows_per_seq + rs
+        int b, pos, r, unit;
+        bool present;
+        uintptr_t R0, A, E, lo, hi;    // row start, window grid start / end, tensor's aligned interior
+    };
+    auto decode_row = [&](int id) -> Row {
+        Row t;
+        t.id = id;
+        t.b = id / p.rows_per_seq;
+        const int rs = id - t.b * p.rows_per_seq;
+        const int bpos = T::kBonus ? bonus_pos(p, t.b) : 0;
+        t.present = row_slot<MODE>(p, rs, bpos, t.pos, t.r);
+        t.unit = T::kBonus ? t.b : t.b * p.units_per_seq + t.pos;
+        if (T::kBonus) t.pos = bpos;  // -1 for an invalid length (its row 0 is read all the same)
+        const unsigned char *row = row_ptr<EB>(p, t.b, t.pos < 0 ? 0 : t.pos, t.r);
+        t.R0 = reinterpret_cast<uintptr_t>(row);
+        t.A = t.R0 & ~uintptr_t(15);
+        t.E = (t.R0 + row_bytes + 15) & ~uintptr_t(15);
+        t.lo = (reinterpret_cast<uintptr_t>(t.r ? p.draft : p.target) + 15) & ~uintptr_t(15);
+        t.hi = reinterpret_cast<uintptr_t>(t.r ? p.d_end : p.t_end) & ~uintptr_t(15);
+        return t;
+    };
+    // window [w0, w1) of tile k of a row, and its bulk-copied part [c0, c1)
+    auto tile_window = [&](const Row &t, int k, uintptr_t &w0, uintptr_t &w1, uintptr_t &c0, uintptr_t &c1) {
+        w0 = t.A + static_cast<uintptr_t>(k) * kTileBytes;
+        w1 = w0 + kTileBytes < t.E ? w0 + kTileBytes : t.E;
+        if (w1 < w0) w1 = w0;  // past the row's end: an empty tile
+        c0 = w0 > t.lo ? w0 : t.lo;
+        c1 = w1 < t.hi ? w1 : t.hi;
+        if (c0 > w1) c0 = w1;
+        if (c1 < c0) c1 = c0;
+    };
+    // unit (b, pos) of a draw entry record
+    auto entry_unit = [&](uint32_t rec, int &u, int &b, int &pos) {
+        u = static_cast<int>(rec & kRecUnit) - 1;
+        if (T::kBonus) {
+            b = u;
+            pos = max(0, bonus_pos(p, b));
+        } else {
+            b = u / p.units_per_seq;
+            pos = u - b * p.units_per_seq;
+        }
+    };
+    // tiles to take at once: shrinks as the space runs out, so the last grabs are short
+    auto guided = [&](long long left) -> int {
+        const long long g = left / (2 * nwarps);
+        return static_cast<int>(g < 1 ? 1 : (g > kMaxGrab ? kMaxGrab : g));
+    };
+
+    // ---------------------------------------------------------- issue side
+    long long sc = 0, se = 0;          // stats tiles [sc, se) to issue
+    Row irow = {};                     // the row of the last issued stats tile
+    irow.id = -1;
+    unsigned s_ahead = 0;              // lane 0: start of the next stats grab
+    int s_ahead_n = 0;                 // its size
+    bool stats_done = (ST == 0);
+    if (!stats_done) {
+        s_ahead_n = guided(ST);
+        if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
+    }
+    long long rc = 0, re = 0;          // residual tiles [rc, re) claimed, not yet issued
+    int r_entry = -1;                  // entry of r_rec
+    uint32_t r_rec = 0;                // its record (0: not yet seen published)
+    bool rec_inflight = false;
+    uint32_t rec_val = 0;              // lane 0: a record load in flight
+    bool claim_inflight = false;
+    unsigned claim_res = 0;            // lane 0: start of a residual claim in flight
+    int claim_n = 0;
+    bool res_done = (RT == 0);
+    unsigned hint_tail = 0, hint_claim = 0;  // lane 0: counters read at the previous stats grab
+    bool hint_valid = false;
+    int issued = 0, handled = 0;
+    int islot = 0;                     // stage of the next issue
+    auto next_islot = [&]() {
+        const int s = islot;
+        islot = (islot + 1 == NS) ? 0 : islot + 1;
+        return s;
+    };
+
+    // tile t of the stats tiling -> (row, k), incrementally for consecutive tiles
+    long long i_t = -2;
+    int i_k = 0;
+    auto locate_stats = [&](long long t) {
+        if (t == i_t + 1 && i_k + 1 < S) {
+            ++i_k;
+        } else {
+            const int id = static_cast<int>(static_cast<unsigned>(t) / static_cast<unsigned>(S));
+            i_k = static_cast<int>(t) - id * S;
+            if (id != irow.id) irow = decode_row(id);
+        }
+        i_t = t;
+    };
+    auto issue_stats = [&](long long t) {
+        const int k = i_k;
+        const int s = next_islot();
+        unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
+        uintptr_t w0, w1, c0, c1;
+        tile_window(irow, k, w0, w1, c0, c1);
+        if (lane == 0) {
+            wc.desc[s] = make_int4(kTileStats, static_cast<int>(t), 0, 0);
+            const uint32_t bar = ptx::smem_addr(&wc.full[s]);
+            const uint32_t bytes = static_cast<uint32_t>(c1 - c0);
+            ptx::mbar_arrive_expect_tx(bar, bytes);
+            if (bytes)
+                ptx::bulk_g2s(ptx::smem_addr(buf + (c0 - w0)), reinterpret_cast<const void *>(c0), bytes, bar);
+        }
+        ++issued;
+    };
+
+    auto issue_resid = [&](long long q, uint32_t rec) {
+        const int e = static_cast<int>(q / p.Sr);
+        const int k = static_cast<int>(q - static_cast<long long>(e) * p.Sr);
+        const bool pair = (rec & kRecPair) != 0;
+        const bool skip = (rec & kRecSkip) != 0;
+        int u, b, pos;
+        entry_unit(rec, u, b, pos);
+        const int s = next_islot();
+        unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
+        const int s0 = k * p.Lr;
+        const int s1 = min(p.V, s0 + p.Lr);
+        const Geo g0 = make_geo<EB>(row_ptr<EB>(p, b, pos, 0), s0, s1, p.target, p.t_end);
+        Geo g1 = g0;
+        if (pair) g1 = make_geo<EB>(row_ptr<EB>(p, b, pos, 1), s0, s1, p.draft, p.d_end);
+        if (lane == 0) {
+            wc.desc[s] = make_int4(kTileResid, static_cast<int>(q), static_cast<int>(rec), 0);
+            const uint32_t bar = ptx::smem_addr(&wc.full[s]);
+            uint32_t bytes = 0;
+            if (!skip)
+                bytes = static_cast<uint32_t>(g0.c1 - g0.c0) + (pair ? static_cast<uint32_t>(g1.c1 - g1.c0) : 0u);
+            ptx::mbar_arrive_expect_tx(bar, bytes);
+            if (!skip) {
+                if (g0.c1 > g0.c0)
+                    ptx::bulk_g2s(ptx::smem_addr(buf + g0.c0), g0.glo + g0.c0, static_cast<uint32_t>(g0.c1 - g0.c0),
+                                  bar);
+                if (pair && g1.c1 > g1.c0)
+                    ptx::bulk_g2s(ptx::smem_addr(buf + kRowBuf + g1.c0), g1.glo + g1.c0,
+                                  static_cast<uint32_t>(g1.c1 - g1.c0), bar);
             }
         }
-        const int bonus = has_bonus ? __ldcg(&p.ws_val[static_cast<size_t>(b) * U + j]) : -1;
+        ++issued;
+    };
+
+    auto claim_resid = [&](int n) {
+        if (lane == 0) claim_res = atomicAdd(&p.ws_ctrl[3], static_cast<unsigned>(n));
+        claim_n = n;
+        claim_inflight = true;
+    };
+
+    // Hand the next tile to the ring.  Returns false when nothing was issued:
+    // nothing is ready now (blocking == false), or no work is left at all.
+    auto try_issue = [&](bool blocking) -> bool {
+        for (int guard = 0; guard < (1 << 20); ++guard) {
+            if (claim_inflight) {
+                const unsigned r = __shfl_sync(kFull, claim_res, 0);
+                claim_inflight = false;
+                if (static_cast<long long>(r) >= RT) {
+                    res_done = true;
+                } else {
+                    rc = r;
+                    re = min(RT, static_cast<long long>(r) + claim_n);
+                }
+            }
+            // 1. claimed residual tiles, once their entry is published
+            if (rc < re) {
+                const int e = static_cast<int>(rc / p.Sr);
+                if (e != r_entry) {
+                    r_entry = e;
+                    r_rec = 0;
+                    rec_inflight = false;
+                }
+                if (r_rec == 0) {
+                    if (rec_inflight) {
+                        r_rec = __shfl_sync(kFull, rec_val, 0);
+                        rec_inflight = false;
+                    }
+                    if (r_rec == 0 && blocking) {
+                        uint32_t rec = 0;
+                        if (lane == 0) {
+                            rec = ld_relaxed(&p.ws_rq[e]);
+                            for (uint32_t i = 0; rec == 0 && i < kSpinLimit; ++i) {
+                                __nanosleep(128);
+                                rec = ld_relaxed(&p.ws_rq[e]);
+                            }
+                        }
+                        r_rec = __shfl_sync(kFull, rec, 0);
+                        if (r_rec == 0) {  // the entry never appeared: give up the residual work
+                            timed_out = true;
+                            rc = re;
+                            res_done = true;
+                            continue;
+                        }
+                    }
+                    if (r_rec == 0 && !rec_inflight) {  // look again at the next call
+                        if (lane == 0) rec_val = ld_relaxed(&p.ws_rq[e]);
+                        rec_inflight = true;
+                    }
+                }
+                if (r_rec != 0) {
+                    issue_resid(rc, r_rec);
+                    ++rc;
+                    return true;
+                }
+            }
+            // 2. the next stats tile
+            if (!stats_done) {
+                if (sc >= se) {
+                    const unsigned a = __shfl_sync(kFull, s_ahead, 0);
+                    if (static_cast<long long>(a) >= ST) {
+                        stats_done = true;
+                    } else {
+                        sc = a;
+                        se = min(ST, static_cast<long long>(a) + s_ahead_n);
+                        s_ahead_n = guided(ST - se);
+                        if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
+                        // residual tiles waiting (by the counters read at the previous grab): claim some
+                        if (!res_done && rc >= re && !claim_inflight) {
+                            int avail = 0;
+                            if (lane == 0 && hint_valid) {
+                                const long long a2 = static_cast<long long>(hint_tail) * p.Sr - hint_claim;
+                                avail = static_cast<int>(a2 < 0 ? 0 : (a2 > kMaxClaim ? kMaxClaim : a2));
+                            }
+                            avail = __shfl_sync(kFull, avail, 0);
+                            if (avail > 0) claim_resid(avail);
+                        }
+                        if (!res_done && lane == 0) {
+                            hint_tail = ld_relaxed(&p.ws_ctrl[2]);
+                            hint_claim = ld_relaxed(&p.ws_ctrl[3]);
+                            hint_valid = true;
+                        }
+                    }
+                }
+                if (!stats_done) {
+                    locate_stats(sc);
+                    if (!irow.present) {  // a row slot with no row (the draft row at the tail): skip it
+                        ++sc;
+                        continue;
+                    }
+                    issue_stats(sc);
+                    ++sc;
+                    return true;
+                }
+            }
+            // 3. stats exhausted: claim residual tiles
+            if (!res_done && rc >= re && !claim_inflight) {
+                long long left = RT;
+                if (lane == 0 && hint_valid) left = RT - static_cast<long long>(hint_claim);
+                left = __shfl_sync(kFull, left, 0);
+                claim_resid(min(kMaxClaim, guided(left < 1 ? 1 : left)));
+                if (lane == 0) hint_claim = ld_relaxed(&p.ws_ctrl[3]);
+                hint_valid = true;
+                if (blocking) continue;
+                return false;
+            }
+            if (!blocking) return false;
+            if (stats_done && res_done && rc >= re && !claim_inflight) return false;
+        }
+        timed_out = true;
+        return false;
+    };
+    auto fill_ring = [&]() {
+        while (issued - handled < NS) {
+            if (!claim_inflight && rc >= re && sc < se && sc == i_t + 1 && i_k + 1 < S && irow.present) {
+                // the next tile of the same row: nothing else to look at
+                ++i_k;
+                i_t = sc;
+                issue_stats(sc);
+                ++sc;
+                continue;
+            }
+            if (!try_issue(false)) break;
+        }
+        __syncwarp();
+    };
+
+    // ----------------------------------------------------- processing side
+    // the run being reduced: consecutive tiles of one row (stats) or one entry (residual)
+    int run_kind = 0;                  // 0: none
+    long long run_next = -1;           // index the run's next tile would have
+    Row prow = {};                     // stats: the run's row
+    prow.id = -1;
+    int run_k0 = 0, run_len = 0;
+    int px = -1;                       // the draft token whose logit this row holds, or -1
+    float am = neg_inf(), as = 0.f;    // lane: running (mc, s), or (max, -) in greedy mode
+    int ai = INT_MAX;                  // lane: index of the max (greedy)
+    int hasx = 0;
+    float xval = 0.f;
+    int r_e = 0, r_u = 0, r_b = 0, r_pos = 0;  // residual run: entry, unit, sequence, position
+    bool r_pair = false, r_skip = false;
+    float4 r_js = make_float4(0.f, 0.f, 0.f, 0.f);
+    // a counter increment whose result is consumed later (1: unit tiles, 2: residual tiles)
+    int pend_kind = 0, pend_unit = 0, pend_b = 0, pend_pos = 0, pend_entry = 0, pend_add = 0;
+    unsigned pend_old = 0;             // lane 0
+
+    // ----------------------------------------------------- finishing side
+    // Emit the sequence: the first j draft tokens, then `extra` (if any), then -1.
+    auto emit_linear = [&](int b, int j, int extra, bool has_extra) {
+        const int K = p.K;
         if (p.out_tokens) {
             for (int i = lane; i <= K; i += 32)
                 p.out_tokens[static_cast<size_t>(b) * (K + 1) + i] =
-                    (i < j) ? p.tokens[static_cast<size_t>(b) * K + i] : ((i == j) ? bonus : -1);
+                    (i < j) ? __ldg(&p.tokens[static_cast<size_t>(b) * K + i]) : ((i == j && has_extra) ? extra : -1);
         }
         if (lane == 0) {
             p.accept_len[b] = j;
-            p.num_emitted[b] = j + (has_bonus ? 1 : 0);
+            p.num_emitted[b] = j + (has_extra ? 1 : 0);
         }
-        // leave this sequence's workspace entries zero for the next call
-        __syncwarp();
-        if (MODE == kLinearSample)
-            for (int i = lane; i < K; i += 32) p.ws_acc[static_cast<size_t>(b) * K + i] = 0;
-        for (int i = lane; i < U; i += 32) p.ws_val[static_cast<size_t>(b) * U + i] = 0;
-        if (lane == 0) {
-            p.ws_first[b] = 0;
-            p.ws_seq_cnt[b] = 0u;
-        }
-    } else if (MODE == kTreeGreedy) {
-        // stage the tree of this sequence in the control warp's scratch area
-        const int N = U;
-        int *par_s = reinterpret_cast<int *>(stage_ints);
+    };
+
+    // Greedy tree walk of sequence b (every node's argmax is in ws_val).
+    auto emit_tree = [&](int b) {
+        const int N = p.units_per_seq;
+        int *par_s = tscratch;
         int *tok_s = par_s + N;
         int *am_s = tok_s + N;
         for (int cidx = lane; cidx < N; cidx += 32) {
-            int pc = p.parents[cidx];
+            int pc = __ldg(&p.parents[cidx]);
             if (cidx == 0) {
                 pc = -1;
             } else if (pc < 0 || pc >= cidx) {
@@ -460,11 +914,11 @@ __device__ void emit_sequence(const Params &p, int b, long long *stage_ints, int
                 pc = -2;
             }
             par_s[cidx] = pc;
-            tok_s[cidx] = p.tokens[static_cast<size_t>(b) * N + cidx];
+            tok_s[cidx] = __ldg(&p.tokens[static_cast<size_t>(b) * N + cidx]);
             am_s[cidx] = __ldcg(&p.ws_val[static_cast<size_t>(b) * N + cidx]);
+            p.ws_val[static_cast<size_t>(b) * N + cidx] = 0;
         }
         __syncwarp();
-        for (int cidx = lane; cidx < N; cidx += 32) p.ws_val[static_cast<size_t>(b) * N + cidx] = 0;
         const int D = p.max_depth;
         int32_t *pn = p.path_nodes + static_cast<size_t>(b) * (D + 1);
         int32_t *ot = p.out_tokens + static_cast<size_t>(b) * (D + 1);
@@ -475,7 +929,7 @@ __device__ void emit_sequence(const Params &p, int b, long long *stage_ints, int
             for (int base = cur + 1; base < N; base += 32) {
                 const int cc = base + lane;
                 const bool hit = cc < N && par_s[cc] == cur && tok_s[cc] == want;
-                const unsigned m = __ballot_sync(0xffffffffu, hit);
+                const unsigned m = __ballot_sync(kFull, hit);
                 if (m) {
                     next = base + __ffs(m) - 1;
                     break;
@@ -493,722 +947,568 @@ __device__ void emit_sequence(const Params &p, int b, long long *stage_ints, int
             pn[0] = 0;
             ot[depth] = am_s[cur];
             p.accept_len[b] = depth;
-            p.ws_seq_cnt[b] = 0u;
         }
         for (int i = depth + 1 + lane; i <= D; i += 32) {
             ot[i] = -1;
             pn[i] = -1;
         }
         __syncwarp();
-    }
-}
+    };
 
-// One more unit of sequence b is finished; emit the sequence if it was the last.
-template <int EB, int MODE>
-__device__ void unit_finished(const Params &p, int b, long long *scratch, int lane) {
-    int last = 0;
-    if (lane == 0)
-        last = (atom_add_acq_rel(&p.ws_seq_cnt[b], 1u) == static_cast<unsigned>(p.units_per_seq - 1)) ? 1 : 0;
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
+    // Publish a draw entry for unit u.
+    auto push_entry = [&](int u, bool pair, bool skip) {
+        if (lane == 0) {
+            const unsigned e = atomicAdd(&p.ws_ctrl[2], 1u);
+            st_release(&p.ws_rq[e], (static_cast<uint32_t>(u) + 1u) | (pair ? kRecPair : 0u) | (skip ? kRecSkip : 0u));
+        }
         __syncwarp();
-        emit_sequence<EB, MODE>(p, b, scratch, lane);
-    }
-}
+    };
 
-// Extra-token draw finished: record the token.
-template <int EB, int MODE>
-__device__ void token_drawn(const Params &p, const Job &jb, int token, long long *scratch, int lane) {
-    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
-    if (kBonus) {
-        if (lane == 0) p.bonus_token[jb.b] = token;
-        return;
-    }
-    if (lane == 0) p.ws_val[static_cast<size_t>(jb.b) * p.units_per_seq + jb.pos] = token;
-    __syncwarp();
-    unit_finished<EB, MODE>(p, jb.b, scratch, lane);
-}
-
-// All residual tiles of job `jb` are reduced: locate the token.  Returns -1
-// when the weights summed to zero (the caller then retries with p alone).
-template <int EB, int MODE>
-__device__ int select_token(const Params &p, const Job &jb, const long long *csum, int lane) {
-    constexpr int G = Elt<EB>::G;
-    const int n = p.S * p.cpt;
-    const int per = (n + 31) / 32;
-    const int lo = min(n, lane * per), hi = min(n, lo + per);
-    long long mine = 0;
-    for (int i = lo; i < hi; ++i) mine += csum[i];
-    long long incl = mine;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-    }
-    const long long tot = __shfl_sync(0xffffffffu, incl, 31);
-    if (tot <= 0) return -1;
-    const long long target = static_cast<long long>(static_cast<double>(jb.ub) * static_cast<double>(tot));
-    // the chunk holding the target: first lane, then first chunk in that lane's block
-    const unsigned bl = __ballot_sync(0xffffffffu, incl > target);
-    const int ol = __ffs(bl) - 1;
-    long long acc = __shfl_sync(0xffffffffu, incl - mine, ol);
-    int chunk = -1;
-    if (lane == ol) {
-        long long a = acc;
-        for (int i = lo; i < hi; ++i) {
-            if (a + csum[i] > target) {
-                chunk = i;
-                break;
-            }
-            a += csum[i];
-        }
-        acc = a;
-    }
-    chunk = __shfl_sync(0xffffffffu, chunk, ol);
-    acc = __shfl_sync(0xffffffffu, acc, ol);
-    const long long rem = target - acc;  // 0 <= rem < csum[chunk]
-    // rescan that chunk from global memory, element by element, with the same weights
-    const int k = chunk / p.cpt;
-    const int cc = chunk - k * p.cpt;
-    const int s0 = min(p.V, k * p.slice_len);
-    const int s1 = min(p.V, s0 + p.slice_len);
-    const UnitRows ur = unit_rows<EB, MODE>(p, jb.unit);
-    const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, nullptr);
-    const bool pair = !jb.tailw;
-    long long q[2];
-    float w[2][G];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int g = cc * kChunk + h * 32 + lane;
-        float sw = 0.f;
-#pragma unroll
-        for (int e = 0; e < G; ++e) {
-            const int v = gt.vbase + g * G + e;
-            float we = 0.f;
-            if (g < gt.ngran && v >= s0 && v < s1) {
-                const float t = Elt<EB>::gload(ur.row[0] + static_cast<size_t>(v) * EB);
-                const float d = pair ? Elt<EB>::gload(ur.row[1] + static_cast<size_t>(v) * EB) : 0.f;
-                we = elem_weight(t, d, pair, jb.Mt, jb.Md, jb.invSt, jb.invSd, p.c);
-            }
-            w[h][e] = we;
-            sw += we;
-        }
-        q[h] = fixq(sw);
-    }
-    // inclusive prefix over the chunk's 64 groups (first half, then second half)
-    long long i0 = q[0], i1 = q[1];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const long long y0 = __shfl_up_sync(0xffffffffu, i0, off);
-        const long long y1 = __shfl_up_sync(0xffffffffu, i1, off);
-        if (lane >= off) {
-            i0 += y0;
-            i1 += y1;
-        }
-    }
-    const long long t0 = __shfl_sync(0xffffffffu, i0, 31);
-    i1 += t0;
-    unsigned bh = __ballot_sync(0xffffffffu, i0 > rem);
-    int half = 0;
-    if (!bh) {
-        bh = __ballot_sync(0xffffffffu, i1 > rem);
-        half = 1;
-    }
-    int token = -1;
-    if (bh) {
-        const int gl = __ffs(bh) - 1;
-        const long long excl = __shfl_sync(0xffffffffu, half ? (i1 - q[1]) : (i0 - q[0]), gl);
-        if (lane == gl) {
-            const int g = cc * kChunk + half * 32 + lane;
-            // the same weights, summed in the same order as the group sum
-            float cum = 0.f;
-            int esel = -1;
-#pragma unroll
-            for (int e = 0; e < G; ++e) {
-                cum += half ? w[1][e] : w[0][e];
-                if (esel < 0 && excl + fixq(cum) > rem) esel = e;
-            }
-            token = gt.vbase + g * G + (esel < 0 ? G - 1 : esel);
-        }
-        token = __shfl_sync(0xffffffffu, token, gl);
-    }
-    return token < 0 ? 0 : token;
-}
-
-// ====================================================== compute-warp side
-template <int EB, int MODE>
-__device__ void compute_stats(const Params &p, Ctl &ctl, unsigned char *stage, const StageMeta &m, int s,
-                              int ct, int cw, int lane) {
-    constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
-    constexpr int G = Elt<EB>::G;
-    const UnitRows ur = unit_rows<EB, MODE>(p, m.unit);
-    const int s0 = min(p.V, m.k * p.slice_len);
-    const int s1 = min(p.V, s0 + p.slice_len);
-    const float c = p.c;
-    // the draft token of a pair unit: its two logits are read here if this slice holds it
-    int x = -1;
-    if (MODE == kLinearSample && m.nrows == 2 && ct == 0) x = p.tokens[static_cast<size_t>(m.b) * p.K + m.pos];
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-        if (r >= m.nrows) continue;
-        const RowGeo g = make_geo<EB>(ur.row[r], s0, s1, stage + r * p.row_buf_bytes);
-        if (kSample) {
-            const float mp = Elt<EB>::group_max(g.buf, ct, g.ngran, kComputeThreads);
-            float sa = 0.f, sb = 0.f;
-            if (mp != neg_inf()) {
-                int gg = ct;
-                for (; gg + kComputeThreads < g.ngran; gg += 2 * kComputeThreads) {
-                    float va[G], vb[G];
-                    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
-                    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * (gg + kComputeThreads)), vb);
-#pragma unroll
-                    for (int k = 0; k < G; ++k) {
-                        sa += ptx::ex2((va[k] - mp) * c);
-                        sb += ptx::ex2((vb[k] - mp) * c);
-                    }
-                }
-                if (gg < g.ngran) {
-                    float va[G];
-                    Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
-#pragma unroll
-                    for (int k = 0; k < G; ++k) sa += ptx::ex2((va[k] - mp) * c);
-                }
-            }
-            // warp: the max first, then one rescale per lane and a plain sum
-            float wmax = mp;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
-            float sum = sa + sb;
-            if (mp != wmax) sum *= ptx::ex2((mp - wmax) * c);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (lane == 0) {
-                ctl.wm[s][r][cw] = wmax;
-                ctl.wsum[s][r][cw] = sum;
-            }
+    // Every unit of sequence b is decided.
+    auto finish_sequence = [&](int b) {
+        const int K = p.K;
+        const int U = p.units_per_seq;
+        if (MODE == kTreeGreedy) {
+            emit_tree(b);
         } else {
-            float bv = neg_inf();
-            int bi = INT_MAX;
-            for (int gg = ct; gg < g.ngran; gg += kComputeThreads) {
-                float va[G];
-                Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(g.buf + 16 * gg), va);
-#pragma unroll
-                for (int k = 0; k < G; ++k)
-                    if (va[k] > bv) {
-                        bv = va[k];
-                        bi = g.vbase + gg * G + k;
-                    }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                merge_vi(bv, bi, __shfl_xor_sync(0xffffffffu, bv, off), __shfl_xor_sync(0xffffffffu, bi, off));
-            if (lane == 0) {
-                ctl.wm[s][r][cw] = bv;
-                ctl.wi[s][r][cw] = bi;
-            }
-        }
-    }
-    if (MODE == kLinearSample && ct == 0) {
-        int has = 0;
-        float2 xv = make_float2(0.f, 0.f);
-        if (m.nrows == 2 && x >= s0 && x < s1) {
-            const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, stage);
-            const RowGeo gd = make_geo<EB>(ur.row[1], s0, s1, stage + p.row_buf_bytes);
-            xv = make_float2(Elt<EB>::load(gt.buf + (x - gt.vbase) * EB), Elt<EB>::load(gd.buf + (x - gd.vbase) * EB));
-            has = 1;
-        }
-        ctl.xval[s] = xv;
-        ctl.xhas[s] = has;
-    }
-}
-
-// Residual tile: exact int64 weight sums per chunk of 64 groups.
-template <int EB, int MODE>
-__device__ void compute_resid(const Params &p, unsigned char *stage, const StageMeta &m, long long *csum, int cw,
-                              int lane) {
-    const UnitRows ur = unit_rows<EB, MODE>(p, m.unit);
-    const int s0 = min(p.V, m.k * p.slice_len);
-    const int s1 = min(p.V, s0 + p.slice_len);
-    const RowGeo gt = make_geo<EB>(ur.row[0], s0, s1, stage);
-    const RowGeo gd = make_geo<EB>(ur.row[1], s0, s1, stage + p.row_buf_bytes);
-    const bool pair = !m.tailw;
-    const bool same_phase =
-        ((reinterpret_cast<uintptr_t>(ur.row[0]) - reinterpret_cast<uintptr_t>(ur.row[1])) & 15u) == 0;
-    for (int ch = cw; ch < p.cpt; ch += kComputeWarps) {
-        long long q = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int g = ch * kChunk + h * 32 + lane;
-            if (g < gt.ngran)
-                q += fixq(group_weight<EB>(gt, gd, pair, same_phase, g, s0, s1, m.Mt, m.Md, m.invSt, m.invSd, p.c));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(0xffffffffu, q, off);
-        if (lane == 0) csum[m.k * p.cpt + ch] = q;
-    }
-}
-
-// ================================================================ kernel
-template <int EB, int MODE>
-__global__ void __maxnreg__(112) spec_verify_kernel(const Params p) {
-    constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
-    constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
-
-    extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ Ctl ctl;
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const int nstage = p.nstage;
-    // after the stages: per-job residual chunk sums (sampling), or the tree-walk scratch
-    long long *extra = reinterpret_cast<long long *>(dsm + static_cast<size_t>(nstage) * p.stage_bytes);
-    const int job_stride = p.S * p.cpt;
-
-    if (tid == 0) {
-        for (int s = 0; s < nstage; ++s) {
-            ptx::mbar_init(ptx::smem_addr(&ctl.full[s]), 2);
-            ptx::mbar_init(ptx::smem_addr(&ctl.done[s]), kComputeWarps);
-        }
-        ptx::fence_mbar_init();
-        ctl.timed_out = 0;
-    }
-    __syncthreads();
-
-    if (warp != 0) {
-        // ===================== compute warps: reduce the stages in ring order
-        const int ct = tid - 32;
-        const int cw = warp - 1;
-        for (int it = 0;; ++it) {
-            const int s = it % nstage;
-            if (!wait_bar(ptx::smem_addr(&ctl.full[s]), static_cast<uint32_t>(it / nstage) & 1u)) {
-                ctl.timed_out = 1;
-                break;
-            }
-            const StageMeta m = ctl.meta[s];
-            if (m.kind == kTileEnd) break;
-            unsigned char *stage = dsm + static_cast<size_t>(s) * p.stage_bytes;
-            if (m.kind == kTileStats)
-                compute_stats<EB, MODE>(p, ctl, stage, m, s, ct, cw, lane);
-            else if (kSample)
-                compute_resid<EB, MODE>(p, stage, m, extra + static_cast<size_t>(m.job) * job_stride, cw, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ptx::smem_addr(&ctl.done[s]));
-        }
-        return;
-    }
-
-    // ========================= control warp: stream tiles, publish, finalize
-    const long long total = static_cast<long long>(p.n_units) * p.S;
-    // tile indices from the global counter; lane 0's copies are authoritative.
-    // The next batch is requested one batch ahead, so its latency is hidden.
-    long long grab_next = 0, grab_end = 0;
-    unsigned grab_ahead = 0;
-    if (lane == 0) grab_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(p.grab));
-    bool exhausted = false;
-    int job_head = 0, job_count = 0;  // FIFO of pending draws (lane 0)
-    int handled = 0, filled = 0;      // tiles handled / tiles handed to the ring
-    bool timed_out = false;
-    // the last published run's counter increment, consumed later
-    unsigned pend_old = 0;
-    int pend_cnt = 0;
-    bool pend_valid = false;
-    StageMeta pend_m = {};
-    // the run of consecutive stats tiles of one unit merged in this CTA (lane 0)
-    int run_unit = -1, run_k0 = 0, run_cnt = 0, run_hasx = 0;
-    uint2 run_part[kMaxRows] = {};
-    float2 run_x = make_float2(0.f, 0.f);
-    StageMeta run_m = {};
-
-    // the next tile of this CTA's stream: pending draws first, then fresh tiles
-    auto next_tile = [&](StageMeta &m) -> bool {
-        int found = 0;
-        if (lane == 0) {
-            for (int q = 0; q < job_count && !found; ++q) {
-                Job &jb = ctl.jobs[(job_head + q) % kMaxJobs];
-                if (!jb.fin && jb.next_k < p.S) {
-                    m.kind = kTileResid;
-                    m.unit = jb.unit;
-                    m.k = jb.next_k++;
-                    m.job = (job_head + q) % kMaxJobs;
-                    m.tailw = jb.tailw;
-                    m.Mt = jb.Mt;
-                    m.invSt = jb.invSt;
-                    m.Md = jb.Md;
-                    m.invSd = jb.invSd;
-                    found = 1;
+            int j = K;
+            for (int base = 0; base < K; base += 32) {
+                const int i = base + lane;
+                bool rej = false;
+                if (i < K) {
+                    if (MODE == kLinearSample)
+                        rej = __ldcg(&p.ws_acc[static_cast<size_t>(b) * K + i]) == 0;
+                    else
+                        rej = __ldg(&p.tokens[static_cast<size_t>(b) * K + i]) !=
+                              __ldcg(&p.ws_val[static_cast<size_t>(b) * U + i]);
+                }
+                const unsigned m = __ballot_sync(kFull, rej);
+                if (m) {
+                    j = base + __ffs(m) - 1;
+                    break;
                 }
             }
-            if (!found && !exhausted) {
-                if (grab_next >= grab_end) {
-                    grab_next = grab_ahead;
-                    grab_end = grab_next + p.grab;
-                    if (grab_next < total)
-                        grab_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(p.grab));
-                }
-                if (grab_next < total) {
-                    const long long t = grab_next++;
-                    m.kind = kTileStats;
-                    m.unit = static_cast<int>(t / p.S);
-                    m.k = static_cast<int>(t - static_cast<long long>(m.unit) * p.S);
-                    m.job = -1;
-                    m.tailw = 0;
-                    found = 1;
+            if (MODE == kLinearSample) {
+                for (int i = lane; i < K; i += 32) p.ws_acc[static_cast<size_t>(b) * K + i] = 0;
+                if (draws) {
+                    const int u = b * U + j;
+                    const float4 js = __ldcg(&p.ws_stats[u]);
+                    push_entry(u, j < K, !(js.y > 0.f));  // a non-finite unit recorded 1/St = 0
                 } else {
-                    exhausted = true;
+                    emit_linear(b, j, -1, false);
                 }
+            } else {  // greedy
+                const int extra = (p.u_bonus != nullptr) ? __ldcg(&p.ws_val[static_cast<size_t>(b) * U + j]) : -1;
+                __syncwarp();
+                for (int i = lane; i < U; i += 32) p.ws_val[static_cast<size_t>(b) * U + i] = 0;
+                emit_linear(b, j, extra, p.u_bonus != nullptr);
             }
         }
-        found = __shfl_sync(0xffffffffu, found, 0);
-        if (!found) return false;
-        m.kind = __shfl_sync(0xffffffffu, m.kind, 0);
-        m.unit = __shfl_sync(0xffffffffu, m.unit, 0);
-        m.k = __shfl_sync(0xffffffffu, m.k, 0);
-        m.job = __shfl_sync(0xffffffffu, m.job, 0);
-        m.tailw = __shfl_sync(0xffffffffu, m.tailw, 0);
-        m.Mt = __shfl_sync(0xffffffffu, m.Mt, 0);
-        m.invSt = __shfl_sync(0xffffffffu, m.invSt, 0);
-        m.Md = __shfl_sync(0xffffffffu, m.Md, 0);
-        m.invSd = __shfl_sync(0xffffffffu, m.invSd, 0);
-        return true;
-    };
-    auto fill_more = [&]() {
-        while (filled < handled + nstage) {
-            StageMeta m;
-            if (!next_tile(m)) break;
-            const UnitRows ur = unit_rows<EB, MODE>(p, m.unit);
-            m.b = ur.b;
-            m.pos = ur.pos;
-            m.nrows = ur.nrows;
-            fill_stage<EB, MODE>(p, ctl, dsm, filled % nstage, m, ur, lane);
-            ++filled;
-        }
-    };
-    auto push_job = [&](const Job &jb) {
-        if (lane == 0) {
-            if (job_count < kMaxJobs) {
-                ctl.jobs[(job_head + job_count) % kMaxJobs] = jb;
-                ++job_count;
-            } else {
-                atomicOr(p.status, SPEC_DEV_TIMEOUT);  // cannot happen: at most nstage + 1 draws pend
-            }
-        }
+        if (lane == 0) p.ws_seq_cnt[b] = 0u;
         __syncwarp();
     };
 
-    // ---- this CTA finished unit m.unit: merge its S partials, decide, maybe queue a draw
-    auto finalize_unit = [&](const StageMeta &m) {
-        const int b = m.b, pos = m.pos, K = p.K;
-        // one round of loads: every partial, t(x) / d(x), the draft token and uniforms
-        float v0 = neg_inf(), s0_ = 0.f, v1 = neg_inf(), s1_ = 0.f;
-        int i0 = INT_MAX, i1 = INT_MAX;
-        for (int l = lane; l < p.S; l += 32) {
+    // Every stats tile of unit u is published: merge, decide, record.
+    auto finish_unit = [&](int u, int b, int pos) {
+        const int K = p.K;
+        const int nrows = unit_nrows<MODE>(p, pos);
+        float Mr[2], Sm[2];
+        int Ar[2];
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r >= m.nrows) continue;
-                uint2 *slot = &p.ws_part[(static_cast<size_t>(m.unit) * 2 + r) * p.S + l];
-                const uint2 e = __ldcg(slot);
-                if (e.y == 0u) continue;  // no run started at this slice
-                *slot = make_uint2(0u, 0u);
-                float &v = r ? v1 : v0;
-                float &sm = r ? s1_ : s0_;
-                int &ii = r ? i1 : i0;
-                if (kSample)
-                    merge_ms(v, sm, __uint_as_float(e.x), __uint_as_float(e.y), p.c);
-                else
-                    merge_vi(v, ii, __uint_as_float(e.x), static_cast<int>(e.y) - 1);
-            }
-        }
-        int x = -1, enc = 0;
-        float ua = 0.f, ub = 0.f;
-        float2 txv = make_float2(0.f, 0.f);
-        if (lane == 0) {
-            if (MODE == kLinearSample) {
-                enc = ld_relaxed(&p.ws_first[b]);
-                if (p.u_bonus) ub = p.u_bonus[b];
-                if (pos < K) {
-                    x = p.tokens[static_cast<size_t>(b) * K + pos];
-                    ua = p.u_accept[static_cast<size_t>(b) * K + pos];
-                    txv = __ldcg(&p.ws_tx[m.unit]);
-                    p.ws_tx[m.unit] = make_float2(0.f, 0.f);
+        for (int r = 0; r < 2; ++r) {
+            float v = neg_inf(), sm = 0.f;
+            int ii = INT_MAX;
+            if (r < nrows) {
+                for (int k = lane; k < S; k += 32) {
+                    uint2 *slot = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * S + k];
+                    const uint2 e = __ldcg(slot);
+                    if (e.x == 0u && e.y == 0u) continue;  // no run starts at this tile
+                    *slot = make_uint2(0u, 0u);
+                    if (T::kSample)
+                        merge_sc(v, sm, __uint_as_float(e.x), __uint_as_float(e.y));
+                    else
+                        merge_vi(v, ii, __uint_as_float(e.x), static_cast<int>(e.y - 1u));
                 }
-            } else if (MODE == kBonusSample) {
-                if (pos >= 0) ub = p.u_bonus[b];
             }
-            p.ws_unit_cnt[m.unit] = 0u;
-        }
-        float Mr[kMaxRows], Sr[kMaxRows];
-        int Ar[kMaxRows];
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-            float v = r ? v1 : v0, sm = r ? s1_ : s0_;
-            int ii = r ? i1 : i0;
-            if (kSample) {
-                float wmax = v;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
-                if (v != wmax) sm *= ptx::ex2((v - wmax) * p.c);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
-                v = wmax;
-            } else {
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    merge_vi(v, ii, __shfl_xor_sync(0xffffffffu, v, off), __shfl_xor_sync(0xffffffffu, ii, off));
-            }
+            if (T::kSample)
+                warp_merge_sc(v, sm);
+            else
+                warp_merge_vi(v, ii);
             Mr[r] = v;
-            Sr[r] = sm;
+            Sm[r] = sm;
             Ar[r] = ii;
         }
         uint32_t fl = 0;
         bool finite = true;
-        if (kSample) {
-            for (int r = 0; r < m.nrows; ++r)
-                if (!(isfinite(Mr[r]) && isfinite(Sr[r]) && Sr[r] > 0.f)) finite = false;
+        if (T::kSample) {
+            for (int r = 0; r < nrows; ++r)
+                if (!(isfinite(Mr[r]) && isfinite(Sm[r]) && Sm[r] > 0.f)) finite = false;
             if (!finite) fl |= SPEC_DEV_NONFINITE;
-        } else if (m.nrows > 0 && Ar[0] == INT_MAX) {
+        } else if (Ar[0] == INT_MAX) {
             fl |= SPEC_DEV_NONFINITE;  // no element above -inf
             Ar[0] = 0;
         }
-        Job jb;
-        jb.unit = m.unit;
-        jb.b = b;
-        jb.pos = pos;
-        jb.nrows = m.nrows;
-        jb.next_k = 0;
-        jb.done_k = 0;
-        jb.fin = 0;
-        jb.Mt = Mr[0];
-        jb.invSt = 1.0f / Sr[0];
-        jb.Md = Mr[1];
-        jb.invSd = (m.nrows == 2) ? 1.0f / Sr[1] : 0.f;
-        jb.tailw = (m.nrows == 2) ? 0 : 1;
-        jb.ub = __shfl_sync(0xffffffffu, ub, 0);
-        int draw = 0;
         if (lane == 0) {
-            if (MODE == kLinearSample) {
-                const int early = (enc != 0 && (K + 1 - enc) < pos) ? 1 : 0;
-                if (pos < K) {
-                    float px = 0.f, qx = 0.f, thr = 0.f;
-                    int accept = 0;
-                    if (x < 0 || x >= p.V) {
-                        fl |= SPEC_DEV_BAD_TOKEN;
-                    } else {
-                        const float tx = txv.x, dx = txv.y;
-                        px = ptx::ex2((tx - Mr[0]) * p.c) / Sr[0];
-                        qx = ptx::ex2((dx - Mr[1]) * p.c) / Sr[1];
-                        const float ratio = ptx::ex2(((tx - Mr[0]) - (dx - Mr[1])) * p.c) * (Sr[1] / Sr[0]);
-                        thr = fminf(1.0f, ratio);
-                        accept = (ua < thr) ? 1 : 0;
-                    }
-                    p.ws_acc[static_cast<size_t>(b) * K + pos] = accept;
-                    if (p.probs) {
-                        float *pr = p.probs + (static_cast<size_t>(b) * K + pos) * 3;
-                        pr[0] = px;
-                        pr[1] = qx;
-                        pr[2] = thr;
-                    }
-                    if (!accept) atomicMax(&p.ws_first[b], K + 1 - pos);
-                    draw = (!accept && p.u_bonus != nullptr && !early) ? 1 : 0;
+            p.ws_unit_cnt[u] = 0u;
+            if (MODE == kLinearSample && pos < K) {
+                const float2 txv = __ldcg(&p.ws_tx[u]);
+                p.ws_tx[u] = make_float2(0.f, 0.f);
+                const int x = __ldg(&p.tokens[static_cast<size_t>(b) * K + pos]);
+                const float ua = __ldg(&p.u_accept[static_cast<size_t>(b) * K + pos]);
+                float px = 0.f, qx = 0.f, thr = 0.f;
+                int accept = 0;
+                if (x < 0 || x >= p.V) {
+                    fl |= SPEC_DEV_BAD_TOKEN;
                 } else {
-                    draw = (p.u_bonus != nullptr && !early) ? 1 : 0;  // tail: p_K
+                    const float lt = __fmaf_rn(txv.x, p.c, -Mr[0]);  // log2 of p(x) * S_t
+                    const float ld = __fmaf_rn(txv.y, p.c, -Mr[1]);
+                    px = ptx::ex2(lt) / Sm[0];
+                    qx = ptx::ex2(ld) / Sm[1];
+                    thr = fminf(1.0f, ptx::ex2(lt - ld) * (Sm[1] / Sm[0]));
+                    accept = (ua < thr) ? 1 : 0;
                 }
-                if (!finite) draw = 0;
-            } else if (MODE == kBonusSample) {
-                draw = (pos >= 0 && finite) ? 1 : 0;
-                if (pos < 0) fl |= SPEC_DEV_BAD_LENGTH;
+                p.ws_acc[static_cast<size_t>(b) * K + pos] = accept;
+                if (p.probs) {
+                    float *pr = p.probs + (static_cast<size_t>(b) * K + pos) * 3;
+                    pr[0] = px;
+                    pr[1] = qx;
+                    pr[2] = thr;
+                }
             }
+            if (draws) {
+                // a non-finite unit records 1/St = 0, which marks its draw as skipped
+                p.ws_stats[u] = finite ? make_float4(Mr[0], 1.0f / Sm[0], Mr[1], nrows == 2 ? 1.0f / Sm[1] : 0.f)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (!T::kSample) {
+                if (T::kBonus)
+                    p.bonus_token[b] = (pos < 0) ? -1 : Ar[0];
+                else
+                    p.ws_val[static_cast<size_t>(b) * p.units_per_seq + pos] = Ar[0];
+            }
+            if (T::kBonus && pos < 0) fl |= SPEC_DEV_BAD_LENGTH;
             if (fl) atomicOr(p.status, fl);
         }
-        draw = __shfl_sync(0xffffffffu, draw, 0);
-        if (draw) {
-            push_job(jb);
-        } else if (MODE == kLinearGreedy || MODE == kTreeGreedy) {
-            if (lane == 0) p.ws_val[static_cast<size_t>(b) * p.units_per_seq + pos] = Ar[0];
-            __syncwarp();
-            unit_finished<EB, MODE>(p, b, extra, lane);
-        } else if (MODE == kBonusGreedy) {
-            if (lane == 0) {
-                if (pos < 0) atomicOr(p.status, SPEC_DEV_BAD_LENGTH);
-                p.bonus_token[b] = (pos < 0) ? -1 : Ar[0];
-            }
-        } else if (MODE == kBonusSample) {
-            if (lane == 0) p.bonus_token[b] = (pos < 0) ? -1 : 0;
-        } else {  // linear sampling without a draw here
-            unit_finished<EB, MODE>(p, b, extra, lane);
+        __syncwarp();
+        if (T::kBonus) {
+            if (T::kSample) push_entry(u, nrows == 2, pos < 0 || !finite);
+            return;
         }
-    };
-    // consume the previous stats tile's counter increment (issued a tile ago)
-    auto resolve_pending = [&]() {
-        if (!pend_valid) return;
-        pend_valid = false;
-        const int last =
-            __shfl_sync(0xffffffffu, (pend_old + static_cast<unsigned>(pend_cnt) == static_cast<unsigned>(p.S)) ? 1 : 0, 0);
-        if (last) {
-            __syncwarp();
-            finalize_unit(pend_m);
-        }
+        int last = 0;
+        if (lane == 0)
+            last = (atom_add_acq_rel(&p.ws_seq_cnt[b], 1u) == static_cast<unsigned>(p.units_per_seq - 1)) ? 1 : 0;
+        last = __shfl_sync(kFull, last, 0);
+        __syncwarp();
+        if (last) finish_sequence(b);
     };
 
-    // write the current run's merged partial, count its tiles (the increment is consumed later)
-    auto publish_run = [&]() {
-        const int have = __shfl_sync(0xffffffffu, run_unit, 0);
-        if (have < 0) return;
-        resolve_pending();
-        const StageMeta rm = run_m;
-        if (lane == 0) {
+    // Chunk sums of every residual slice of unit (b, pos) with weights p
+    // alone, read from global memory (the rare redraw after a vanished residual).
+    auto resid_from_global = [&](int e, int b, int pos, const float4 &js) {
+        const unsigned char *rt = row_ptr<EB>(p, b, pos, 0);
+        long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
+        for (int k = 0; k < p.Sr; ++k) {
+            const int s0 = k * p.Lr;
+            const int s1 = min(p.V, s0 + p.Lr);
+            const Geo g = make_geo<EB>(rt, s0, s1, p.target, p.t_end);
+            long long q[kCpt];
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r)
-                if (r < rm.nrows) p.ws_part[(static_cast<size_t>(run_unit) * 2 + r) * p.S + run_k0] = run_part[r];
-            if (run_hasx) p.ws_tx[run_unit] = run_x;
-            pend_old = atom_add_acq_rel(&p.ws_unit_cnt[run_unit], static_cast<unsigned>(run_cnt));
-            pend_cnt = run_cnt;
-            run_unit = -1;
+            for (int c = 0; c < kCpt; ++c) q[c] = 0;
+#pragma unroll
+            for (int h = 0; h < (kCpt * kChunk) / 32; ++h) {
+                const int gi = h * 32 + lane;
+                float sw = 0.f;
+#pragma unroll
+                for (int k2 = 0; k2 < G; ++k2) {
+                    const int v = g.vbase + gi * G + k2;
+                    float w = 0.f;
+                    if (gi < g.ngran && v >= s0 && v < s1)
+                        w = elem_weight(Elt<EB>::gload(rt + static_cast<size_t>(v) * EB), 0.f, false, js, p.c);
+                    sw += w;
+                }
+                q[h / 2] += fixq(sw);
+            }
+#pragma unroll
+            for (int c = 0; c < kCpt; ++c) {
+                const long long t = warp_sum64(q[c]);
+                if (lane == 0) cs[k * kCpt + c] = t;
+            }
         }
-        pend_valid = true;
-        pend_m = rm;
+        __syncwarp();
     };
 
-    fill_more();
-    for (;;) {
-        if (filled == handled) {
-            publish_run();
-            resolve_pending();
-            fill_more();
-            if (filled == handled) break;  // nothing in flight and nothing left
+    // Locate the extra token of entry e; -1 when the weights sum to zero.
+    auto select_token = [&](int e, int b, int pos, bool pair, const float4 &js, float ub) -> int {
+        const int n = p.Sr * kCpt;
+        const long long *cs = p.ws_csum + static_cast<size_t>(e) * n;
+        const int per = (n + 31) / 32;
+        const int lo = min(n, lane * per), hi = min(n, lo + per);
+        long long mine = 0;
+        for (int i = lo; i < hi; ++i) mine += __ldcg(&cs[i]);
+        long long incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += y;
         }
-        const int s = handled % nstage;
-        if (!wait_bar(ptx::smem_addr(&ctl.done[s]), static_cast<uint32_t>(handled / nstage) & 1u)) {
-            timed_out = true;
-            break;
+        const long long tot = __shfl_sync(kFull, incl, 31);
+        if (tot <= 0) return -1;
+        const double ud = (ub >= 0.f) ? static_cast<double>(ub) : 0.0;  // a NaN uniform counts as 0
+        long long target = static_cast<long long>(ud * static_cast<double>(tot));
+        if (target >= tot) target = tot - 1;
+        // the chunk holding the target: first lane, then first chunk in that lane's block
+        const unsigned bl = __ballot_sync(kFull, incl > target);
+        const int ol = __ffs(bl) - 1;
+        long long acc = __shfl_sync(kFull, incl - mine, ol);
+        int chunk = -1;
+        if (lane == ol) {
+            long long a = acc;
+            for (int i = lo; i < hi; ++i) {
+                const long long ci = __ldcg(&cs[i]);
+                if (a + ci > target) {
+                    chunk = i;
+                    break;
+                }
+                a += ci;
+            }
+            acc = a;
         }
-        const StageMeta m = ctl.meta[s];
-        ++handled;
-        if (m.kind != kTileStats) {
-            publish_run();
-            resolve_pending();
+        chunk = __shfl_sync(kFull, chunk, ol);
+        acc = __shfl_sync(kFull, acc, ol);
+        const long long rem = target - acc;  // 0 <= rem < cs[chunk]
+        // rescan that chunk from global memory with the same weights and order
+        const int k = chunk / kCpt;
+        const int cc = chunk - k * kCpt;
+        const int s0 = k * p.Lr;
+        const int s1 = min(p.V, s0 + p.Lr);
+        const unsigned char *rt = row_ptr<EB>(p, b, pos, 0);
+        const unsigned char *rd = pair ? row_ptr<EB>(p, b, pos, 1) : rt;
+        const Geo gt = make_geo<EB>(rt, s0, s1, p.target, p.t_end);
+        long long q[2];
+        float w[2][G];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int g = cc * kChunk + h * 32 + lane;
+            float sw = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < G; ++k2) {
+                const int v = gt.vbase + g * G + k2;
+                float we = 0.f;
+                if (g < gt.ngran && v >= s0 && v < s1) {
+                    const float t = Elt<EB>::gload(rt + static_cast<size_t>(v) * EB);
+                    const float d = pair ? Elt<EB>::gload(rd + static_cast<size_t>(v) * EB) : 0.f;
+                    we = elem_weight(t, d, pair, js, p.c);
+                }
+                w[h][k2] = we;
+                sw += we;
+            }
+            q[h] = fixq(sw);
         }
-        if (m.kind == kTileStats) {
-            // ---- CTA partial of this tile -> workspace (the max first, then one rescale per warp)
-            uint2 part[kMaxRows];
+        long long i0 = q[0], i1 = q[1];
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r >= m.nrows) continue;
-                float v = lane < kComputeWarps ? ctl.wm[s][r][lane] : neg_inf();
-                if (kSample) {
-                    float sum = lane < kComputeWarps ? ctl.wsum[s][r][lane] : 0.f;
-                    float wmax = v;
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y0 = __shfl_up_sync(kFull, i0, off);
+            const long long y1 = __shfl_up_sync(kFull, i1, off);
+            if (lane >= off) {
+                i0 += y0;
+                i1 += y1;
+            }
+        }
+        i1 += __shfl_sync(kFull, i0, 31);
+        unsigned bh = __ballot_sync(kFull, i0 > rem);
+        int half = 0;
+        if (!bh) {
+            bh = __ballot_sync(kFull, i1 > rem);
+            half = 1;
+        }
+        int token = -1;
+        if (bh) {
+            const int gl = __ffs(bh) - 1;
+            const long long excl = __shfl_sync(kFull, half ? (i1 - q[1]) : (i0 - q[0]), gl);
+            if (lane == gl) {
+                const int g = cc * kChunk + half * 32 + lane;
+                float cum = 0.f;
+                int esel = -1;
 #pragma unroll
-                    for (int off = 4; off > 0; off >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, off));
-                    if (v != wmax) sum *= ptx::ex2((v - wmax) * p.c);
-#pragma unroll
-                    for (int off = 4; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                    part[r] = make_uint2(__float_as_uint(wmax), __float_as_uint(sum));
-                } else {
-                    int i = lane < kComputeWarps ? ctl.wi[s][r][lane] : INT_MAX;
-#pragma unroll
-                    for (int off = 4; off > 0; off >>= 1)
-                        merge_vi(v, i, __shfl_xor_sync(0xffffffffu, v, off), __shfl_xor_sync(0xffffffffu, i, off));
-                    part[r] = make_uint2(__float_as_uint(v), static_cast<unsigned>(i) + 1u);  // +1: never 0
+                for (int k2 = 0; k2 < G; ++k2) {
+                    cum += half ? w[1][k2] : w[0][k2];
+                    if (esel < 0 && excl + fixq(cum) > rem) esel = k2;
                 }
+                token = gt.vbase + g * G + (esel < 0 ? G - 1 : esel);
             }
-            const int has_x = (MODE == kLinearSample) ? ctl.xhas[s] : 0;
-            const float2 xv = ctl.xval[s];
-            fill_more();  // refill first: the publication below waits on its own stores
-            const int same = __shfl_sync(0xffffffffu, (run_unit == m.unit && run_k0 + run_cnt == m.k) ? 1 : 0, 0);
-            if (!same) publish_run();
-            if (lane == 0) {
-                if (!same) {
-                    run_unit = m.unit;
-                    run_k0 = m.k;
-                    run_cnt = 0;
-                    run_hasx = 0;
-#pragma unroll
-                    for (int r = 0; r < kMaxRows; ++r) run_part[r] = part[r];
-                } else {
-#pragma unroll
-                    for (int r = 0; r < kMaxRows; ++r) {
-                        if (r >= m.nrows) continue;
-                        float v = __uint_as_float(run_part[r].x);
-                        if (kSample) {
-                            float sm = __uint_as_float(run_part[r].y);
-                            merge_ms(v, sm, __uint_as_float(part[r].x), __uint_as_float(part[r].y), p.c);
-                            run_part[r] = make_uint2(__float_as_uint(v), __float_as_uint(sm));
-                        } else {
-                            int ii = static_cast<int>(run_part[r].y) - 1;
-                            merge_vi(v, ii, __uint_as_float(part[r].x), static_cast<int>(part[r].y) - 1);
-                            run_part[r] = make_uint2(__float_as_uint(v), static_cast<unsigned>(ii) + 1u);
-                        }
-                    }
-                }
-                run_cnt += 1;
-                if (has_x) {
-                    run_hasx = 1;
-                    run_x = xv;
-                }
-            }
-            if (!same) run_m = m;
-        } else if (kSample) {
-            // ---- a residual tile of a pending draw is reduced
-            Job jb = ctl.jobs[m.job];
-            __syncwarp();
-            int finished = 0;
-            if (lane == 0) {
-                ctl.jobs[m.job].done_k += 1;
-                finished = (ctl.jobs[m.job].done_k == p.S) ? 1 : 0;
-            }
-            finished = __shfl_sync(0xffffffffu, finished, 0);
-            if (!finished) {
-                fill_more();
-                continue;
-            }
-            __syncwarp();
-            const int token = select_token<EB, MODE>(p, jb, extra + static_cast<size_t>(m.job) * job_stride, lane);
-            if (token < 0 && !jb.tailw) {
+            token = __shfl_sync(kFull, token, gl);
+        }
+        return token < 0 ? 0 : token;
+    };
+
+    // Every residual tile of entry e is summed: draw, emit, and clean up.
+    auto finish_entry = [&](int e) {
+        const uint32_t rec = __ldcg(&p.ws_rq[e]);
+        const int u = static_cast<int>(rec & kRecUnit) - 1;
+        const bool pair = (rec & kRecPair) != 0;
+        const bool skip = (rec & kRecSkip) != 0;
+        int b, pos;
+        if (T::kBonus) {
+            b = u;
+            pos = bonus_pos(p, b);
+        } else {
+            b = u / p.units_per_seq;
+            pos = u - b * p.units_per_seq;
+        }
+        int token = 0;
+        if (!skip) {
+            const float4 js = __ldcg(&p.ws_stats[u]);
+            const float ub = __ldg(&p.u_bonus[b]);
+            token = select_token(e, b, pos, pair, js, ub);
+            if (token < 0 && pair) {
                 // the residual vanished through rounding: draw from p_j instead
-                if (lane == 0) {
-                    atomicOr(p.status, SPEC_DEV_ZERO_RESIDUAL);
-                    ctl.jobs[m.job].tailw = 1;
-                    ctl.jobs[m.job].next_k = 0;
-                    ctl.jobs[m.job].done_k = 0;
+                if (lane == 0) atomicOr(p.status, SPEC_DEV_ZERO_RESIDUAL);
+                resid_from_global(e, b, pos, js);
+                token = select_token(e, b, pos, false, js, ub);
+            }
+            if (token < 0) token = 0;
+        }
+        if (T::kBonus) {
+            if (lane == 0) p.bonus_token[b] = (pos < 0) ? -1 : token;
+        } else {
+            emit_linear(b, pos, token, true);
+        }
+        // leave the workspace zeroed
+        long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
+        for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0;
+        if (T::kBonus) {
+            if (lane == 0) p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (int i = lane; i < p.units_per_seq; i += 32)
+                p.ws_stats[static_cast<size_t>(b) * p.units_per_seq + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (lane == 0) {
+            p.ws_rq[e] = 0u;
+            p.ws_res_cnt[e] = 0u;
+        }
+        __syncwarp();
+    };
+
+    // consume the pending counter increment
+    auto resolve_pending = [&]() {
+        if (pend_kind == 0) return;
+        const int kind = pend_kind;
+        pend_kind = 0;
+        int last = 0;
+        if (lane == 0) {
+            const unsigned now = pend_old + static_cast<unsigned>(pend_add);
+            if (kind == 1)
+                last = (now == static_cast<unsigned>(unit_nrows<MODE>(p, pend_pos) * S)) ? 1 : 0;
+            else
+                last = (now == static_cast<unsigned>(p.Sr)) ? 1 : 0;
+        }
+        last = __shfl_sync(kFull, last, 0);
+        if (!last) return;
+        fence_acquire();  // every partial counted so far is visible from here on
+        __syncwarp();
+        if (kind == 1)
+            finish_unit(pend_unit, pend_b, pend_pos);
+        else
+            finish_entry(pend_entry);
+    };
+
+    // close the run: publish its partial (stats) and count its tiles
+    auto close_run = [&]() {
+        if (run_kind == 0) return;
+        if (run_kind == kTileStats) {
+            if (T::kSample)
+                warp_merge_sc(am, as);
+            else
+                warp_merge_vi(am, ai);
+        }
+        resolve_pending();
+        if (run_kind == kTileStats) {
+            if (lane == 0) {
+                const uint2 part = T::kSample ? make_uint2(__float_as_uint(am), __float_as_uint(as))
+                                              : make_uint2(__float_as_uint(am), static_cast<unsigned>(ai) + 1u);
+                p.ws_part[(static_cast<size_t>(prow.unit) * 2 + prow.r) * S + run_k0] = part;
+                if (hasx) reinterpret_cast<float *>(&p.ws_tx[prow.unit])[prow.r] = xval;
+                pend_old = atom_add_release(&p.ws_unit_cnt[prow.unit], static_cast<unsigned>(run_len));
+            }
+            pend_kind = 1;
+            pend_unit = prow.unit;
+            pend_b = prow.b;
+            pend_pos = prow.pos;
+        } else {
+            if (lane == 0) pend_old = atom_add_release(&p.ws_res_cnt[r_e], static_cast<unsigned>(run_len));
+            pend_kind = 2;
+            pend_entry = r_e;
+        }
+        pend_add = run_len;
+        run_kind = 0;
+        run_next = -1;
+    };
+
+    // ------------------------------------------------------------ main loop
+    int hslot = 0;                     // stage of the next tile to reduce
+    uint32_t hphase = 0;               // its mbarrier phase parity
+    fill_ring();
+    for (;;) {
+        if (issued == handled) {
+            // nothing in flight: settle before anything that may wait
+            close_run();
+            resolve_pending();
+            if (!try_issue(true)) break;
+            fill_ring();
+        }
+        const int s = hslot;
+        const int4 d = wc.desc[s];
+        unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
+        const uint32_t bar = ptx::smem_addr(&wc.full[s]);
+        const uint32_t parity = hphase;
+        const long long idx = static_cast<unsigned>(d.y);
+        if (run_kind != 0 && (d.x != run_kind || idx != run_next)) close_run();
+        if (d.x == kTileStats) {
+            int k;
+            if (run_kind == kTileStats) {
+                k = run_k0 + run_len;  // continues the run
+            } else {
+                const int id = static_cast<int>(static_cast<unsigned>(idx) / static_cast<unsigned>(S));
+                k = static_cast<int>(idx) - id * S;
+                if (id != prow.id) prow = decode_row(id);
+            }
+            if (run_kind == 0) {
+                run_kind = kTileStats;
+                run_k0 = k;
+                run_len = 0;
+                am = neg_inf();
+                as = 0.f;
+                ai = INT_MAX;
+                hasx = 0;
+                xval = 0.f;
+                px = -1;
+                if (MODE == kLinearSample && prow.pos < p.K) {
+                    const int x = __ldg(&p.tokens[static_cast<size_t>(prow.b) * p.K + prow.pos]);
+                    px = (x >= 0 && x < p.V) ? x : -1;
+                }
+            }
+            if (!wait_bar(bar, parity)) {
+                timed_out = true;
+                break;
+            }
+            uintptr_t w0, w1, c0, c1;
+            tile_window(prow, k, w0, w1, c0, c1);
+            const int ngran = static_cast<int>((w1 - w0) >> 4);
+            const int vbase = static_cast<int>((static_cast<long long>(w0) - static_cast<long long>(prow.R0)) / EB);
+            const uintptr_t R1 = prow.R0 + row_bytes;
+            const bool patch = ngran > 0 && (w0 < prow.R0 || w1 > R1 || c0 > w0 || c1 < w1);
+            if (patch) {
+                if (lane < 16) {
+                    Geo g;
+                    g.glo = reinterpret_cast<const unsigned char *>(w0);
+                    g.ngran = ngran;
+                    g.c0 = static_cast<int>(c0 - w0);
+                    g.c1 = static_cast<int>(c1 - w0);
+                    g.a0 = w0 < prow.R0 ? static_cast<int>(prow.R0 - w0) : 0;
+                    g.a1 = static_cast<int>((R1 < w1 ? R1 : w1) - w0);
+                    g.vbase = vbase;
+                    g.patch = true;
+                    patch_row<EB>(buf, g, lane);
                 }
                 __syncwarp();
-                fill_more();
-                continue;
             }
-            // the draw is done; drop finished draws from the head of the FIFO
-            if (lane == 0) {
-                ctl.jobs[m.job].fin = 1;
-                while (job_count > 0 && ctl.jobs[job_head].fin) {
-                    job_head = (job_head + 1) % kMaxJobs;
-                    --job_count;
+            if (T::kSample)
+                lane_sum<EB>(buf, ngran, p.c, lane, am, as);
+            else
+                lane_argmax<EB>(buf, ngran, vbase, lane, am, ai);
+            if (px >= 0) {
+                const int off = px - vbase;
+                if (off >= 0 && off < ngran * G) {
+                    hasx = 1;
+                    xval = Elt<EB>::load(buf + off * EB);
                 }
             }
             __syncwarp();
-            token_drawn<EB, MODE>(p, jb, token < 0 ? 0 : token, extra, lane);
-            fill_more();
+            if (patch) fence_proxy_async();  // generic writes to this stage precede its next bulk copy
+            ++run_len;
+            run_next = (k + 1 < S) ? idx + 1 : -1;
+        } else {
+            // ---- a residual tile
+            const uint32_t rec = static_cast<uint32_t>(d.z);
+            const int e = static_cast<int>(idx / p.Sr);
+            const int k = static_cast<int>(idx - static_cast<long long>(e) * p.Sr);
+            if (run_kind == 0) {
+                run_kind = kTileResid;
+                run_k0 = k;
+                run_len = 0;
+                r_e = e;
+                r_pair = (rec & kRecPair) != 0;
+                r_skip = (rec & kRecSkip) != 0;
+                entry_unit(rec, r_u, r_b, r_pos);
+                if (!r_skip) {
+                    if (lane == 0) (void)ld_acquire(&p.ws_rq[e]);  // orders the loads of the entry's statistics
+                    __syncwarp();
+                    r_js = __ldcg(&p.ws_stats[r_u]);
+                }
+            }
+            if (!wait_bar(bar, parity)) {
+                timed_out = true;
+                break;
+            }
+            long long q[kCpt];
+#pragma unroll
+            for (int c = 0; c < kCpt; ++c) q[c] = 0;
+            bool patched = false;
+            if (!r_skip) {
+                const int s0 = k * p.Lr;
+                const int s1 = min(p.V, s0 + p.Lr);
+                const Geo g0 = make_geo<EB>(row_ptr<EB>(p, r_b, r_pos, 0), s0, s1, p.target, p.t_end);
+                Geo g1 = g0;
+                if (r_pair) g1 = make_geo<EB>(row_ptr<EB>(p, r_b, r_pos, 1), s0, s1, p.draft, p.d_end);
+                patched = g0.patch || (r_pair && g1.patch);
+                if (patched) {
+                    if (lane < 16) {
+                        if (g0.patch) patch_row<EB>(buf, g0, lane);
+                    } else if (r_pair && g1.patch) {
+                        patch_row<EB>(buf + kRowBuf, g1, lane - 16);
+                    }
+                    __syncwarp();
+                }
+                tile_resid<EB>(buf, g0.ngran, g0.vbase, g1.vbase, s0, s1, r_pair, g0.vbase == g1.vbase, r_js, p.c,
+                               lane, q);
+            }
+            __syncwarp();
+            if (patched) fence_proxy_async();
+            if (lane == 0) {
+                long long *dst = p.ws_csum + (static_cast<size_t>(e) * p.Sr + k) * kCpt;
+#pragma unroll
+                for (int c = 0; c < kCpt; ++c) dst[c] = q[c];
+            }
+            ++run_len;
+            run_next = (k + 1 < p.Sr) ? idx + 1 : -1;
         }
+        ++handled;
+        if (++hslot == NS) {
+            hslot = 0;
+            hphase ^= 1u;
+        }
+        fill_ring();
+        resolve_pending();
+        // close the run now unless the next tile in the ring continues it
+        bool cont = false;
+        if (run_next >= 0 && issued > handled) {
+            const int4 nd = wc.desc[hslot];
+            cont = nd.x == run_kind && static_cast<long long>(static_cast<unsigned>(nd.y)) == run_next;
+        }
+        if (!cont) close_run();
     }
 
-    // ---- end of the stream: release the compute warps, account for the CTA
-    if (!timed_out) {
-        const int s = filled % nstage;
-        if (lane == 0) {
-            StageMeta e{};
-            e.kind = kTileEnd;
-            ctl.meta[s] = e;
-            mbar_arrive(ptx::smem_addr(&ctl.full[s]));
-            mbar_arrive(ptx::smem_addr(&ctl.full[s]));
-        }
-    }
-    if (lane == 0) {
-        if (timed_out || ctl.timed_out) atomicOr(p.status, SPEC_DEV_TIMEOUT);
+    if (lane == 0 && timed_out) atomicOr(p.status, SPEC_DEV_TIMEOUT);
+    // ---- the last CTA to finish leaves the counters zeroed
+    __syncthreads();
+    if (threadIdx.x == 0) {
         if (atom_add_acq_rel(&p.ws_ctrl[1], 1u) == gridDim.x - 1) {
-            p.ws_ctrl[0] = 0u;  // the last CTA leaves the tile counter zeroed
+            p.ws_ctrl[0] = 0u;
             p.ws_ctrl[1] = 0u;
+            p.ws_ctrl[2] = 0u;
+            p.ws_ctrl[3] = 0u;
         }
     }
-    (void)kBonus;
 }
 
 }  // namespace spec
