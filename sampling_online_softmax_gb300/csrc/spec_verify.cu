@@ -55,9 +55,7 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         g_dev[dev].sms = sms;
-        g_dev[dev].max_dyn = static_cast<size_t>(smem) > sizeof(WarpCtl) * kWarps + 1024
-                                 ? static_cast<size_t>(smem) - sizeof(WarpCtl) * kWarps - 1024
-                                 : 0;
+        g_dev[dev].max_dyn = static_cast<size_t>(smem);  // less each kernel's static shared memory
     });
     *out = g_dev[dev];
     *dev_out = dev;
@@ -72,6 +70,7 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
 int stats_tiles_per_row(int V, int eb) {
     return static_cast<int>((static_cast<long long>(V) * eb + 30 + kTileBytes - 1) / kTileBytes);
 }
+int segments_per_row(int V, int eb) { return (stats_tiles_per_row(V, eb) + kSegTiles - 1) / kSegTiles; }
 
 // Residual slices of a row: at most kResidSliceBytes each, a whole number of
 // 16-byte groups long, none empty.  A function of V and the element size only.
@@ -91,23 +90,25 @@ Slicing resid_slicing(int V, int eb) {
 
 // Workspace layout (16-byte aligned parts):
 //   [counters: 4 u32][stats tiles per unit: n_units u32][units per sequence: B u32]
-//   [accept bits: B*K i32][argmax: n_units i32][run partials: n_units*2*S uint2]
-//   [t(x), d(x): n_units float2][draw statistics: n_units float4]
+//   [decided / accepted masks: B u64]
+//   [accept bits: B*K i32][argmax: n_units i32][segment partials: n_units*2*nseg uint2]
+//   [t(x), d(x): n_units * 2 u64][draw statistics: n_units float4]
 //   [draw entries: B u32][residual tiles per entry: B u32][chunk sums: B*Sr*kCpt i64]
 struct WsLayout {
-    size_t ctrl, unit_cnt, seq_cnt, acc, val, part, tx, stats, rq, res_cnt, csum, total;
+    size_t ctrl, unit_cnt, seq_cnt, seqmask, acc, val, part, tx, stats, rq, res_cnt, csum, total;
 };
-WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, bool draws) {
+WsLayout ws_layout(int B, int K, int units_per_seq, int nseg, int Sr, bool draws) {
     const size_t n_units = static_cast<size_t>(B) * units_per_seq;
     WsLayout w;
     w.ctrl = 0;
     w.unit_cnt = 16;
     w.seq_cnt = w.unit_cnt + align16(n_units * 4);
-    w.acc = w.seq_cnt + align16(static_cast<size_t>(B) * 4);
+    w.seqmask = w.seq_cnt + align16(static_cast<size_t>(B) * 4);
+    w.acc = w.seqmask + align16(static_cast<size_t>(B) * 8);
     w.val = w.acc + align16(static_cast<size_t>(B) * K * 4);
     w.part = w.val + align16(n_units * 4);
-    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
-    w.stats = w.tx + align16(n_units * 8);
+    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(nseg) * 8);
+    w.stats = w.tx + align16(n_units * 16);
     const size_t entries = draws ? static_cast<size_t>(B) : 0;
     w.rq = w.stats + (draws ? align16(n_units * 16) : 0);
     w.res_cnt = w.rq + align16(entries * 4);
@@ -120,24 +121,25 @@ void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
     p.ws_ctrl = reinterpret_cast<uint32_t *>(ws + wl.ctrl);
     p.ws_unit_cnt = reinterpret_cast<uint32_t *>(ws + wl.unit_cnt);
     p.ws_seq_cnt = reinterpret_cast<uint32_t *>(ws + wl.seq_cnt);
+    p.ws_seqmask = reinterpret_cast<unsigned long long *>(ws + wl.seqmask);
     p.ws_acc = reinterpret_cast<int32_t *>(ws + wl.acc);
     p.ws_val = reinterpret_cast<int32_t *>(ws + wl.val);
-    p.ws_part = reinterpret_cast<uint2 *>(ws + wl.part);
-    p.ws_tx = reinterpret_cast<float2 *>(ws + wl.tx);
+    p.ws_part = reinterpret_cast<unsigned long long *>(ws + wl.part);
+    p.ws_txw = reinterpret_cast<unsigned long long *>(ws + wl.tx);
     p.ws_stats = reinterpret_cast<float4 *>(ws + wl.stats);
     p.ws_rq = reinterpret_cast<uint32_t *>(ws + wl.rq);
     p.ws_res_cnt = reinterpret_cast<uint32_t *>(ws + wl.res_cnt);
-    p.ws_csum = reinterpret_cast<long long *>(ws + wl.csum);
+    p.ws_csum = reinterpret_cast<unsigned long long *>(ws + wl.csum);
 }
 
 WsLayout layout_linear(int B, int K, int V, int eb) {
-    return ws_layout(B, K, K + 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
+    return ws_layout(B, K, K + 1, segments_per_row(V, eb), resid_slicing(V, eb).S, true);
 }
 WsLayout layout_bonus(int B, int V, int eb) {
-    return ws_layout(B, 0, 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
+    return ws_layout(B, 0, 1, segments_per_row(V, eb), resid_slicing(V, eb).S, true);
 }
 WsLayout layout_tree(int B, int N, int V, int eb) {
-    return ws_layout(B, 0, N, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, false);
+    return ws_layout(B, 0, N, segments_per_row(V, eb), resid_slicing(V, eb).S, false);
 }
 
 // Resident blocks per SM for this kernel and shared-memory size (cached).
@@ -167,22 +169,28 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     if (st != SPEC_OK) return st;
     auto kernel = spec_verify_kernel<EB, MODE>;
     {
-        // per device and kernel, once: allow the largest dynamic shared memory
-        static bool configured[kMaxDevices] = {};
+        // per device and kernel, once: allow the largest dynamic shared memory next to the static part
+        static size_t max_dyn[kMaxDevices] = {};
         std::lock_guard<std::mutex> lock(g_attr_mutex);
-        if (!configured[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(di.max_dyn));
+        if (max_dyn[dev] == 0) {
+            cudaFuncAttributes fa;
+            cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kernel));
+            if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+            if (fa.sharedSizeBytes >= di.max_dyn) return fail(SPEC_ERR_UNSUPPORTED, "static shared memory too large");
+            const size_t m = di.max_dyn - fa.sharedSizeBytes;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(m));
             if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            configured[dev] = true;
+            max_dyn[dev] = m;
         }
+        di.max_dyn = max_dyn[dev];
     }
     Params p = p0;
     const Slicing rs = resid_slicing(p.V, EB);
     p.S = stats_tiles_per_row(p.V, EB);
+    p.nseg = segments_per_row(p.V, EB);
     p.Sr = rs.S;
     p.Lr = rs.L;
-    p.stats_tiles = static_cast<long long>(p.B) * p.rows_per_seq * p.S;
+    p.stats_segs = static_cast<long long>(p.B) * p.rows_per_seq * p.nseg;
     p.res_tiles = draws ? static_cast<long long>(p.B) * p.Sr : 0;
     // ring depth: the deepest ring that keeps kMinCtas CTAs on an SM
     const size_t scratch = (MODE == kTreeGreedy) ? static_cast<size_t>(kWarps) * 3 * p.units_per_seq * 4 : 0;
@@ -202,10 +210,10 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     if (per_sm <= 0) return fail(SPEC_ERR_UNSUPPORTED, "kernel does not fit an SM (N=%d)", p.units_per_seq);
     p.nstage = ns;
     // enough CTAs for every warp to get a tile, at most what is resident at once
-    const long long want = std::max<long long>(1, (p.stats_tiles + kWarps - 1) / kWarps);
+    const long long want = std::max<long long>(1, (p.stats_segs + kWarps - 1) / kWarps);
     const long long grid = std::min<long long>(want, static_cast<long long>(per_sm) * di.sms);
     const long long warps = grid * kWarps;
-    if (p.stats_tiles + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxGrab >= (1ll << 31))
+    if (p.stats_segs + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxClaim >= (1ll << 31))
         return fail(SPEC_ERR_UNSUPPORTED, "too many tiles (B=%d, V=%d)", p.B, p.V);
     spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, dyn, stream>>>(p);
     cudaError_t e = cudaGetLastError();

@@ -69,8 +69,10 @@ constexpr int kStageBytes = 2 * kRowBuf;
 constexpr int kChunk = 64;                           // 16-byte groups per residual chunk
 constexpr int kCpt = (kResidSliceBytes / 16 + 2 + kChunk - 1) / kChunk;  // residual chunks per tile
 static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout");
-constexpr int kMaxGrab = 32;            // stats tiles taken from the global counter at once (at most)
-constexpr int kMaxClaim = 8;            // residual tiles claimed at once (at most)
+constexpr int kSegTiles = 4;            // stats tiles per segment: one partial each, never split between warps
+constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
+constexpr int kMaxClaim = 4;            // residual tiles claimed at once (at most)
+constexpr int kHintEvery = 1;           // tiles between looks at the residual counters
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr unsigned kFull = 0xffffffffu;
@@ -101,9 +103,10 @@ struct Params {
     int units_per_seq;             // K+1 (linear), N (tree), 1 (extra token alone)
     int n_units;
     int S;                         // stats tiles per row (windows of kTileBytes on the 16-byte grid)
+    int nseg;                      // segments per row: ceil(S / kSegTiles)
     int Sr, Lr;                    // residual slices per entry, elements per slice
     int nstage;                    // stages per warp ring (2..kMaxStages)
-    long long stats_tiles;         // B * rows_per_seq * S
+    long long stats_segs;          // B * rows_per_seq * nseg
     long long res_tiles;           // (draw entries: B or 0) * Sr
     float c;                       // log2(e) / T  (sampling modes)
     const int32_t *tokens;         // [B, K] draft tokens, or [B, N] node tokens
@@ -119,17 +122,18 @@ struct Params {
     int32_t *path_nodes;           // [B, max_depth+1]
     int32_t *bonus_token;          // [B]
     uint32_t *status;              // [1]
-    uint32_t *ws_ctrl;             // [0] stats tiles taken, [1] CTAs finished, [2] draw entries, [3] residual tiles taken
+    uint32_t *ws_ctrl;             // [0] stats segments taken, [1] CTAs finished, [2] draw entries, [3] residual tiles taken
     uint32_t *ws_unit_cnt;         // [n_units] stats tiles published per unit
-    uint32_t *ws_seq_cnt;          // [B] units decided per sequence
+    uint32_t *ws_seq_cnt;          // [B] units decided per sequence (K >= 32 and trees)
+    unsigned long long *ws_seqmask;  // [B] decided bits 0..31, accepted bits 32..63 (linear, K < 32)
     int32_t *ws_acc;               // [B*K] accept bits
     int32_t *ws_val;               // [B*units_per_seq] argmax per unit (greedy)
-    uint2 *ws_part;                // [n_units * 2 * S] run partials (slot = the run's first tile)
-    float2 *ws_tx;                 // [n_units] target and draft logit of the draft token
+    unsigned long long *ws_part;   // [n_units * 2 * nseg] segment partials: (mc | s << 32) or (max | (index + 1) << 32)
+    unsigned long long *ws_txw;    // [n_units * 2] the draft token's logit in each row: bits | 1 << 32
     float4 *ws_stats;              // [n_units] (MCt, 1/St, MCd, 1/Sd) of units that may draw
     uint32_t *ws_rq;               // [B] draw entries
     uint32_t *ws_res_cnt;          // [B] residual tiles finished per entry
-    long long *ws_csum;            // [B * Sr * kCpt] residual chunk sums
+    unsigned long long *ws_csum;   // [B * Sr * kCpt] residual chunk sums, stored plus one
 };
 
 // One stage's tile: {kTileStats, tile} or {kTileResid, residual tile, entry record}.
@@ -152,7 +156,47 @@ __device__ __forceinline__ unsigned atom_add_release(uint32_t *p, unsigned v) {
     asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+__device__ __forceinline__ unsigned long long atom_or_acq_rel64(unsigned long long *p, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+// First rejected position of a sequence once it is known from a decided /
+// accepted mask (every earlier position decided and accepted), K when every
+// position 0..K is decided and none rejected, else -1.  K < 32.
+__device__ __forceinline__ int first_rejection(unsigned long long m, int K) {
+    const unsigned dec = static_cast<unsigned>(m);
+    const unsigned acc = static_cast<unsigned>(m >> 32);
+    const unsigned rej = dec & ~acc & ((1u << K) - 1u);
+    const int f = __ffs(~dec) - 1;  // first undecided position, -1 if none
+    if (rej) {
+        const int j = __ffs(rej) - 1;
+        return (f < 0 || j < f) ? j : -1;
+    }
+    const unsigned all = (K + 1 == 32) ? 0xffffffffu : ((1u << (K + 1)) - 1u);
+    return ((dec & all) == all) ? K : -1;
+}
 __device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Values another warp writes exactly once per call, never as zero: a relaxed
+// 64-bit store is seen whole, so a reader that finds zero simply looks again.
+// This spares the writers a release fence on the hot path.
+__device__ __forceinline__ void st_relaxed64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long await64(const unsigned long long *p, bool &late) {
+    unsigned long long v = ld_relaxed64(p);
+    for (uint32_t i = 0; v == 0ull && i < kSpinLimit; ++i) {
+        __nanosleep(32);
+        v = ld_relaxed64(p);
+    }
+    if (v == 0ull) late = true;
+    return v;
+}
 __device__ __forceinline__ unsigned ld_relaxed(const uint32_t *p) {
     unsigned v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -581,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     }
     __syncwarp();
 
-    const long long ST = p.stats_tiles;
+    const long long NSEG = p.stats_segs;
     const long long RT = p.res_tiles;
     const int S = p.S;
     const size_t row_bytes = static_cast<size_t>(p.V) * EB;
@@ -599,8 +643,27 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     auto decode_row = [&](int id) -> Row {
         Row t;
         t.id = id;
-        t.b = id / p.rows_per_seq;
-        const int rs = id - t.b * p.rows_per_seq;
+        int rs;
+        if (MODE == kLinearSample) {
+            // position-major: (target i, draft i) of every sequence for i = 0..K-1, then every tail row
+            const int twoB = 2 * p.B;
+            if (id < p.K * twoB) {
+                const int i = id / twoB;
+                const int rem = id - i * twoB;
+                t.b = rem >> 1;
+                rs = 2 * i + (rem & 1);
+            } else {
+                t.b = id - p.K * twoB;
+                rs = 2 * p.K;
+            }
+        } else if (MODE == kLinearGreedy) {
+            const int i = id / p.B;  // position-major
+            t.b = id - i * p.B;
+            rs = i;
+        } else {
+            t.b = id / p.rows_per_seq;
+            rs = id - t.b * p.rows_per_seq;
+        }
         const int bpos = T::kBonus ? bonus_pos(p, t.b) : 0;
         t.present = row_slot<MODE>(p, rs, bpos, t.pos, t.r);
         t.unit = T::kBonus ? t.b : t.b * p.units_per_seq + t.pos;
@@ -635,20 +698,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
     };
     // tiles to take at once: shrinks as the space runs out, so the last grabs are short
-    auto guided = [&](long long left) -> int {
-        const long long g = left / (2 * nwarps);
-        return static_cast<int>(g < 1 ? 1 : (g > kMaxGrab ? kMaxGrab : g));
+    auto guided = [&](long long left, int most) -> int {
+        const long long g = left / nwarps;
+        return static_cast<int>(g < 1 ? 1 : (g > most ? most : g));
     };
 
     // ---------------------------------------------------------- issue side
-    long long sc = 0, se = 0;          // stats tiles [sc, se) to issue
-    Row irow = {};                     // the row of the last issued stats tile
+    long long sc = 0, se = 0;          // stats segments [sc, se) grabbed, not yet begun
+    Row irow = {};                     // the row of the segment being issued
     irow.id = -1;
+    int iseg = 0, ik = 0, ik1 = 0;     // that segment and its tiles [ik, ik1) still to issue
     unsigned s_ahead = 0;              // lane 0: start of the next stats grab
     int s_ahead_n = 0;                 // its size
-    bool stats_done = (ST == 0);
+    bool stats_done = (NSEG == 0);
     if (!stats_done) {
-        s_ahead_n = guided(ST);
+        s_ahead_n = guided(NSEG, kMaxGrab);
         if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
     }
     long long rc = 0, re = 0;          // residual tiles [rc, re) claimed, not yet issued
@@ -660,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     unsigned claim_res = 0;            // lane 0: start of a residual claim in flight
     int claim_n = 0;
     bool res_done = (RT == 0);
-    unsigned hint_tail = 0, hint_claim = 0;  // lane 0: counters read at the previous stats grab
+    unsigned hint_tail = 0, hint_claim = 0;  // lane 0: counters read at the previous look
     bool hint_valid = false;
     int issued = 0, handled = 0;
     int islot = 0;                     // stage of the next issue
@@ -670,33 +734,31 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         return s;
     };
 
-    // tile t of the stats tiling -> (row, k), incrementally for consecutive tiles
-    long long i_t = -2;
-    int i_k = 0;
-    auto locate_stats = [&](long long t) {
-        if (t == i_t + 1 && i_k + 1 < S) {
-            ++i_k;
-        } else {
-            const int id = static_cast<int>(static_cast<unsigned>(t) / static_cast<unsigned>(S));
-            i_k = static_cast<int>(t) - id * S;
-            if (id != irow.id) irow = decode_row(id);
-        }
-        i_t = t;
+    // begin segment sg: its row and tiles; false if the row slot holds no row
+    auto begin_segment = [&](long long sg) -> bool {
+        const int id = static_cast<int>(static_cast<unsigned>(sg) / static_cast<unsigned>(p.nseg));
+        const int j = static_cast<int>(sg) - id * p.nseg;
+        if (id != irow.id) irow = decode_row(id);
+        iseg = static_cast<int>(sg);
+        ik = j * kSegTiles;
+        ik1 = min(S, ik + kSegTiles);
+        return irow.present;
     };
-    auto issue_stats = [&](long long t) {
-        const int k = i_k;
+    // issue tile ik of the current segment
+    auto issue_stats = [&]() {
         const int s = next_islot();
         unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
         uintptr_t w0, w1, c0, c1;
-        tile_window(irow, k, w0, w1, c0, c1);
+        tile_window(irow, ik, w0, w1, c0, c1);
         if (lane == 0) {
-            wc.desc[s] = make_int4(kTileStats, static_cast<int>(t), 0, 0);
+            wc.desc[s] = make_int4(kTileStats, iseg, ik, 0);
             const uint32_t bar = ptx::smem_addr(&wc.full[s]);
             const uint32_t bytes = static_cast<uint32_t>(c1 - c0);
             ptx::mbar_arrive_expect_tx(bar, bytes);
             if (bytes)
                 ptx::bulk_g2s(ptx::smem_addr(buf + (c0 - w0)), reinterpret_cast<const void *>(c0), bytes, bar);
         }
+        ++ik;
         ++issued;
     };
 
@@ -796,40 +858,27 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             }
             // 2. the next stats tile
             if (!stats_done) {
-                if (sc >= se) {
-                    const unsigned a = __shfl_sync(kFull, s_ahead, 0);
-                    if (static_cast<long long>(a) >= ST) {
-                        stats_done = true;
-                    } else {
-                        sc = a;
-                        se = min(ST, static_cast<long long>(a) + s_ahead_n);
-                        s_ahead_n = guided(ST - se);
-                        if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
-                        // residual tiles waiting (by the counters read at the previous grab): claim some
-                        if (!res_done && rc >= re && !claim_inflight) {
-                            int avail = 0;
-                            if (lane == 0 && hint_valid) {
-                                const long long a2 = static_cast<long long>(hint_tail) * p.Sr - hint_claim;
-                                avail = static_cast<int>(a2 < 0 ? 0 : (a2 > kMaxClaim ? kMaxClaim : a2));
-                            }
-                            avail = __shfl_sync(kFull, avail, 0);
-                            if (avail > 0) claim_resid(avail);
+                if (ik >= ik1) {
+                    if (sc >= se) {
+                        const unsigned a = __shfl_sync(kFull, s_ahead, 0);
+                        if (static_cast<long long>(a) >= NSEG) {
+                            stats_done = true;
+                        } else {
+                            sc = a;
+                            se = min(NSEG, static_cast<long long>(a) + s_ahead_n);
+                            s_ahead_n = guided(NSEG - se, kMaxGrab);
+                            if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
                         }
-                        if (!res_done && lane == 0) {
-                            hint_tail = ld_relaxed(&p.ws_ctrl[2]);
-                            hint_claim = ld_relaxed(&p.ws_ctrl[3]);
-                            hint_valid = true;
+                    }
+                    if (!stats_done) {
+                        if (!begin_segment(sc++)) {  // a row slot with no row (the draft row at the tail)
+                            ik = ik1 = 0;
+                            continue;
                         }
                     }
                 }
                 if (!stats_done) {
-                    locate_stats(sc);
-                    if (!irow.present) {  // a row slot with no row (the draft row at the tail): skip it
-                        ++sc;
-                        continue;
-                    }
-                    issue_stats(sc);
-                    ++sc;
+                    issue_stats();
                     return true;
                 }
             }
@@ -838,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 long long left = RT;
                 if (lane == 0 && hint_valid) left = RT - static_cast<long long>(hint_claim);
                 left = __shfl_sync(kFull, left, 0);
-                claim_resid(min(kMaxClaim, guided(left < 1 ? 1 : left)));
+                claim_resid(guided(left < 1 ? 1 : left, kMaxClaim));
                 if (lane == 0) hint_claim = ld_relaxed(&p.ws_ctrl[3]);
                 hint_valid = true;
                 if (blocking) continue;
@@ -850,14 +899,27 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         timed_out = true;
         return false;
     };
+    int since_hint = 0;
     auto fill_ring = [&]() {
+        // every few tiles: claim residual tiles if the counters read last time showed some waiting
+        if (!res_done && !claim_inflight && rc >= re && ++since_hint >= kHintEvery) {
+            since_hint = 0;
+            int avail = 0;
+            if (lane == 0 && hint_valid) {
+                const long long a2 = static_cast<long long>(hint_tail) * p.Sr - static_cast<long long>(hint_claim);
+                avail = static_cast<int>(a2 < 0 ? 0 : (a2 > kMaxClaim ? kMaxClaim : a2));
+            }
+            avail = __shfl_sync(kFull, avail, 0);
+            if (avail > 0) claim_resid(avail);
+            if (lane == 0) {
+                hint_tail = ld_relaxed(&p.ws_ctrl[2]);
+                hint_claim = ld_relaxed(&p.ws_ctrl[3]);
+            }
+            hint_valid = true;
+        }
         while (issued - handled < NS) {
-            if (!claim_inflight && rc >= re && sc < se && sc == i_t + 1 && i_k + 1 < S && irow.present) {
-                // the next tile of the same row: nothing else to look at
-                ++i_k;
-                i_t = sc;
-                issue_stats(sc);
-                ++sc;
+            if (!claim_inflight && rc >= re && ik < ik1) {  // the next tile of the segment
+                issue_stats();
                 continue;
             }
             if (!try_issue(false)) break;
@@ -866,18 +928,20 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
 
     // ----------------------------------------------------- processing side
-    // the run being reduced: consecutive tiles of one row (stats) or one entry (residual)
-    int run_kind = 0;                  // 0: none
-    long long run_next = -1;           // index the run's next tile would have
-    Row prow = {};                     // stats: the run's row
+    // the stats segment being reduced (one row, tiles [k0, k1)), and the residual run
+    bool srun = false;
+    int run_seg = -1, run_last = 0, run_len = 0;
+    Row prow = {};
     prow.id = -1;
-    int run_k0 = 0, run_len = 0;
     int px = -1;                       // the draft token whose logit this row holds, or -1
     float am = neg_inf(), as = 0.f;    // lane: running (mc, s), or (max, -) in greedy mode
     int ai = INT_MAX;                  // lane: index of the max (greedy)
     int hasx = 0;
     float xval = 0.f;
-    int r_e = 0, r_u = 0, r_b = 0, r_pos = 0;  // residual run: entry, unit, sequence, position
+    bool rrun = false;
+    long long r_next = -1;             // residual tile that would continue the residual run
+    int r_len = 0;
+    int r_e = 0, r_u = 0, r_b = 0, r_pos = 0;
     bool r_pair = false, r_skip = false;
     float4 r_js = make_float4(0.f, 0.f, 0.f, 0.f);
     // a counter increment whose result is consumed later (1: unit tiles, 2: residual tiles)
@@ -964,54 +1028,87 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         __syncwarp();
     };
 
-    // Every unit of sequence b is decided.
+    // The first rejection j of linear sequence b is known: draw the extra token
+    // (publish a draw entry) or emit the sequence; unit j's scratch is ours.
+    auto draw_or_emit = [&](int b, int j) {
+        const int U = p.units_per_seq;
+        const int u = b * U + j;
+        if (MODE == kLinearSample) {
+            if (draws) {
+                const float4 js = __ldcg(&p.ws_stats[u]);
+                push_entry(u, j < p.K, !(js.y > 0.f));  // a non-finite unit recorded 1/St = 0
+            } else {
+                emit_linear(b, j, -1, false);
+            }
+        } else if (MODE == kLinearGreedy) {
+            const int extra = (p.u_bonus != nullptr) ? __ldcg(&p.ws_val[u]) : -1;
+            __syncwarp();
+            if (lane == 0) p.ws_val[u] = 0;
+            emit_linear(b, j, extra, p.u_bonus != nullptr);
+        }
+        __syncwarp();
+    };
+
+    // Every unit of linear sequence b is decided: zero its scratch except unit j's.
+    auto cleanup_seq = [&](int b, int j, bool masked) {
+        const int U = p.units_per_seq;
+        if (masked) {
+            if (lane == 0) p.ws_seqmask[b] = 0ull;
+        } else {
+            if (MODE == kLinearSample)
+                for (int i = lane; i < p.K; i += 32) p.ws_acc[static_cast<size_t>(b) * p.K + i] = 0;
+            if (lane == 0) p.ws_seq_cnt[b] = 0u;
+        }
+        for (int i = lane; i < U; i += 32) {
+            if (i == j) continue;
+            if (MODE == kLinearSample && draws) p.ws_stats[static_cast<size_t>(b) * U + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (MODE == kLinearGreedy) p.ws_val[static_cast<size_t>(b) * U + i] = 0;
+        }
+        __syncwarp();
+    };
+
+    // Every unit of sequence b is decided (trees, and linear sequences with K >= 32).
     auto finish_sequence = [&](int b) {
         const int K = p.K;
         const int U = p.units_per_seq;
         if (MODE == kTreeGreedy) {
             emit_tree(b);
-        } else {
-            int j = K;
-            for (int base = 0; base < K; base += 32) {
-                const int i = base + lane;
-                bool rej = false;
-                if (i < K) {
-                    if (MODE == kLinearSample)
-                        rej = __ldcg(&p.ws_acc[static_cast<size_t>(b) * K + i]) == 0;
-                    else
-                        rej = __ldg(&p.tokens[static_cast<size_t>(b) * K + i]) !=
-                              __ldcg(&p.ws_val[static_cast<size_t>(b) * U + i]);
-                }
-                const unsigned m = __ballot_sync(kFull, rej);
-                if (m) {
-                    j = base + __ffs(m) - 1;
-                    break;
-                }
+            if (lane == 0) p.ws_seq_cnt[b] = 0u;
+            __syncwarp();
+            return;
+        }
+        int j = K;
+        for (int base = 0; base < K; base += 32) {
+            const int i = base + lane;
+            bool rej = false;
+            if (i < K) {
+                if (MODE == kLinearSample)
+                    rej = __ldcg(&p.ws_acc[static_cast<size_t>(b) * K + i]) == 0;
+                else
+                    rej = __ldg(&p.tokens[static_cast<size_t>(b) * K + i]) !=
+                          __ldcg(&p.ws_val[static_cast<size_t>(b) * U + i]);
             }
-            if (MODE == kLinearSample) {
-                for (int i = lane; i < K; i += 32) p.ws_acc[static_cast<size_t>(b) * K + i] = 0;
-                if (draws) {
-                    const int u = b * U + j;
-                    const float4 js = __ldcg(&p.ws_stats[u]);
-                    push_entry(u, j < K, !(js.y > 0.f));  // a non-finite unit recorded 1/St = 0
-                } else {
-                    emit_linear(b, j, -1, false);
-                }
-            } else {  // greedy
-                const int extra = (p.u_bonus != nullptr) ? __ldcg(&p.ws_val[static_cast<size_t>(b) * U + j]) : -1;
-                __syncwarp();
-                for (int i = lane; i < U; i += 32) p.ws_val[static_cast<size_t>(b) * U + i] = 0;
-                emit_linear(b, j, extra, p.u_bonus != nullptr);
+            const unsigned m = __ballot_sync(kFull, rej);
+            if (m) {
+                j = base + __ffs(m) - 1;
+                break;
             }
         }
-        if (lane == 0) p.ws_seq_cnt[b] = 0u;
-        __syncwarp();
+        draw_or_emit(b, j);
+        cleanup_seq(b, j, false);
     };
 
     // Every stats tile of unit u is published: merge, decide, record.
     auto finish_unit = [&](int u, int b, int pos) {
         const int K = p.K;
         const int nrows = unit_nrows<MODE>(p, pos);
+        // the decision's inputs, loaded while the partials are merged
+        int x = -1;
+        float ua = 0.f;
+        if ((MODE == kLinearSample || MODE == kLinearGreedy) && pos >= 0 && pos < K) {
+            x = __ldg(&p.tokens[static_cast<size_t>(b) * K + pos]);
+            if (MODE == kLinearSample) ua = __ldg(&p.u_accept[static_cast<size_t>(b) * K + pos]);
+        }
         float Mr[2], Sm[2];
         int Ar[2];
 #pragma unroll
@@ -1019,11 +1116,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             float v = neg_inf(), sm = 0.f;
             int ii = INT_MAX;
             if (r < nrows) {
-                for (int k = lane; k < S; k += 32) {
-                    uint2 *slot = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * S + k];
-                    const uint2 e = __ldcg(slot);
-                    if (e.x == 0u && e.y == 0u) continue;  // no run starts at this tile
-                    *slot = make_uint2(0u, 0u);
+                for (int k = lane; k < p.nseg; k += 32) {
+                    unsigned long long *slot = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * p.nseg + k];
+                    bool late = false;
+                    const unsigned long long w = await64(slot, late);  // every segment publishes once
+                    if (late) {
+                        atomicOr(p.status, SPEC_DEV_TIMEOUT);
+                        continue;
+                    }
+                    *slot = 0ull;
+                    const uint2 e = make_uint2(static_cast<unsigned>(w), static_cast<unsigned>(w >> 32));
                     if (T::kSample)
                         merge_sc(v, sm, __uint_as_float(e.x), __uint_as_float(e.y));
                     else
@@ -1040,6 +1142,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         uint32_t fl = 0;
         bool finite = true;
+        int accept = 0;  // lane 0
         if (T::kSample) {
             for (int r = 0; r < nrows; ++r)
                 if (!(isfinite(Mr[r]) && isfinite(Sm[r]) && Sm[r] > 0.f)) finite = false;
@@ -1051,12 +1154,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (lane == 0) {
             p.ws_unit_cnt[u] = 0u;
             if (MODE == kLinearSample && pos < K) {
-                const float2 txv = __ldcg(&p.ws_tx[u]);
-                p.ws_tx[u] = make_float2(0.f, 0.f);
-                const int x = __ldg(&p.tokens[static_cast<size_t>(b) * K + pos]);
-                const float ua = __ldg(&p.u_accept[static_cast<size_t>(b) * K + pos]);
+                float2 txv = make_float2(0.f, 0.f);
+                if (x >= 0 && x < p.V) {  // the segments holding x published its logits
+                    bool late = false;
+                    const unsigned long long wt = await64(&p.ws_txw[static_cast<size_t>(u) * 2], late);
+                    const unsigned long long wd = await64(&p.ws_txw[static_cast<size_t>(u) * 2 + 1], late);
+                    if (late) fl |= SPEC_DEV_TIMEOUT;
+                    p.ws_txw[static_cast<size_t>(u) * 2] = 0ull;
+                    p.ws_txw[static_cast<size_t>(u) * 2 + 1] = 0ull;
+                    txv = make_float2(__uint_as_float(static_cast<unsigned>(wt)), __uint_as_float(static_cast<unsigned>(wd)));
+                }
                 float px = 0.f, qx = 0.f, thr = 0.f;
-                int accept = 0;
                 if (x < 0 || x >= p.V) {
                     fl |= SPEC_DEV_BAD_TOKEN;
                 } else {
@@ -1067,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     thr = fminf(1.0f, ptx::ex2(lt - ld) * (Sm[1] / Sm[0]));
                     accept = (ua < thr) ? 1 : 0;
                 }
-                p.ws_acc[static_cast<size_t>(b) * K + pos] = accept;
+                if (K >= 32) p.ws_acc[static_cast<size_t>(b) * K + pos] = accept;
                 if (p.probs) {
                     float *pr = p.probs + (static_cast<size_t>(b) * K + pos) * 3;
                     pr[0] = px;
@@ -1085,6 +1193,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     p.bonus_token[b] = (pos < 0) ? -1 : Ar[0];
                 else
                     p.ws_val[static_cast<size_t>(b) * p.units_per_seq + pos] = Ar[0];
+                if (MODE == kLinearGreedy && pos < K) accept = (x == Ar[0]) ? 1 : 0;
             }
             if (T::kBonus && pos < 0) fl |= SPEC_DEV_BAD_LENGTH;
             if (fl) atomicOr(p.status, fl);
@@ -1092,6 +1201,20 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         __syncwarp();
         if (T::kBonus) {
             if (T::kSample) push_entry(u, nrows == 2, pos < 0 || !finite);
+            return;
+        }
+        if ((MODE == kLinearSample || MODE == kLinearGreedy) && K < 32) {
+            // the first rejection is known as soon as every earlier position is decided
+            unsigned long long bits = 1ull << pos;
+            if (pos < K && __shfl_sync(kFull, accept, 0)) bits |= 1ull << (32 + pos);
+            unsigned long long old = 0;
+            if (lane == 0) old = atom_or_acq_rel64(&p.ws_seqmask[b], bits);
+            old = __shfl_sync(kFull, old, 0);
+            __syncwarp();
+            const unsigned long long now = old | bits;
+            const int jn = first_rejection(now, K);
+            if (first_rejection(old, K) < 0 && jn >= 0) draw_or_emit(b, jn);
+            if (__popc(static_cast<unsigned>(now)) == K + 1) cleanup_seq(b, jn, true);
             return;
         }
         int last = 0;
@@ -1106,7 +1229,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     // alone, read from global memory (the rare redraw after a vanished residual).
     auto resid_from_global = [&](int e, int b, int pos, const float4 &js) {
         const unsigned char *rt = row_ptr<EB>(p, b, pos, 0);
-        long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
+        unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
         for (int k = 0; k < p.Sr; ++k) {
             const int s0 = k * p.Lr;
             const int s1 = min(p.V, s0 + p.Lr);
@@ -1131,7 +1254,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
             for (int c = 0; c < kCpt; ++c) {
                 const long long t = warp_sum64(q[c]);
-                if (lane == 0) cs[k * kCpt + c] = t;
+                if (lane == 0) st_relaxed64(&cs[k * kCpt + c], static_cast<unsigned long long>(t) + 1ull);
             }
         }
         __syncwarp();
@@ -1140,41 +1263,76 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     // Locate the extra token of entry e; -1 when the weights sum to zero.
     auto select_token = [&](int e, int b, int pos, bool pair, const float4 &js, float ub) -> int {
         const int n = p.Sr * kCpt;
-        const long long *cs = p.ws_csum + static_cast<size_t>(e) * n;
-        const int per = (n + 31) / 32;
-        const int lo = min(n, lane * per), hi = min(n, lo + per);
-        long long mine = 0;
-        for (int i = lo; i < hi; ++i) mine += __ldcg(&cs[i]);
-        long long incl = mine;
+        const unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * n;
+        bool late = false;
+        // the total, in rounds of 256 loads issued together (each sum is stored plus one)
+        long long tot = 0;
+        for (int base = 0; base < n; base += 256) {
+            long long v[8];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const long long y = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off) incl += y;
+            for (int r = 0; r < 8; ++r) {
+                const int i = base + r * 32 + lane;
+                v[r] = (i < n) ? static_cast<long long>(ld_relaxed64(&cs[i])) : 1;
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if (v[r] == 0) {  // not visible yet
+                    const int i = base + r * 32 + lane;
+                    v[r] = static_cast<long long>(await64(&cs[i], late));
+                }
+                tot += v[r] - 1;
+            }
         }
-        const long long tot = __shfl_sync(kFull, incl, 31);
+        tot = warp_sum64(tot);
+        if (__any_sync(kFull, late)) {
+            if (lane == 0) atomicOr(p.status, SPEC_DEV_TIMEOUT);
+            return -1;
+        }
         if (tot <= 0) return -1;
         const double ud = (ub >= 0.f) ? static_cast<double>(ub) : 0.0;  // a NaN uniform counts as 0
         long long target = static_cast<long long>(ud * static_cast<double>(tot));
         if (target >= tot) target = tot - 1;
-        // the chunk holding the target: first lane, then first chunk in that lane's block
-        const unsigned bl = __ballot_sync(kFull, incl > target);
-        const int ol = __ffs(bl) - 1;
-        long long acc = __shfl_sync(kFull, incl - mine, ol);
+        // the chunk holding the target: rounds of 256 consecutive sums, 8 per lane
+        long long carry = 0, acc = 0;
         int chunk = -1;
-        if (lane == ol) {
-            long long a = acc;
-            for (int i = lo; i < hi; ++i) {
-                const long long ci = __ldcg(&cs[i]);
-                if (a + ci > target) {
-                    chunk = i;
-                    break;
-                }
-                a += ci;
+        for (int base = 0; base < n && chunk < 0; base += 256) {
+            long long v[8];
+            long long mine = 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int i = base + lane * 8 + r;
+                v[r] = (i < n) ? static_cast<long long>(ld_relaxed64(&cs[i])) - 1 : 0;
+                mine += v[r];
             }
-            acc = a;
+            long long incl = mine;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long y = __shfl_up_sync(kFull, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const unsigned bl = __ballot_sync(kFull, carry + incl > target);
+            if (bl) {
+                const int ol = __ffs(bl) - 1;
+                int ch = -1;
+                long long a = carry + incl - mine;
+                if (lane == ol) {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        if (ch < 0) {
+                            if (a + v[r] > target)
+                                ch = base + lane * 8 + r;
+                            else
+                                a += v[r];
+                        }
+                    }
+                }
+                chunk = __shfl_sync(kFull, ch, ol);
+                acc = __shfl_sync(kFull, a, ol);
+            } else {
+                carry += __shfl_sync(kFull, incl, 31);
+            }
         }
-        chunk = __shfl_sync(kFull, chunk, ol);
-        acc = __shfl_sync(kFull, acc, ol);
+        if (chunk < 0) return -1;  // (not reached: target < tot)
         const long long rem = target - acc;  // 0 <= rem < cs[chunk]
         // rescan that chunk from global memory with the same weights and order
         const int k = chunk / kCpt;
@@ -1274,14 +1432,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             emit_linear(b, pos, token, true);
         }
         // leave the workspace zeroed
-        long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
-        for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0;
-        if (T::kBonus) {
-            if (lane == 0) p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-            for (int i = lane; i < p.units_per_seq; i += 32)
-                p.ws_stats[static_cast<size_t>(b) * p.units_per_seq + i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
+        for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0ull;
+        if (lane == 0) p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // the other units' by their sequence
         if (lane == 0) {
             p.ws_rq[e] = 0u;
             p.ws_res_cnt[e] = 0u;
@@ -1304,44 +1457,46 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         last = __shfl_sync(kFull, last, 0);
         if (!last) return;
-        fence_acquire();  // every partial counted so far is visible from here on
-        __syncwarp();
+        __syncwarp();  // (the partials are validated as they are read: no fence needed)
         if (kind == 1)
             finish_unit(pend_unit, pend_b, pend_pos);
         else
             finish_entry(pend_entry);
     };
 
-    // close the run: publish its partial (stats) and count its tiles
-    auto close_run = [&]() {
-        if (run_kind == 0) return;
-        if (run_kind == kTileStats) {
-            if (T::kSample)
-                warp_merge_sc(am, as);
-            else
-                warp_merge_vi(am, ai);
-        }
+    // the segment's last tile is reduced: merge the lanes, publish, count its tiles
+    auto close_stats = [&]() {
+        if (T::kSample)
+            warp_merge_sc(am, as);
+        else
+            warp_merge_vi(am, ai);
         resolve_pending();
-        if (run_kind == kTileStats) {
-            if (lane == 0) {
-                const uint2 part = T::kSample ? make_uint2(__float_as_uint(am), __float_as_uint(as))
-                                              : make_uint2(__float_as_uint(am), static_cast<unsigned>(ai) + 1u);
-                p.ws_part[(static_cast<size_t>(prow.unit) * 2 + prow.r) * S + run_k0] = part;
-                if (hasx) reinterpret_cast<float *>(&p.ws_tx[prow.unit])[prow.r] = xval;
-                pend_old = atom_add_release(&p.ws_unit_cnt[prow.unit], static_cast<unsigned>(run_len));
-            }
-            pend_kind = 1;
-            pend_unit = prow.unit;
-            pend_b = prow.b;
-            pend_pos = prow.pos;
-        } else {
-            if (lane == 0) pend_old = atom_add_release(&p.ws_res_cnt[r_e], static_cast<unsigned>(run_len));
-            pend_kind = 2;
-            pend_entry = r_e;
+        if (lane == 0) {
+            const uint2 part = T::kSample ? make_uint2(__float_as_uint(am), __float_as_uint(as))
+                                          : make_uint2(__float_as_uint(am), static_cast<unsigned>(ai) + 1u);
+            const int j = run_seg - prow.id * p.nseg;
+            st_relaxed64(&p.ws_part[(static_cast<size_t>(prow.unit) * 2 + prow.r) * p.nseg + j],
+                         static_cast<unsigned long long>(part.x) | (static_cast<unsigned long long>(part.y) << 32));
+            if (hasx)
+                st_relaxed64(&p.ws_txw[static_cast<size_t>(prow.unit) * 2 + prow.r],
+                             static_cast<unsigned long long>(__float_as_uint(xval)) | (1ull << 32));
+            pend_old = atomicAdd(&p.ws_unit_cnt[prow.unit], static_cast<unsigned>(run_len));
         }
+        pend_kind = 1;
+        pend_unit = prow.unit;
+        pend_b = prow.b;
+        pend_pos = prow.pos;
         pend_add = run_len;
-        run_kind = 0;
-        run_next = -1;
+        srun = false;
+    };
+    // the residual run ends: count its tiles
+    auto close_resid = [&]() {
+        resolve_pending();
+        if (lane == 0) pend_old = atomicAdd(&p.ws_res_cnt[r_e], static_cast<unsigned>(r_len));
+        pend_kind = 2;
+        pend_entry = r_e;
+        pend_add = r_len;
+        rrun = false;
     };
 
     // ------------------------------------------------------------ main loop
@@ -1351,7 +1506,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     for (;;) {
         if (issued == handled) {
             // nothing in flight: settle before anything that may wait
-            close_run();
+            if (rrun) close_resid();
             resolve_pending();
             if (!try_issue(true)) break;
             fill_ring();
@@ -1361,20 +1516,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
         const uint32_t bar = ptx::smem_addr(&wc.full[s]);
         const uint32_t parity = hphase;
-        const long long idx = static_cast<unsigned>(d.y);
-        if (run_kind != 0 && (d.x != run_kind || idx != run_next)) close_run();
         if (d.x == kTileStats) {
-            int k;
-            if (run_kind == kTileStats) {
-                k = run_k0 + run_len;  // continues the run
-            } else {
-                const int id = static_cast<int>(static_cast<unsigned>(idx) / static_cast<unsigned>(S));
-                k = static_cast<int>(idx) - id * S;
+            const int k = d.z;
+            if (!srun) {
+                // a new segment: its row, and fresh lane statistics
+                const int id = static_cast<int>(static_cast<unsigned>(d.y) / static_cast<unsigned>(p.nseg));
+                const int j = d.y - id * p.nseg;
                 if (id != prow.id) prow = decode_row(id);
-            }
-            if (run_kind == 0) {
-                run_kind = kTileStats;
-                run_k0 = k;
+                srun = true;
+                run_seg = d.y;
+                run_last = min(S, (j + 1) * kSegTiles) - 1;
                 run_len = 0;
                 am = neg_inf();
                 as = 0.f;
@@ -1426,16 +1577,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             __syncwarp();
             if (patch) fence_proxy_async();  // generic writes to this stage precede its next bulk copy
             ++run_len;
-            run_next = (k + 1 < S) ? idx + 1 : -1;
         } else {
             // ---- a residual tile
+            const long long idx = static_cast<unsigned>(d.y);
             const uint32_t rec = static_cast<uint32_t>(d.z);
             const int e = static_cast<int>(idx / p.Sr);
             const int k = static_cast<int>(idx - static_cast<long long>(e) * p.Sr);
-            if (run_kind == 0) {
-                run_kind = kTileResid;
-                run_k0 = k;
-                run_len = 0;
+            if (rrun && idx != r_next) close_resid();
+            if (!rrun) {
+                rrun = true;
+                r_len = 0;
                 r_e = e;
                 r_pair = (rec & kRecPair) != 0;
                 r_skip = (rec & kRecSkip) != 0;
@@ -1475,12 +1626,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             __syncwarp();
             if (patched) fence_proxy_async();
             if (lane == 0) {
-                long long *dst = p.ws_csum + (static_cast<size_t>(e) * p.Sr + k) * kCpt;
+                unsigned long long *dst = p.ws_csum + (static_cast<size_t>(e) * p.Sr + k) * kCpt;
 #pragma unroll
-                for (int c = 0; c < kCpt; ++c) dst[c] = q[c];
+                for (int c = 0; c < kCpt; ++c) st_relaxed64(&dst[c], static_cast<unsigned long long>(q[c]) + 1ull);
             }
-            ++run_len;
-            run_next = (k + 1 < p.Sr) ? idx + 1 : -1;
+            ++r_len;
+            r_next = (k + 1 < p.Sr) ? idx + 1 : -1;
         }
         ++handled;
         if (++hslot == NS) {
@@ -1489,13 +1640,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         fill_ring();
         resolve_pending();
-        // close the run now unless the next tile in the ring continues it
-        bool cont = false;
-        if (run_next >= 0 && issued > handled) {
-            const int4 nd = wc.desc[hslot];
-            cont = nd.x == run_kind && static_cast<long long>(static_cast<unsigned>(nd.y)) == run_next;
+        if (d.x == kTileStats) {
+            if (d.z == run_last) close_stats();
+        } else if (rrun) {
+            // close the residual run now unless the next tile in the ring continues it
+            bool cont = false;
+            if (r_next >= 0 && issued > handled) {
+                const int4 nd = wc.desc[hslot];
+                cont = nd.x == kTileResid && static_cast<long long>(static_cast<unsigned>(nd.y)) == r_next;
+            }
+            if (!cont) close_resid();
         }
-        if (!cont) close_run();
     }
 
     if (lane == 0 && timed_out) atomicOr(p.status, SPEC_DEV_TIMEOUT);
