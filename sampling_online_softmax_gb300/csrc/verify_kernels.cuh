@@ -11,37 +11,41 @@
 //   from max(0, p_j - q_j) (j < K) or p_K (j == K), or argmax in greedy mode.
 //
 // How (GB300 design): a streaming reduction in which every warp runs its own
-// pipeline and no warp waits on another while it holds unpublished work.
+// pipeline and no warp waits on another while it holds unfinished work.
 //   * A "unit" is one (sequence, position): target row i with draft row i for
-//     linear sampling, otherwise one target row.  Every row is cut into S
-//     tiles: 4 KB windows on the 16-byte grid of global memory, so only a
-//     row's first and last tile can hold bytes of a neighbouring row.  A batch
-//     is up to `grab` consecutive tiles of one row.
-//   * Persistent CTAs of eight warps, two per SM.  Each warp takes batches
-//     from a global counter (the next batch is requested one batch ahead) and
-//     keeps a ring of shared-memory stages filled with 1-D bulk copies
-//     (cp.async.bulk, one mbarrier per stage, a 16-byte descriptor per stage).
-//   * Row statistics live in the log2-scaled domain: every lane keeps a
-//     running (mc, s) over its logits of the batch, mc = fl(max(l) * c) and
-//     s = sum 2^(fma(l, c, -mc)), c = log2(e) / T; the inner loop is packed
-//     fp32x2 FMA/ADD plus one MUFU ex2 per logit.  Greedy lanes keep (max,
-//     lowest argmax).  The warp merges its lanes once per batch.
-//   * A warp publishes each batch's partial and adds one to the unit's batch
-//     counter with an acq_rel atomic whose result it looks at one tile later.
-//     The warp that completes a unit merges the partials and decides it; the
-//     warp that completes a sequence finds the first rejection and emits the
-//     sequence, or, when an extra token is drawn, publishes a draw entry.
+//     linear sampling, otherwise one target row.  Every row is read as S tiles,
+//     8 KB windows on the 16-byte grid of global memory (only a row's first and
+//     last window can hold bytes of a neighbouring row), grouped into segments
+//     of kSegTiles tiles.  Linear rows are ordered position-major, so every
+//     sequence's first positions are decided early.
+//   * Persistent CTAs of eight warps, one per SM.  A warp takes ranges of
+//     segments from a global counter (the next range is requested one range
+//     ahead, and ranges shrink as the work runs out) and keeps a ring of three
+//     stages filled with 1-D bulk copies (cp.async.bulk, one mbarrier and one
+//     descriptor per stage).
+//   * Row statistics live in the log2-scaled domain: every lane keeps a running
+//     (mc, s), s = sum 2^(fma(l, c, -mc)), c = log2(e) / T, with packed fp32x2
+//     FMA/ADD and one MUFU ex2 per logit; mc is only an offset, re-based on the
+//     lane's max when a tile's terms grow past 2^64.  Greedy lanes keep (max,
+//     lowest argmax).  One warp reduces each whole segment and publishes one
+//     partial, so results do not depend on timing.
+//   * Publishing costs no fence: a partial (or the draft token's logit, or a
+//     residual chunk sum) is written once per call as a non-zero 64-bit value
+//     with a relaxed store and counted with a relaxed atomic.  The warp whose
+//     count completes a unit reads the values, waiting for any that still read
+//     zero, decides the unit, and records it in the sequence's decided/accepted
+//     mask; the update that makes the first rejection known publishes a draw
+//     entry (or emits the sequence).
 //   * A draw entry names one row pair (or the tail row) and is cut into Sr
-//     residual tiles of at most 2 KB per row.  Any warp may claim residual
-//     tiles (a second global counter); they take precedence over stats tiles,
-//     so rows are re-read while they are still in L2.  A residual tile sums
-//     the fp32 weights max(0, p - q) (or p) of every 16-byte group exactly in
-//     int64 fixed point (units of 2^-52) per 64-group chunk.  The warp that
-//     completes an entry's residual locates the token (a prefix over the
-//     chunk sums, then a rescan of one chunk) and emits the sequence.
-//   * No tensor cores (nothing here is a contraction).  A warp waits on other
-//     warps only with an empty ring and nothing unpublished; every wait is
-//     bounded and reports SPEC_DEV_TIMEOUT instead of trapping.
+//     residual tiles of at most 4 KB per row.  Warps take residual tiles once
+//     their stats work is exhausted (the stats stream has priority: the tail
+//     rows it ends with decide the last draws).  A residual tile sums the fp32
+//     weights max(0, p - q) (or p) of every 16-byte group exactly in int64
+//     fixed point (units of 2^-52) per 64-group chunk.  The warp that completes
+//     an entry's residual locates the token (a prefix over the chunk sums, then
+//     a rescan of one chunk) and emits the sequence.
+//   * No tensor cores (nothing here is a contraction).  Every wait is bounded
+//     and reports SPEC_DEV_TIMEOUT instead of trapping.
 #pragma once
 
 #include <climits>
@@ -71,8 +75,7 @@ constexpr int kCpt = (kResidSliceBytes / 16 + 2 + kChunk - 1) / kChunk;  // resi
 static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout");
 constexpr int kSegTiles = 4;            // stats tiles per segment: one partial each, never split between warps
 constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
-constexpr int kMaxClaim = 4;            // residual tiles claimed at once (at most)
-constexpr int kHintEvery = 1;           // tiles between looks at the residual counters
+constexpr int kMaxClaim = 2;            // residual tiles claimed at once (at most)
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr unsigned kFull = 0xffffffffu;
@@ -242,6 +245,21 @@ __device__ __forceinline__ unsigned long long f2add(unsigned long long a, unsign
     unsigned long long d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+__device__ __forceinline__ unsigned long long f2mul(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2sub(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2ex2(unsigned long long v) {
+    float a, b;
+    f2unpack(v, a, b);
+    return f2pack(ptx::ex2(a), ptx::ex2(b));
 }
 // sum + (2^x.lo, 2^x.hi) with x = fma(v, c, -mc)
 __device__ __forceinline__ unsigned long long exp_acc(unsigned long long sum, unsigned long long v,
@@ -436,6 +454,9 @@ __device__ __forceinline__ long long warp_sum64(long long q) {
 }
 
 // ------------------------------------------------------ extra-token weights
+// The weights of a 16-byte group are summed as (w0 + w2 + w4 + ...) + (w1 + w3
+// + w5 + ...): even and odd elements in order, then the two; the packed tile
+// pass and the element-wise rescan both follow it.
 // Weight of one element: pair (residual) max(0, p_v - q_v) with
 // p_v = 2^(t c - MCt) / St and q_v = 2^(d c - MCd) / Sd; tail p_v.
 // js = (MCt, 1/St, MCd, 1/Sd).  The explicit _rn intrinsics keep every
@@ -517,37 +538,53 @@ __device__ __forceinline__ void lane_argmax(const unsigned char *buf, int ngran,
 
 // Exact weight sums of one residual tile per chunk of 64 groups (every lane
 // ends with them).  Groups follow the target row's window; `same` when both
-// row buffers share the 16-byte phase.
+// row buffers share the 16-byte phase.  Packed fp32x2 arithmetic on element
+// pairs; every weight is the same as elem_weight's.
 template <int EB>
 __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, int vbase0, int vbase1, int s0,
                                            int s1, bool pair, bool same, const float4 &js, float c, int lane,
                                            long long (&q)[kCpt]) {
     constexpr int G = Elt<EB>::G;
+    constexpr int P = Elt<EB>::P;
     const unsigned char *bt = buf;
     const unsigned char *bd = buf + kRowBuf;
+    const unsigned long long c2 = f2pack(c, c);
+    const unsigned long long nmt = f2pack(-js.x, -js.x), ist = f2pack(js.y, js.y);
+    const unsigned long long nmd = f2pack(-js.z, -js.z), isd = f2pack(js.w, js.w);
 #pragma unroll
     for (int ch = 0; ch < kCpt; ++ch) q[ch] = 0;
     for (int g = lane; g < ngran; g += 32) {
-        float t[G], d[G];
-        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(bt + 16 * g), t);
+        unsigned long long t2[P], d2[P];
+        Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bt + 16 * g), t2);
         if (pair) {
             if (same) {
-                Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(bd + 16 * g), d);
+                Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bd + 16 * g), d2);
             } else {
+                float d[G];
 #pragma unroll
                 for (int k = 0; k < G; ++k) {
                     const int v = vbase0 + g * G + k;
                     d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(bd + (v - vbase1) * EB) : neg_inf();
                 }
+#pragma unroll
+                for (int k = 0; k < P; ++k) d2[k] = f2pack(d[2 * k], d[2 * k + 1]);
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < G; ++k) d[k] = 0.f;
         }
-        float sw = 0.f;
+        unsigned long long acc = 0ull;  // (even sum, odd sum)
 #pragma unroll
-        for (int k = 0; k < G; ++k) sw += elem_weight(t[k], d[k], pair, js, c);
-        const long long qq = fixq(sw);
+        for (int k = 0; k < P; ++k) {
+            unsigned long long w2 = f2mul(f2ex2(f2fma(t2[k], c2, nmt)), ist);  // p of two elements
+            if (pair) {
+                const unsigned long long q2 = f2mul(f2ex2(f2fma(d2[k], c2, nmd)), isd);
+                float a, b;
+                f2unpack(f2sub(w2, q2), a, b);
+                w2 = f2pack(fmaxf(0.0f, a), fmaxf(0.0f, b));
+            }
+            acc = f2add(acc, w2);
+        }
+        float se, so;
+        f2unpack(acc, se, so);
+        const long long qq = fixq(se + so);
         const int chunk = g >> 6;
 #pragma unroll
         for (int ch = 0; ch < kCpt; ++ch)
@@ -882,16 +919,39 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     return true;
                 }
             }
-            // 3. stats exhausted: claim residual tiles
+            // 3. stats exhausted: claim residual tiles of published entries (wait for some if blocking)
             if (!res_done && rc >= re && !claim_inflight) {
-                long long left = RT;
-                if (lane == 0 && hint_valid) left = RT - static_cast<long long>(hint_claim);
-                left = __shfl_sync(kFull, left, 0);
-                claim_resid(guided(left < 1 ? 1 : left, kMaxClaim));
-                if (lane == 0) hint_claim = ld_relaxed(&p.ws_ctrl[3]);
+                int avail = 0, all = 0;
+                if (lane == 0) {
+                    if (blocking || !hint_valid) {
+                        hint_tail = ld_relaxed(&p.ws_ctrl[2]);
+                        hint_claim = ld_relaxed(&p.ws_ctrl[3]);
+                    }
+                    const long long a2 = static_cast<long long>(hint_tail) * p.Sr - static_cast<long long>(hint_claim);
+                    avail = static_cast<int>(a2 < 0 ? 0 : (a2 > kMaxClaim ? kMaxClaim : a2));
+                    all = static_cast<long long>(hint_claim) >= RT ? 1 : 0;
+                }
                 hint_valid = true;
-                if (blocking) continue;
-                return false;
+                avail = __shfl_sync(kFull, avail, 0);
+                all = __shfl_sync(kFull, all, 0);
+                if (all) {
+                    res_done = true;
+                    continue;
+                }
+                if (avail > 0) {
+                    claim_resid(avail);
+                    if (blocking) continue;
+                    return false;
+                }
+                if (!blocking) {
+                    if (lane == 0) {  // fresh counters for the next look
+                        hint_tail = ld_relaxed(&p.ws_ctrl[2]);
+                        hint_claim = ld_relaxed(&p.ws_ctrl[3]);
+                    }
+                    return false;
+                }
+                __nanosleep(256);  // nothing published yet: every unfinished unit is held by a running warp
+                continue;
             }
             if (!blocking) return false;
             if (stats_done && res_done && rc >= re && !claim_inflight) return false;
@@ -899,24 +959,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         timed_out = true;
         return false;
     };
-    int since_hint = 0;
     auto fill_ring = [&]() {
-        // every few tiles: claim residual tiles if the counters read last time showed some waiting
-        if (!res_done && !claim_inflight && rc >= re && ++since_hint >= kHintEvery) {
-            since_hint = 0;
-            int avail = 0;
-            if (lane == 0 && hint_valid) {
-                const long long a2 = static_cast<long long>(hint_tail) * p.Sr - static_cast<long long>(hint_claim);
-                avail = static_cast<int>(a2 < 0 ? 0 : (a2 > kMaxClaim ? kMaxClaim : a2));
-            }
-            avail = __shfl_sync(kFull, avail, 0);
-            if (avail > 0) claim_resid(avail);
-            if (lane == 0) {
-                hint_tail = ld_relaxed(&p.ws_ctrl[2]);
-                hint_claim = ld_relaxed(&p.ws_ctrl[3]);
-            }
-            hint_valid = true;
-        }
         while (issued - handled < NS) {
             if (!claim_inflight && rc >= re && ik < ik1) {  // the next tile of the segment
                 issue_stats();
@@ -1240,16 +1283,19 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
             for (int h = 0; h < (kCpt * kChunk) / 32; ++h) {
                 const int gi = h * 32 + lane;
-                float sw = 0.f;
+                float se = 0.f, so = 0.f;  // even and odd elements, in order
 #pragma unroll
                 for (int k2 = 0; k2 < G; ++k2) {
                     const int v = g.vbase + gi * G + k2;
                     float w = 0.f;
                     if (gi < g.ngran && v >= s0 && v < s1)
                         w = elem_weight(Elt<EB>::gload(rt + static_cast<size_t>(v) * EB), 0.f, false, js, p.c);
-                    sw += w;
+                    if (k2 & 1)
+                        so += w;
+                    else
+                        se += w;
                 }
-                q[h / 2] += fixq(sw);
+                q[h / 2] += fixq(se + so);
             }
 #pragma unroll
             for (int c = 0; c < kCpt; ++c) {
@@ -1347,7 +1393,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int g = cc * kChunk + h * 32 + lane;
-            float sw = 0.f;
+            float se = 0.f, so = 0.f;  // the group's sum, in the tile pass's order
 #pragma unroll
             for (int k2 = 0; k2 < G; ++k2) {
                 const int v = gt.vbase + g * G + k2;
@@ -1358,9 +1404,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     we = elem_weight(t, d, pair, js, p.c);
                 }
                 w[h][k2] = we;
-                sw += we;
+                if (k2 & 1)
+                    so += we;
+                else
+                    se += we;
             }
-            q[h] = fixq(sw);
+            q[h] = fixq(se + so);
         }
         long long i0 = q[0], i1 = q[1];
 #pragma unroll
