@@ -17,6 +17,10 @@
 #include "spec_verify.h"
 #include "verify_kernels.cuh"
 
+#ifndef SPEC_MAX_STAGES
+#define SPEC_MAX_STAGES 2
+#endif
+
 namespace spec {
 namespace {
 
@@ -196,7 +200,7 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     const size_t scratch = (MODE == kTreeGreedy) ? static_cast<size_t>(kWarps) * 3 * p.units_per_seq * 4 : 0;
     int ns = 0, per_sm = 0;
     size_t dyn = 0;
-    for (int cand : {3, 2}) {
+    for (int cand : {SPEC_MAX_STAGES, 2}) {
         const size_t d = static_cast<size_t>(kWarps) * cand * kStageBytes + scratch;
         if (d > di.max_dyn) continue;
         const int b = blocks_per_sm(dev, reinterpret_cast<const void *>(kernel), d);

@@ -18,9 +18,9 @@
 //     last window can hold bytes of a neighbouring row), grouped into segments
 //     of kSegTiles tiles.  Linear rows are ordered position-major, so every
 //     sequence's first positions are decided early.
-//   * Persistent CTAs of eight warps, one per SM.  A warp takes ranges of
+//   * Persistent CTAs of twelve warps, one per SM.  A warp takes ranges of
 //     segments from a global counter (the next range is requested one range
-//     ahead, and ranges shrink as the work runs out) and keeps a ring of three
+//     ahead, and ranges shrink as the work runs out) and keeps a ring of two
 //     stages filled with 1-D bulk copies (cp.async.bulk, one mbarrier and one
 //     descriptor per stage).
 //   * Row statistics live in the log2-scaled domain: every lane keeps a running
@@ -56,7 +56,10 @@
 
 namespace spec {
 
-constexpr int kWarps = 8;
+#ifndef SPEC_WARPS
+#define SPEC_WARPS 12
+#endif
+constexpr int kWarps = SPEC_WARPS;  // streaming warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxStages = 4;
 #ifndef SPEC_TILE_KB
