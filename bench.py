@@ -169,6 +169,22 @@ def measured_peak():
 
 
 # ------------------------------------------------------------ reference arm
+def max_over_ranks(value, device=None):
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, per_rank_units, steps, elapsed):
+    """Units per second over all ranks: every rank processes its own batch each step."""
+    return world * per_rank_units * steps / elapsed
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -273,11 +289,7 @@ def run_ours(args):
         dist.barrier()
     if clocks:
         clocks.stop()
-    elapsed = t_start.elapsed_time(t_end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, dev)
     assert int(status.item()) == 0, "device status %#x" % int(status.item())
 
     # end to end through the public API: pinned host logits in, results out
@@ -307,11 +319,7 @@ def run_ours(args):
         e2e_step()
     x1.record(stream)
     torch.cuda.synchronize()
-    e2e_el = x0.elapsed_time(x1) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_el], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_el = float(t.item())
+    e2e_el = max_over_ranks(x0.elapsed_time(x1) / 1e3, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -326,7 +334,7 @@ def run_ours(args):
         gbps = bytes_per_step / step_s / 1e9
         traffic = committed_traffic(kernel_source_hash())
         line = {
-            "metric": METRIC, "value": world * B / step_s, "unit": "seqs/s", "n_gpus": world,
+            "metric": METRIC, "value": job_rate(world, B, args.steps, elapsed), "unit": "seqs/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "gbps_per_gpu": gbps,
@@ -334,7 +342,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": gbps, "peak": peak, "unit": "GB/s", "frac": gbps / peak,
                          "peak_kind": peak_kind, "traffic": traffic,
                          "kernel": "spec_verify_kernel<2, kLinearSample>"},
-            "e2e": {"value": world * B * e2e_steps / e2e_el, "unit": "seqs/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(world, B, e2e_steps, e2e_el), "unit": "seqs/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": args.steps,
             "clocks": clocks.summary() if clocks else None,

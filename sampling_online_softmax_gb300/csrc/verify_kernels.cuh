@@ -76,9 +76,13 @@ constexpr int kStageBytes = 2 * kRowBuf;
 constexpr int kChunk = 64;                           // 16-byte groups per residual chunk
 constexpr int kCpt = (kResidSliceBytes / 16 + 2 + kChunk - 1) / kChunk;  // residual chunks per tile
 static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout");
-constexpr int kSegTiles = 4;            // stats tiles per segment: one partial each, never split between warps
+#ifndef SPEC_SEG_TILES
+#define SPEC_SEG_TILES 4
+#endif
+constexpr int kSegTiles = SPEC_SEG_TILES;  // stats tiles per segment: one partial each, never split between warps
 constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
 constexpr int kMaxClaim = 2;            // residual tiles claimed at once (at most)
+constexpr int kTailZone = 4;            // below this many segments per warp left, grab without reserve
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr unsigned kFull = 0xffffffffu;
@@ -750,10 +754,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     int iseg = 0, ik = 0, ik1 = 0;     // that segment and its tiles [ik, ik1) still to issue
     unsigned s_ahead = 0;              // lane 0: start of the next stats grab
     int s_ahead_n = 0;                 // its size
+    bool ahead_issued = false;         // the next grab was requested ahead (away from the end)
     bool stats_done = (NSEG == 0);
     if (!stats_done) {
         s_ahead_n = guided(NSEG, kMaxGrab);
         if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
+        ahead_issued = true;
     }
     long long rc = 0, re = 0;          // residual tiles [rc, re) claimed, not yet issued
     int r_entry = -1;                  // entry of r_rec
@@ -900,6 +906,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             if (!stats_done) {
                 if (ik >= ik1) {
                     if (sc >= se) {
+                        // near the end a grab is made only when needed, so no warp holds work in reserve
+                        if (!ahead_issued && lane == 0)
+                            s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
                         const unsigned a = __shfl_sync(kFull, s_ahead, 0);
                         if (static_cast<long long>(a) >= NSEG) {
                             stats_done = true;
@@ -907,7 +916,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                             sc = a;
                             se = min(NSEG, static_cast<long long>(a) + s_ahead_n);
                             s_ahead_n = guided(NSEG - se, kMaxGrab);
-                            if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
+                            ahead_issued = NSEG - se >= kTailZone * nwarps;
+                            if (ahead_issued && lane == 0)
+                                s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
                         }
                     }
                     if (!stats_done) {
