@@ -95,13 +95,13 @@ Slicing resid_slicing(int V, int eb) {
 // Workspace layout (16-byte aligned parts):
 //   [counters: 4 u32][stats tiles per unit: n_units u32][units per sequence: B u32]
 //   [decided / accepted masks: B u64]
-//   [accept bits: B*K i32][argmax: n_units i32][segment partials: n_units*2*nseg uint2]
+//   [accept bits: B*K i32][argmax: n_units i32][run partials: n_units*2*S u64]
 //   [t(x), d(x): n_units * 2 u64][draw statistics: n_units float4]
 //   [draw entries: B u32][residual tiles per entry: B u32][chunk sums: B*Sr*kCpt i64]
 struct WsLayout {
     size_t ctrl, unit_cnt, seq_cnt, seqmask, acc, val, part, tx, stats, rq, res_cnt, csum, total;
 };
-WsLayout ws_layout(int B, int K, int units_per_seq, int nseg, int Sr, bool draws) {
+WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, bool draws) {
     const size_t n_units = static_cast<size_t>(B) * units_per_seq;
     WsLayout w;
     w.ctrl = 0;
@@ -111,7 +111,7 @@ WsLayout ws_layout(int B, int K, int units_per_seq, int nseg, int Sr, bool draws
     w.acc = w.seqmask + align16(static_cast<size_t>(B) * 8);
     w.val = w.acc + align16(static_cast<size_t>(B) * K * 4);
     w.part = w.val + align16(n_units * 4);
-    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(nseg) * 8);
+    w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
     w.stats = w.tx + align16(n_units * 16);
     const size_t entries = draws ? static_cast<size_t>(B) : 0;
     w.rq = w.stats + (draws ? align16(n_units * 16) : 0);
@@ -137,13 +137,13 @@ void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
 }
 
 WsLayout layout_linear(int B, int K, int V, int eb) {
-    return ws_layout(B, K, K + 1, segments_per_row(V, eb), resid_slicing(V, eb).S, true);
+    return ws_layout(B, K, K + 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
 }
 WsLayout layout_bonus(int B, int V, int eb) {
-    return ws_layout(B, 0, 1, segments_per_row(V, eb), resid_slicing(V, eb).S, true);
+    return ws_layout(B, 0, 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
 }
 WsLayout layout_tree(int B, int N, int V, int eb) {
-    return ws_layout(B, 0, N, segments_per_row(V, eb), resid_slicing(V, eb).S, false);
+    return ws_layout(B, 0, N, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, false);
 }
 
 // Resident blocks per SM for this kernel and shared-memory size (cached).
@@ -217,6 +217,10 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     const long long want = std::max<long long>(1, (p.stats_segs + kWarps - 1) / kWarps);
     const long long grid = std::min<long long>(want, static_cast<long long>(per_sm) * di.sms);
     const long long warps = grid * kWarps;
+    // small problems: a static split of the tiles, balanced to one tile; large ones: dynamic segments
+    p.stats_tiles = static_cast<long long>(p.B) * p.rows_per_seq * p.S;
+    p.nwarps = static_cast<int>(warps);
+    p.static_split = p.stats_tiles <= kStaticTilesPerWarp * warps ? 1 : 0;
     if (p.stats_segs + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxClaim >= (1ll << 31))
         return fail(SPEC_ERR_UNSUPPORTED, "too many tiles (B=%d, V=%d)", p.B, p.V);
     spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, dyn, stream>>>(p);

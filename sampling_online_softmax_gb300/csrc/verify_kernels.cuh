@@ -83,6 +83,7 @@ constexpr int kSegTiles = SPEC_SEG_TILES;  // stats tiles per segment: one parti
 constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
 constexpr int kMaxClaim = 2;            // residual tiles claimed at once (at most)
 constexpr int kTailZone = 4;            // below this many segments per warp left, grab without reserve
+constexpr long long kStaticTilesPerWarp = 32;  // up to this many stats tiles per warp: a static split
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 21;
 constexpr unsigned kFull = 0xffffffffu;
@@ -113,7 +114,10 @@ struct Params {
     int units_per_seq;             // K+1 (linear), N (tree), 1 (extra token alone)
     int n_units;
     int S;                         // stats tiles per row (windows of kTileBytes on the 16-byte grid)
-    int nseg;                      // segments per row: ceil(S / kSegTiles)
+    int nseg;                      // segments per row: ceil(S / kSegTiles) (dynamic mode)
+    int static_split;              // 1: warp w reduces stats tiles [T*w/W, T*(w+1)/W) (small problems)
+    long long stats_tiles;         // T = rows * S
+    int nwarps;                    // W = grid * kWarps
     int Sr, Lr;                    // residual slices per entry, elements per slice
     int nstage;                    // stages per warp ring (2..kMaxStages)
     long long stats_segs;          // B * rows_per_seq * nseg
@@ -138,7 +142,7 @@ struct Params {
     unsigned long long *ws_seqmask;  // [B] decided bits 0..31, accepted bits 32..63 (linear, K < 32)
     int32_t *ws_acc;               // [B*K] accept bits
     int32_t *ws_val;               // [B*units_per_seq] argmax per unit (greedy)
-    unsigned long long *ws_part;   // [n_units * 2 * nseg] segment partials: (mc | s << 32) or (max | (index + 1) << 32)
+    unsigned long long *ws_part;   // [n_units * 2 * S] run partials at the run's first tile: (mc | s << 32) or (max | (index + 1) << 32)
     unsigned long long *ws_txw;    // [n_units * 2] the draft token's logit in each row: bits | 1 << 32
     float4 *ws_stats;              // [n_units] (MCt, 1/St, MCd, 1/Sd) of units that may draw
     uint32_t *ws_rq;               // [B] draw entries
@@ -646,6 +650,27 @@ __device__ __forceinline__ bool row_slot(const Params &p, int rs, int bpos, int 
     return true;
 }
 
+// Row id (index in the stats tiling) of row r of unit (b, pos); the inverse of
+// the kernel's row decoding.  pos < 0 (an invalid length) reads row 0.
+template <int MODE>
+__device__ __forceinline__ int row_id_of(const Params &p, int b, int pos, int r) {
+    if (MODE == kLinearSample) return (pos < p.K) ? (pos * p.B + b) * 2 + r : 2 * p.K * p.B + b;
+    if (MODE == kLinearGreedy) return pos * p.B + b;
+    if (MODE == kTreeGreedy) return b * p.rows_per_seq + pos;
+    if (MODE == kBonusSample) return b * 2 + r;
+    return b;  // kBonusGreedy
+}
+
+// Does a run of stats tiles start at global tile t?  Static split: at every
+// warp's first tile and at every row start; dynamic: at every segment start.
+__device__ __forceinline__ bool run_starts_at(const Params &p, long long t, int k) {
+    if (!p.static_split) return (k % kSegTiles) == 0;
+    if (k == 0) return true;
+    const long long T = p.stats_tiles, W = p.nwarps;
+    const long long w = (t * W + T - 1) / T;  // the first warp whose range starts at or after t
+    return (T * w) / W == t;
+}
+
 // =================================================================== kernel
 template <int EB, int MODE>
 __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const Params p) {
@@ -748,15 +773,22 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
 
     // ---------------------------------------------------------- issue side
-    long long sc = 0, se = 0;          // stats segments [sc, se) grabbed, not yet begun
-    Row irow = {};                     // the row of the segment being issued
+    // dynamic: stats segments [sc, se) grabbed, not yet begun; static: this warp's tiles [sc, se)
+    long long sc = 0, se = 0;
+    Row irow = {};                     // the row of the run being issued
     irow.id = -1;
-    int iseg = 0, ik = 0, ik1 = 0;     // that segment and its tiles [ik, ik1) still to issue
+    int ik = 0, ik1 = 0;               // that run's tiles [ik, ik1) still to issue (within the row)
+    int irun_last = 0;                 // the run's last tile
     unsigned s_ahead = 0;              // lane 0: start of the next stats grab
     int s_ahead_n = 0;                 // its size
     bool ahead_issued = false;         // the next grab was requested ahead (away from the end)
     bool stats_done = (NSEG == 0);
-    if (!stats_done) {
+    if (p.static_split) {
+        const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
+        sc = p.stats_tiles * gw / p.nwarps;
+        se = p.stats_tiles * (gw + 1) / p.nwarps;
+        stats_done = sc >= se;
+    } else if (!stats_done) {
         s_ahead_n = guided(NSEG, kMaxGrab);
         if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
         ahead_issued = true;
@@ -785,9 +817,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         const int id = static_cast<int>(static_cast<unsigned>(sg) / static_cast<unsigned>(p.nseg));
         const int j = static_cast<int>(sg) - id * p.nseg;
         if (id != irow.id) irow = decode_row(id);
-        iseg = static_cast<int>(sg);
         ik = j * kSegTiles;
         ik1 = min(S, ik + kSegTiles);
+        irun_last = ik1 - 1;
+        return irow.present;
+    };
+    // static split: begin the next run of this warp's tiles (up to the row's end)
+    auto begin_static_run = [&]() -> bool {
+        const int id = static_cast<int>(static_cast<unsigned long long>(sc) / static_cast<unsigned>(S));
+        const int k = static_cast<int>(sc - static_cast<long long>(id) * S);
+        const int n = static_cast<int>(min(static_cast<long long>(S - k), se - sc));
+        if (id != irow.id) irow = decode_row(id);
+        ik = k;
+        ik1 = k + n;
+        irun_last = ik1 - 1;
+        sc += n;
         return irow.present;
     };
     // issue tile ik of the current segment
@@ -797,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         uintptr_t w0, w1, c0, c1;
         tile_window(irow, ik, w0, w1, c0, c1);
         if (lane == 0) {
-            wc.desc[s] = make_int4(kTileStats, iseg, ik, 0);
+            wc.desc[s] = make_int4(kTileStats, irow.id, ik, irun_last);
             const uint32_t bar = ptx::smem_addr(&wc.full[s]);
             const uint32_t bytes = static_cast<uint32_t>(c1 - c0);
             ptx::mbar_arrive_expect_tx(bar, bytes);
@@ -903,7 +947,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 }
             }
             // 2. the next stats tile
-            if (!stats_done) {
+            if (!stats_done && p.static_split) {
+                if (ik >= ik1) {
+                    if (sc >= se) {
+                        stats_done = true;
+                    } else if (!begin_static_run()) {  // a row slot with no row
+                        ik = ik1 = 0;
+                        continue;
+                    }
+                }
+                if (!stats_done) {
+                    issue_stats();
+                    return true;
+                }
+            }
+            if (!stats_done && !p.static_split) {
                 if (ik >= ik1) {
                     if (sc >= se) {
                         // near the end a grab is made only when needed, so no warp holds work in reserve
@@ -987,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     // ----------------------------------------------------- processing side
     // the stats segment being reduced (one row, tiles [k0, k1)), and the residual run
     bool srun = false;
-    int run_seg = -1, run_last = 0, run_len = 0;
+    int run_k0 = 0, run_last = 0, run_len = 0;
     Row prow = {};
     prow.id = -1;
     int px = -1;                       // the draft token whose logit this row holds, or -1
@@ -1173,8 +1231,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             float v = neg_inf(), sm = 0.f;
             int ii = INT_MAX;
             if (r < nrows) {
-                for (int k = lane; k < p.nseg; k += 32) {
-                    unsigned long long *slot = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * p.nseg + k];
+                const long long t0 = static_cast<long long>(row_id_of<MODE>(p, b, pos, r)) * S;
+                for (int k = lane; k < S; k += 32) {
+                    if (!run_starts_at(p, t0 + k, k)) continue;  // every run publishes at its first tile
+                    unsigned long long *slot = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * S + k];
                     bool late = false;
                     const unsigned long long w = await64(slot, late);  // every segment publishes once
                     if (late) {
@@ -1537,8 +1597,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (lane == 0) {
             const uint2 part = T::kSample ? make_uint2(__float_as_uint(am), __float_as_uint(as))
                                           : make_uint2(__float_as_uint(am), static_cast<unsigned>(ai) + 1u);
-            const int j = run_seg - prow.id * p.nseg;
-            st_relaxed64(&p.ws_part[(static_cast<size_t>(prow.unit) * 2 + prow.r) * p.nseg + j],
+            st_relaxed64(&p.ws_part[(static_cast<size_t>(prow.unit) * 2 + prow.r) * S + run_k0],
                          static_cast<unsigned long long>(part.x) | (static_cast<unsigned long long>(part.y) << 32));
             if (hasx)
                 st_relaxed64(&p.ws_txw[static_cast<size_t>(prow.unit) * 2 + prow.r],
@@ -1582,13 +1641,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (d.x == kTileStats) {
             const int k = d.z;
             if (!srun) {
-                // a new segment: its row, and fresh lane statistics
-                const int id = static_cast<int>(static_cast<unsigned>(d.y) / static_cast<unsigned>(p.nseg));
-                const int j = d.y - id * p.nseg;
-                if (id != prow.id) prow = decode_row(id);
+                // a new run: its row, and fresh lane statistics
+                if (d.y != prow.id) prow = decode_row(d.y);
                 srun = true;
-                run_seg = d.y;
-                run_last = min(S, (j + 1) * kSegTiles) - 1;
+                run_k0 = k;
+                run_last = d.w;
                 run_len = 0;
                 am = neg_inf();
                 as = 0.f;
