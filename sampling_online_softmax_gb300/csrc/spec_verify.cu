@@ -43,6 +43,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     int sms = 0;
     size_t max_dyn = 0;  // opt-in dynamic shared memory per block
+    size_t l2 = 0;       // L2 cache bytes
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -55,10 +56,12 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(SPEC_ERR_UNSUPPORTED, "device index %d", dev);
     std::call_once(g_dev_once[dev], [dev]() {
-        int sms = 0, smem = 0;
+        int sms = 0, smem = 0, l2 = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
         g_dev[dev].sms = sms;
+        g_dev[dev].l2 = l2 > 0 ? static_cast<size_t>(l2) : 0;
         g_dev[dev].max_dyn = static_cast<size_t>(smem);  // less each kernel's static shared memory
     });
     *out = g_dev[dev];
@@ -97,7 +100,8 @@ Slicing resid_slicing(int V, int eb) {
 //   [decided / accepted masks: B u64]
 //   [accept bits: B*K i32][argmax: n_units i32][run partials: n_units*2*S u64]
 //   [t(x), d(x): n_units * 2 u64][draw statistics: n_units float4]
-//   [draw entries: B u32][residual tiles per entry: B u32][chunk sums: B*Sr*kCpt i64]
+//   [draw entries: B lines of kEntWords u32, the record at word 0 and the residual
+//    tile count at word 16][chunk sums: B*Sr*kCpt i64]
 struct WsLayout {
     size_t ctrl, unit_cnt, seq_cnt, seqmask, acc, val, part, tx, stats, rq, res_cnt, csum, total;
 };
@@ -115,8 +119,8 @@ WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, bool draws) {
     w.stats = w.tx + align16(n_units * 16);
     const size_t entries = draws ? static_cast<size_t>(B) : 0;
     w.rq = w.stats + (draws ? align16(n_units * 16) : 0);
-    w.res_cnt = w.rq + align16(entries * 4);
-    w.csum = w.res_cnt + align16(entries * 4);
+    w.res_cnt = w.rq + 64;  // in the record's line
+    w.csum = w.rq + entries * kEntWords * 4;
     w.total = w.csum + align16(entries * static_cast<size_t>(Sr) * kCpt * 8);
     return w;
 }
@@ -221,6 +225,15 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     p.stats_tiles = static_cast<long long>(p.B) * p.rows_per_seq * p.S;
     p.nwarps = static_cast<int>(warps);
     p.static_split = p.stats_tiles <= kStaticTilesPerWarp * warps ? 1 : 0;
+    // Rows a residual pass may re-read, in stream order, up to 1/kKeepDiv of L2, are read at normal
+    // L2 priority and everything else first-to-evict, so the first draws find their rows in L2:
+    // the row pairs of the first positions (linear), or every row (extra token alone).
+    p.keep_rows = 0;
+    if (draws) {
+        const long long budget = static_cast<long long>(di.l2 / kKeepDiv) / (static_cast<long long>(p.V) * EB);
+        const long long cand = (MODE == kLinearSample) ? 2ll * p.K * p.B : static_cast<long long>(p.B) * p.rows_per_seq;
+        p.keep_rows = static_cast<int>(std::min(budget, cand));
+    }
     if (p.stats_segs + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxClaim >= (1ll << 31))
         return fail(SPEC_ERR_UNSUPPORTED, "too many tiles (B=%d, V=%d)", p.B, p.V);
     spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, dyn, stream>>>(p);

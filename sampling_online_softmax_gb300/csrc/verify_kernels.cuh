@@ -81,8 +81,17 @@ static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout
 #endif
 constexpr int kSegTiles = SPEC_SEG_TILES;  // stats tiles per segment: one partial each, never split between warps
 constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
-constexpr int kMaxClaim = 2;            // residual tiles claimed at once (at most)
+#ifndef SPEC_MAX_CLAIM
+#define SPEC_MAX_CLAIM 4
+#endif
+constexpr int kMaxClaim = SPEC_MAX_CLAIM;  // residual tiles claimed at once (at most)
 constexpr int kTailZone = 4;            // below this many segments per warp left, grab without reserve
+#ifndef SPEC_KEEP_DIV
+#define SPEC_KEEP_DIV 4
+#endif
+constexpr int kKeepDiv = SPEC_KEEP_DIV;  // rows kept in L2 for a residual pass: at most 1/kKeepDiv of L2
+constexpr int kEntWords = 32;           // a draw entry's record and counter share one 128-byte line of their own
+constexpr int kHold = 12;               // chunk sums per lane held in registers while an extra token is located
 constexpr long long kStaticTilesPerWarp = 32;  // up to this many stats tiles per warp: a static split
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSpinLimit = 1u << 21;
@@ -118,6 +127,8 @@ struct Params {
     int static_split;              // 1: warp w reduces stats tiles [T*w/W, T*(w+1)/W) (small problems)
     long long stats_tiles;         // T = rows * S
     int nwarps;                    // W = grid * kWarps
+    int keep_rows;                 // stats rows with id < keep_rows are read at normal L2 priority (the
+                                   // rest first-to-evict), so that a residual pass finds them in L2
     int Sr, Lr;                    // residual slices per entry, elements per slice
     int nstage;                    // stages per warp ring (2..kMaxStages)
     long long stats_segs;          // B * rows_per_seq * nseg
@@ -145,8 +156,8 @@ struct Params {
     unsigned long long *ws_part;   // [n_units * 2 * S] run partials at the run's first tile: (mc | s << 32) or (max | (index + 1) << 32)
     unsigned long long *ws_txw;    // [n_units * 2] the draft token's logit in each row: bits | 1 << 32
     float4 *ws_stats;              // [n_units] (MCt, 1/St, MCd, 1/Sd) of units that may draw
-    uint32_t *ws_rq;               // [B] draw entries
-    uint32_t *ws_res_cnt;          // [B] residual tiles finished per entry
+    uint32_t *ws_rq;               // draw entry e's record: ws_rq[e * kEntWords]
+    uint32_t *ws_res_cnt;          // its residual tiles counted: ws_res_cnt[e * kEntWords] (same line)
     unsigned long long *ws_csum;   // [B * Sr * kCpt] residual chunk sums, stored plus one
 };
 
@@ -562,9 +573,13 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
     const unsigned long long c2 = f2pack(c, c);
     const unsigned long long nmt = f2pack(-js.x, -js.x), ist = f2pack(js.y, js.y);
     const unsigned long long nmd = f2pack(-js.z, -js.z), isd = f2pack(js.w, js.w);
+    static_assert(kChunk == 64, "two groups per lane and chunk");
 #pragma unroll
     for (int ch = 0; ch < kCpt; ++ch) q[ch] = 0;
-    for (int g = lane; g < ngran; g += 32) {
+#pragma unroll
+    for (int it = 0; it < 2 * kCpt; ++it) {
+        const int g = it * 32 + lane;  // chunk it / 2
+        if (g >= ngran) break;
         unsigned long long t2[P], d2[P];
         Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bt + 16 * g), t2);
         if (pair) {
@@ -595,11 +610,7 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
         }
         float se, so;
         f2unpack(acc, se, so);
-        const long long qq = fixq(se + so);
-        const int chunk = g >> 6;
-#pragma unroll
-        for (int ch = 0; ch < kCpt; ++ch)
-            if (chunk == ch) q[ch] += qq;
+        q[it >> 1] += fixq(se + so);
     }
 #pragma unroll
     for (int ch = 0; ch < kCpt; ++ch) q[ch] = warp_sum64(q[ch]);
@@ -773,6 +784,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
 
     // ---------------------------------------------------------- issue side
+    const uint64_t pol_first = ptx::policy_evict_first();
     // dynamic: stats segments [sc, se) grabbed, not yet begun; static: this warp's tiles [sc, se)
     long long sc = 0, se = 0;
     Row irow = {};                     // the row of the run being issued
@@ -801,9 +813,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     bool claim_inflight = false;
     unsigned claim_res = 0;            // lane 0: start of a residual claim in flight
     int claim_n = 0;
+    long long claim_seen = 0;          // residual tiles claimed by all warps, as of this warp's last claim
     bool res_done = (RT == 0);
-    unsigned hint_tail = 0, hint_claim = 0;  // lane 0: counters read at the previous look
-    bool hint_valid = false;
     int issued = 0, handled = 0;
     int islot = 0;                     // stage of the next issue
     auto next_islot = [&]() {
@@ -845,8 +856,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             const uint32_t bar = ptx::smem_addr(&wc.full[s]);
             const uint32_t bytes = static_cast<uint32_t>(c1 - c0);
             ptx::mbar_arrive_expect_tx(bar, bytes);
-            if (bytes)
-                ptx::bulk_g2s(ptx::smem_addr(buf + (c0 - w0)), reinterpret_cast<const void *>(c0), bytes, bar);
+            if (bytes) {
+                // rows a residual pass is likely to re-read stay in L2 at normal priority; the rest
+                // of the stream is marked first to go
+                if (irow.id < p.keep_rows)
+                    ptx::bulk_g2s(ptx::smem_addr(buf + (c0 - w0)), reinterpret_cast<const void *>(c0), bytes, bar);
+                else
+                    ptx::bulk_g2s_hint(ptx::smem_addr(buf + (c0 - w0)), reinterpret_cast<const void *>(c0), bytes,
+                                       bar, pol_first);
+            }
         }
         ++ik;
         ++issued;
@@ -874,12 +892,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 bytes = static_cast<uint32_t>(g0.c1 - g0.c0) + (pair ? static_cast<uint32_t>(g1.c1 - g1.c0) : 0u);
             ptx::mbar_arrive_expect_tx(bar, bytes);
             if (!skip) {
+                // the last read of these rows: they may leave L2 first
                 if (g0.c1 > g0.c0)
-                    ptx::bulk_g2s(ptx::smem_addr(buf + g0.c0), g0.glo + g0.c0, static_cast<uint32_t>(g0.c1 - g0.c0),
-                                  bar);
+                    ptx::bulk_g2s_hint(ptx::smem_addr(buf + g0.c0), g0.glo + g0.c0,
+                                       static_cast<uint32_t>(g0.c1 - g0.c0), bar, pol_first);
                 if (pair && g1.c1 > g1.c0)
-                    ptx::bulk_g2s(ptx::smem_addr(buf + kRowBuf + g1.c0), g1.glo + g1.c0,
-                                  static_cast<uint32_t>(g1.c1 - g1.c0), bar);
+                    ptx::bulk_g2s_hint(ptx::smem_addr(buf + kRowBuf + g1.c0), g1.glo + g1.c0,
+                                       static_cast<uint32_t>(g1.c1 - g1.c0), bar, pol_first);
             }
         }
         ++issued;
@@ -898,6 +917,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             if (claim_inflight) {
                 const unsigned r = __shfl_sync(kFull, claim_res, 0);
                 claim_inflight = false;
+                claim_seen = static_cast<long long>(r) + claim_n;
                 if (static_cast<long long>(r) >= RT) {
                     res_done = true;
                 } else {
@@ -921,10 +941,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     if (r_rec == 0 && blocking) {
                         uint32_t rec = 0;
                         if (lane == 0) {
-                            rec = ld_relaxed(&p.ws_rq[e]);
+                            rec = ld_relaxed(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
                             for (uint32_t i = 0; rec == 0 && i < kSpinLimit; ++i) {
                                 __nanosleep(128);
-                                rec = ld_relaxed(&p.ws_rq[e]);
+                                rec = ld_relaxed(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
                             }
                         }
                         r_rec = __shfl_sync(kFull, rec, 0);
@@ -936,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                         }
                     }
                     if (r_rec == 0 && !rec_inflight) {  // look again at the next call
-                        if (lane == 0) rec_val = ld_relaxed(&p.ws_rq[e]);
+                        if (lane == 0) rec_val = ld_relaxed(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
                         rec_inflight = true;
                     }
                 }
@@ -991,39 +1011,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     return true;
                 }
             }
-            // 3. stats exhausted: claim residual tiles of published entries (wait for some if blocking)
+            // 3. stats exhausted: claim residual tiles.  Every sequence publishes exactly one draw
+            //    entry, so the entry of every claimed tile appears; step 1 waits for its record.
             if (!res_done && rc >= re && !claim_inflight) {
-                int avail = 0, all = 0;
-                if (lane == 0) {
-                    if (blocking || !hint_valid) {
-                        hint_tail = ld_relaxed(&p.ws_ctrl[2]);
-                        hint_claim = ld_relaxed(&p.ws_ctrl[3]);
-                    }
-                    const long long a2 = static_cast<long long>(hint_tail) * p.Sr - static_cast<long long>(hint_claim);
-                    avail = static_cast<int>(a2 < 0 ? 0 : (a2 > kMaxClaim ? kMaxClaim : a2));
-                    all = static_cast<long long>(hint_claim) >= RT ? 1 : 0;
-                }
-                hint_valid = true;
-                avail = __shfl_sync(kFull, avail, 0);
-                all = __shfl_sync(kFull, all, 0);
-                if (all) {
-                    res_done = true;
-                    continue;
-                }
-                if (avail > 0) {
-                    claim_resid(avail);
-                    if (blocking) continue;
-                    return false;
-                }
-                if (!blocking) {
-                    if (lane == 0) {  // fresh counters for the next look
-                        hint_tail = ld_relaxed(&p.ws_ctrl[2]);
-                        hint_claim = ld_relaxed(&p.ws_ctrl[3]);
-                    }
-                    return false;
-                }
-                __nanosleep(256);  // nothing published yet: every unfinished unit is held by a running warp
-                continue;
+                // once what is left (as far as this warp knows) fits one round of every warp, an even
+                // share of it; before that one tile at a time, which keeps the warps balanced
+                const long long left = RT - claim_seen;
+                const long long share = (left + nwarps - 1) / nwarps;
+                claim_resid(share <= kMaxClaim ? static_cast<int>(max(1ll, share)) : 1);
+                if (blocking) continue;
+                return false;
             }
             if (!blocking) return false;
             if (stats_done && res_done && rc >= re && !claim_inflight) return false;
@@ -1056,7 +1053,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     bool rrun = false;
     long long r_next = -1;             // residual tile that would continue the residual run
     int r_len = 0;
-    int r_e = 0, r_u = 0, r_b = 0, r_pos = 0;
+    int r_e = -1, r_u = 0, r_b = 0, r_pos = 0;
+    uint32_t r_rec_run = 0;            // the residual run's record
     bool r_pair = false, r_skip = false;
     float4 r_js = make_float4(0.f, 0.f, 0.f, 0.f);
     // a counter increment whose result is consumed later (1: unit tiles, 2: residual tiles)
@@ -1138,20 +1136,21 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     auto push_entry = [&](int u, bool pair, bool skip) {
         if (lane == 0) {
             const unsigned e = atomicAdd(&p.ws_ctrl[2], 1u);
-            st_release(&p.ws_rq[e], (static_cast<uint32_t>(u) + 1u) | (pair ? kRecPair : 0u) | (skip ? kRecSkip : 0u));
+            st_release(&p.ws_rq[static_cast<size_t>(e) * kEntWords], (static_cast<uint32_t>(u) + 1u) | (pair ? kRecPair : 0u) | (skip ? kRecSkip : 0u));
         }
         __syncwarp();
     };
 
     // The first rejection j of linear sequence b is known: draw the extra token
     // (publish a draw entry) or emit the sequence; unit j's scratch is ours.
-    auto draw_or_emit = [&](int b, int j) {
+    // skip: 1 / 0 when the caller knows whether unit j is non-finite, -1 if not.
+    auto draw_or_emit = [&](int b, int j, int skip) {
         const int U = p.units_per_seq;
         const int u = b * U + j;
         if (MODE == kLinearSample) {
             if (draws) {
-                const float4 js = __ldcg(&p.ws_stats[u]);
-                push_entry(u, j < p.K, !(js.y > 0.f));  // a non-finite unit recorded 1/St = 0
+                if (skip < 0) skip = (__ldcg(&p.ws_stats[u]).y > 0.f) ? 0 : 1;  // a non-finite unit recorded 1/St = 0
+                push_entry(u, j < p.K, skip != 0);
             } else {
                 emit_linear(b, j, -1, false);
             }
@@ -1209,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 break;
             }
         }
-        draw_or_emit(b, j);
+        draw_or_emit(b, j, -1);
         cleanup_seq(b, j, false);
     };
 
@@ -1224,38 +1223,58 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             x = __ldg(&p.tokens[static_cast<size_t>(b) * K + pos]);
             if (MODE == kLinearSample) ua = __ldg(&p.u_accept[static_cast<size_t>(b) * K + pos]);
         }
+        // t(x), d(x): lane 0 loads them with its first partials and waits for them after the merge
+        const bool want_tx = MODE == kLinearSample && pos >= 0 && pos < K && x >= 0 && x < p.V;
+        unsigned long long *txs = p.ws_txw + static_cast<size_t>(u) * 2;
+        unsigned long long txw[2] = {0ull, 0ull};
+        long long t0[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) t0[r] = static_cast<long long>(row_id_of<MODE>(p, b, pos, r < nrows ? r : 0)) * S;
         float Mr[2], Sm[2];
         int Ar[2];
+        float v[2] = {neg_inf(), neg_inf()}, sm[2] = {0.f, 0.f};
+        int ii[2] = {INT_MAX, INT_MAX};
+        // every run publishes one partial at its first tile; both rows' loads are issued before any wait
+        for (int k = lane; k < S; k += 32) {
+            unsigned long long *slot[2];
+            unsigned long long w[2];
+            bool has[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                slot[r] = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * S + k];
+                has[r] = r < nrows && run_starts_at(p, t0[r] + k, k);
+                w[r] = has[r] ? ld_relaxed64(slot[r]) : 0ull;
+            }
+            if (want_tx && k == 0) {  // lane 0's first slot
+                txw[0] = ld_relaxed64(&txs[0]);
+                txw[1] = ld_relaxed64(&txs[1]);
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (!has[r]) continue;
+                bool late = false;
+                if (w[r] == 0ull) w[r] = await64(slot[r], late);  // every run publishes once
+                if (late) {
+                    atomicOr(p.status, SPEC_DEV_TIMEOUT);
+                    continue;
+                }
+                *slot[r] = 0ull;
+                const uint2 e = make_uint2(static_cast<unsigned>(w[r]), static_cast<unsigned>(w[r] >> 32));
+                if (T::kSample)
+                    merge_sc(v[r], sm[r], __uint_as_float(e.x), __uint_as_float(e.y));
+                else
+                    merge_vi(v[r], ii[r], __uint_as_float(e.x), static_cast<int>(e.y - 1u));
+            }
+        }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            float v = neg_inf(), sm = 0.f;
-            int ii = INT_MAX;
-            if (r < nrows) {
-                const long long t0 = static_cast<long long>(row_id_of<MODE>(p, b, pos, r)) * S;
-                for (int k = lane; k < S; k += 32) {
-                    if (!run_starts_at(p, t0 + k, k)) continue;  // every run publishes at its first tile
-                    unsigned long long *slot = &p.ws_part[(static_cast<size_t>(u) * 2 + r) * S + k];
-                    bool late = false;
-                    const unsigned long long w = await64(slot, late);  // every segment publishes once
-                    if (late) {
-                        atomicOr(p.status, SPEC_DEV_TIMEOUT);
-                        continue;
-                    }
-                    *slot = 0ull;
-                    const uint2 e = make_uint2(static_cast<unsigned>(w), static_cast<unsigned>(w >> 32));
-                    if (T::kSample)
-                        merge_sc(v, sm, __uint_as_float(e.x), __uint_as_float(e.y));
-                    else
-                        merge_vi(v, ii, __uint_as_float(e.x), static_cast<int>(e.y - 1u));
-                }
-            }
             if (T::kSample)
-                warp_merge_sc(v, sm);
+                warp_merge_sc(v[r], sm[r]);
             else
-                warp_merge_vi(v, ii);
-            Mr[r] = v;
-            Sm[r] = sm;
-            Ar[r] = ii;
+                warp_merge_vi(v[r], ii[r]);
+            Mr[r] = v[r];
+            Sm[r] = sm[r];
+            Ar[r] = ii[r];
         }
         uint32_t fl = 0;
         bool finite = true;
@@ -1272,14 +1291,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             p.ws_unit_cnt[u] = 0u;
             if (MODE == kLinearSample && pos < K) {
                 float2 txv = make_float2(0.f, 0.f);
-                if (x >= 0 && x < p.V) {  // the segments holding x published its logits
+                if (want_tx) {  // the runs holding x published its logits
                     bool late = false;
-                    const unsigned long long wt = await64(&p.ws_txw[static_cast<size_t>(u) * 2], late);
-                    const unsigned long long wd = await64(&p.ws_txw[static_cast<size_t>(u) * 2 + 1], late);
+                    if (txw[0] == 0ull) txw[0] = await64(&txs[0], late);
+                    if (txw[1] == 0ull) txw[1] = await64(&txs[1], late);
                     if (late) fl |= SPEC_DEV_TIMEOUT;
-                    p.ws_txw[static_cast<size_t>(u) * 2] = 0ull;
-                    p.ws_txw[static_cast<size_t>(u) * 2 + 1] = 0ull;
-                    txv = make_float2(__uint_as_float(static_cast<unsigned>(wt)), __uint_as_float(static_cast<unsigned>(wd)));
+                    txs[0] = 0ull;
+                    txs[1] = 0ull;
+                    txv = make_float2(__uint_as_float(static_cast<unsigned>(txw[0])),
+                                      __uint_as_float(static_cast<unsigned>(txw[1])));
                 }
                 float px = 0.f, qx = 0.f, thr = 0.f;
                 if (x < 0 || x >= p.V) {
@@ -1330,7 +1350,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             __syncwarp();
             const unsigned long long now = old | bits;
             const int jn = first_rejection(now, K);
-            if (first_rejection(old, K) < 0 && jn >= 0) draw_or_emit(b, jn);
+            if (first_rejection(old, K) < 0 && jn >= 0) draw_or_emit(b, jn, jn == pos ? (finite ? 0 : 1) : -1);
             if (__popc(static_cast<unsigned>(now)) == K + 1) cleanup_seq(b, jn, true);
             return;
         }
@@ -1384,26 +1404,31 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     auto select_token = [&](int e, int b, int pos, bool pair, const float4 &js, float ub) -> int {
         const int n = p.Sr * kCpt;
         const unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * n;
+        // lane l owns the chunk sums [l0, l0 + m), l0 = lane * m; the first kHold stay in registers.  Each
+        // sum is stored plus one, so a zero means "not visible yet".
+        const int m = (n + 31) / 32;
+        const int l0 = lane * m;
         bool late = false;
-        // the total, in rounds of 256 loads issued together (each sum is stored plus one)
-        long long tot = 0;
-        for (int base = 0; base < n; base += 256) {
-            long long v[8];
+        long long v[kHold];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int i = base + r * 32 + lane;
-                v[r] = (i < n) ? static_cast<long long>(ld_relaxed64(&cs[i])) : 1;
-            }
+        for (int r = 0; r < kHold; ++r)
+            v[r] = (r < m && l0 + r < n) ? static_cast<long long>(ld_relaxed64(&cs[l0 + r])) : 1;
+        long long mine = 0;
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                if (v[r] == 0) {  // not visible yet
-                    const int i = base + r * 32 + lane;
-                    v[r] = static_cast<long long>(await64(&cs[i], late));
-                }
-                tot += v[r] - 1;
-            }
+        for (int r = 0; r < kHold; ++r) {
+            if (v[r] == 0) v[r] = static_cast<long long>(await64(&cs[l0 + r], late));
+            v[r] -= 1;
+            mine += v[r];
         }
-        tot = warp_sum64(tot);
+        for (int j = kHold; j < m && l0 + j < n; ++j)  // long rows only
+            mine += static_cast<long long>(await64(&cs[l0 + j], late)) - 1;
+        long long incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const long long tot = __shfl_sync(kFull, incl, 31);
         if (__any_sync(kFull, late)) {
             if (lane == 0) atomicOr(p.status, SPEC_DEV_TIMEOUT);
             return -1;
@@ -1412,46 +1437,31 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         const double ud = (ub >= 0.f) ? static_cast<double>(ub) : 0.0;  // a NaN uniform counts as 0
         long long target = static_cast<long long>(ud * static_cast<double>(tot));
         if (target >= tot) target = tot - 1;
-        // the chunk holding the target: rounds of 256 consecutive sums, 8 per lane
-        long long carry = 0, acc = 0;
-        int chunk = -1;
-        for (int base = 0; base < n && chunk < 0; base += 256) {
-            long long v[8];
-            long long mine = 0;
+        // the first chunk whose cumulative sum exceeds the target: its lane, then its place there
+        const unsigned bl = __ballot_sync(kFull, incl > target);
+        const int ol = __ffs(bl) - 1;  // bl != 0: lane 31 holds tot > target
+        int ch = -1;
+        long long a = incl - mine;
+        if (lane == ol) {
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int i = base + lane * 8 + r;
-                v[r] = (i < n) ? static_cast<long long>(ld_relaxed64(&cs[i])) - 1 : 0;
-                mine += v[r];
-            }
-            long long incl = mine;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const long long y = __shfl_up_sync(kFull, incl, off);
-                if (lane >= off) incl += y;
-            }
-            const unsigned bl = __ballot_sync(kFull, carry + incl > target);
-            if (bl) {
-                const int ol = __ffs(bl) - 1;
-                int ch = -1;
-                long long a = carry + incl - mine;
-                if (lane == ol) {
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        if (ch < 0) {
-                            if (a + v[r] > target)
-                                ch = base + lane * 8 + r;
-                            else
-                                a += v[r];
-                        }
-                    }
+            for (int r = 0; r < kHold; ++r) {
+                if (ch < 0 && r < m && l0 + r < n) {
+                    if (a + v[r] > target)
+                        ch = l0 + r;
+                    else
+                        a += v[r];
                 }
-                chunk = __shfl_sync(kFull, ch, ol);
-                acc = __shfl_sync(kFull, a, ol);
-            } else {
-                carry += __shfl_sync(kFull, incl, 31);
+            }
+            for (int j = kHold; ch < 0 && j < m && l0 + j < n; ++j) {  // seen non-zero above
+                const long long w = static_cast<long long>(ld_relaxed64(&cs[l0 + j])) - 1;
+                if (a + w > target)
+                    ch = l0 + j;
+                else
+                    a += w;
             }
         }
+        const int chunk = __shfl_sync(kFull, ch, ol);
+        const long long acc = __shfl_sync(kFull, a, ol);
         if (chunk < 0) return -1;  // (not reached: target < tot)
         const long long rem = target - acc;  // 0 <= rem < cs[chunk]
         // rescan that chunk from global memory with the same weights and order
@@ -1522,9 +1532,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         return token < 0 ? 0 : token;
     };
 
-    // Every residual tile of entry e is summed: draw, emit, and clean up.
+    // Every residual tile of entry e is summed: draw, emit, and clean up.  When this
+    // warp's last residual run was entry e, its record and statistics are at hand.
     auto finish_entry = [&](int e) {
-        const uint32_t rec = __ldcg(&p.ws_rq[e]);
+        const bool mine = (e == r_e);
+        const uint32_t rec = mine ? r_rec_run : __ldcg(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
         const int u = static_cast<int>(rec & kRecUnit) - 1;
         const bool pair = (rec & kRecPair) != 0;
         const bool skip = (rec & kRecSkip) != 0;
@@ -1538,7 +1550,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         int token = 0;
         if (!skip) {
-            const float4 js = __ldcg(&p.ws_stats[u]);
+            const float4 js = mine ? r_js : __ldcg(&p.ws_stats[u]);
             const float ub = __ldg(&p.u_bonus[b]);
             token = select_token(e, b, pos, pair, js, ub);
             if (token < 0 && pair) {
@@ -1559,8 +1571,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0ull;
         if (lane == 0) p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // the other units' by their sequence
         if (lane == 0) {
-            p.ws_rq[e] = 0u;
-            p.ws_res_cnt[e] = 0u;
+            p.ws_rq[static_cast<size_t>(e) * kEntWords] = 0u;
+            p.ws_res_cnt[static_cast<size_t>(e) * kEntWords] = 0u;
         }
         __syncwarp();
     };
@@ -1614,7 +1626,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     // the residual run ends: count its tiles
     auto close_resid = [&]() {
         resolve_pending();
-        if (lane == 0) pend_old = atomicAdd(&p.ws_res_cnt[r_e], static_cast<unsigned>(r_len));
+        if (lane == 0) pend_old = atomicAdd(&p.ws_res_cnt[static_cast<size_t>(r_e) * kEntWords], static_cast<unsigned>(r_len));
         pend_kind = 2;
         pend_entry = r_e;
         pend_add = r_len;
@@ -1710,9 +1722,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 r_e = e;
                 r_pair = (rec & kRecPair) != 0;
                 r_skip = (rec & kRecSkip) != 0;
+                r_rec_run = rec;
                 entry_unit(rec, r_u, r_b, r_pos);
                 if (!r_skip) {
-                    if (lane == 0) (void)ld_acquire(&p.ws_rq[e]);  // orders the loads of the entry's statistics
+                    if (lane == 0) (void)ld_acquire(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);  // orders the loads of the entry's statistics
                     __syncwarp();
                     r_js = __ldcg(&p.ws_stats[r_u]);
                 }
