@@ -61,6 +61,9 @@ def _declare(lib):
     lib.oracle_sample_bonus.restype = i32
     lib.oracle_verify_tree.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, P, P]
     lib.oracle_verify_tree.restype = i32
+    lib.oracle_verify_tree_sample.argtypes = [P, i32, i32, i32, i32, P, P, P, ctypes.c_float, i32,
+                                              P, P, P, P]
+    lib.oracle_verify_tree_sample.restype = i32
     lib.oracle_threads.argtypes = [i32]
     lib.oracle_threads.restype = i32
     return lib
@@ -163,4 +166,26 @@ def verify_tree(target, parents, node_tokens, max_depth, lib=None):
                                 _ptr(out["out_tokens"]))
     if rc != 0:
         raise ValueError("oracle_verify_tree rejected its arguments")
+    return out
+
+
+def verify_tree_sample(target, parents, node_tokens, u_nodes, temperature, max_depth, lib=None):
+    """Tree verify in sampling mode.  target [B, N, V], parents [N], node_tokens [B, N],
+    u_nodes [B, N] (the uniform of the target's draw at each node), temperature > 0.
+    node_cdf [B, N, 2] is every node's draw as its normalised cumulative interval."""
+    lib = lib or load()
+    target, dt = _logits(target)
+    B, N, V = target.shape
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(N)
+    tok = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
+    un = np.ascontiguousarray(u_nodes, dtype=np.float32).reshape(B, N)
+    out = dict(path_nodes=np.zeros((B, max_depth + 1), np.int32),
+               path_len=np.zeros(B, np.int32),
+               out_tokens=np.zeros((B, max_depth + 1), np.int32),
+               node_cdf=np.zeros((B, N, 2), np.float64))
+    rc = lib.oracle_verify_tree_sample(_ptr(target), dt, B, N, V, _ptr(par), _ptr(tok), _ptr(un),
+                                       float(temperature), int(max_depth), _ptr(out["path_nodes"]),
+                                       _ptr(out["path_len"]), _ptr(out["out_tokens"]), _ptr(out["node_cdf"]))
+    if rc != 0:
+        raise ValueError("oracle_verify_tree_sample rejected its arguments")
     return out

@@ -43,6 +43,11 @@
  *     take the first whose token equals argmax of the current node's target
  *     row; stop when none matches or max_depth nodes were accepted; the extra
  *     token is argmax at the last accepted node.
+ *   - tree, sampling mode (the page's "Greedy或者Sampling"): the target's
+ *     choice at node n is a draw from softmax(target_n / T) by inverse CDF
+ *     with the caller's uniform u[b, n]; the walk is the greedy walk with that
+ *     draw in place of the argmax, and the extra token is the draw at the last
+ *     accepted node.
  *
  * Precision: every logit is widened to double (fp32 directly; bf16 by placing
  * its 16 bits in the high half of an IEEE single), and all arithmetic is
@@ -334,6 +339,61 @@ int oracle_verify_tree(const void *target, int dtype, int B, int N, int V, const
         }
         path_len[b] = depth;
         ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);
+    }
+    return 0;
+}
+
+/*
+ * Tree verify in sampling mode ("Speculative-Decoding / Medusa", section 三,
+ * the sampled variant of the walk).  Arguments as oracle_verify_tree, plus
+ *   u_nodes [B, N]: the uniform for the target's draw at each node;
+ *   temperature > 0;
+ *   node_cdf [B, N, 2] or NULL: each node's draw as its normalised cumulative
+ *   interval [lo, hi) (every node is drawn, visited or not).
+ * The draw at node n is inverse_cdf(softmax(target_n / T), u[b, n]).
+ */
+int oracle_verify_tree_sample(const void *target, int dtype, int B, int N, int V, const int32_t *parents,
+                              const int32_t *node_tokens, const float *u_nodes, float temperature,
+                              int max_depth, int32_t *path_nodes, int32_t *path_len, int32_t *out_tokens,
+                              double *node_cdf) {
+    if (B < 0 || N < 1 || V < 1 || max_depth < 0 || !(temperature > 0.0f)) return 1;
+    const double T = (double)temperature;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t *draw = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+        for (int n = 0; n < N; ++n) {
+            double lo = 0.0, hi = 0.0;
+            softmax_row(target, dtype, (size_t)b * N + n, V, T, p, NULL, NULL);
+            draw[n] = inverse_cdf(p, V, (double)u_nodes[(size_t)b * N + n], &lo, &hi);
+            if (node_cdf) {
+                node_cdf[((size_t)b * N + n) * 2 + 0] = lo;
+                node_cdf[((size_t)b * N + n) * 2 + 1] = hi;
+            }
+        }
+        int32_t *pn = path_nodes + (size_t)b * (max_depth + 1);
+        int32_t *ot = out_tokens + (size_t)b * (max_depth + 1);
+        for (int d = 0; d <= max_depth; ++d) pn[d] = ot[d] = -1;
+        int cur = 0, depth = 0;
+        pn[0] = 0;
+        while (depth < max_depth) {
+            int next = -1;
+            for (int c = 1; c < N; ++c) {
+                if (parents[c] == cur && node_tokens[(size_t)b * N + c] == draw[cur]) {
+                    next = c;
+                    break;
+                }
+            }
+            if (next < 0) break;
+            ot[depth] = node_tokens[(size_t)b * N + next];
+            ++depth;
+            pn[depth] = next;
+            cur = next;
+        }
+        path_len[b] = depth;
+        ot[depth] = draw[cur];
+        free(p);
+        free(draw);
     }
     return 0;
 }

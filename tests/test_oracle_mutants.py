@@ -16,6 +16,7 @@ import pytest
 import oracle
 import test_oracle_pins as pins
 import test_tree_pins as tpins
+import test_tree_sample_pins as spins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
 
@@ -39,7 +40,18 @@ MUTANTS = [
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
     ("tree_extra_token_at_root", "ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);",
      "ot[depth] = argmax_row(target, dtype, (size_t)b * N + 0, V);"),
-    ("tree_any_child", "if (parents[c] == cur && node_tokens", "if (parents[c] >= 0 && node_tokens"),
+    ("tree_any_child", "if (parents[c] == cur && node_tokens[(size_t)b * N + c] == want)",
+     "if (parents[c] >= 0 && node_tokens[(size_t)b * N + c] == want)"),
+    ("tree_sample_temperature_dropped",
+     "softmax_row(target, dtype, (size_t)b * N + n, V, T, p, NULL, NULL);",
+     "softmax_row(target, dtype, (size_t)b * N + n, V, 1.0, p, NULL, NULL);"),
+    ("tree_sample_uniform_of_root", "(double)u_nodes[(size_t)b * N + n]", "(double)u_nodes[(size_t)b * N]"),
+    ("tree_sample_matches_root_draw", "node_tokens[(size_t)b * N + c] == draw[cur]",
+     "node_tokens[(size_t)b * N + c] == draw[0]"),
+    ("tree_sample_extra_is_argmax", "ot[depth] = draw[cur];",
+     "ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);"),
+    ("tree_sample_row_of_root", "softmax_row(target, dtype, (size_t)b * N + n, V, T, p, NULL, NULL);",
+     "softmax_row(target, dtype, (size_t)b * N, V, T, p, NULL, NULL);"),
 ]
 
 
@@ -56,6 +68,9 @@ def _pin_suite(lib):
         ("bf16", lambda: pins.test_bf16_decoding_equals_fp32_values(lib)),
         ("spike", lambda: pins.test_spiked_constant_row_closed_form(lib, 1000, 5.0, 1.0)),
         ("tree", lambda: _tree_check(lib)),
+        ("tree_sample_freq", lambda: spins.check_draw_frequencies(lib, V=4, T=0.5, M=4000)),
+        ("tree_sample_walk", lambda: spins.check_walk_brute_force(lib)),
+        ("tree_sample_greedy", lambda: spins.check_dominant_logit_is_greedy(lib)),
     ]
     for name, fn in checks:
         try:
