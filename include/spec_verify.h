@@ -90,6 +90,10 @@ size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype);
 /* Bytes of workspace spec_verify_tree needs for B sequences of N tree nodes. */
 size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype);
 
+/* Bytes of workspace spec_verify_tree_sample needs (one draw per node: grows
+ * with B * N * V). */
+size_t spec_workspace_bytes_tree_sample(int B, int N, int V, spec_dtype dtype);
+
 /*
  * Linear verify and (optionally) the extra token, in one launch.
  *
@@ -158,6 +162,30 @@ spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B,
                              int32_t *path_nodes, int32_t *path_len, int32_t *out_tokens,
                              uint32_t *dev_status, void *workspace, size_t workspace_bytes,
                              void *stream);
+
+/*
+ * Tree verify in sampling mode ("Speculative-Decoding / Medusa" blog, section
+ * 三: the target's choice at a node may be greedy or sampled).  At every node n
+ * the target's choice is a draw from softmax(target_n / T) by inverse CDF with
+ * the caller's uniform u_nodes[b, n] (the first v whose cumulative weight
+ * exceeds u * W, over exact int64 sums as in the linear draw).  The walk is that
+ * of spec_verify_tree with the draw in place of the argmax: from the root, move
+ * to the lowest-index child whose token equals the draw at the current node;
+ * stop when none does or max_depth nodes were accepted.  The extra token is
+ * the draw at the last accepted node.  Every node is drawn, visited or not
+ * (a data-parallel pass: two reads of every row, the second mostly from L2).
+ *
+ *   target_logits [B, N, V], parents [N], node_tokens [B, N]: as spec_verify_tree.
+ *   u_nodes       [B, N] fp32 in [0, 1): one uniform per node (device).
+ *   temperature   T > 0, finite.
+ *   max_depth, path_nodes, path_len, out_tokens, dev_status: as spec_verify_tree.
+ *   workspace, workspace_bytes: spec_workspace_bytes_tree_sample(B, N, V, dtype).
+ */
+spec_status spec_verify_tree_sample(const void *target_logits, spec_dtype dtype, int B, int N, int V,
+                                    const int32_t *parents, const int32_t *node_tokens, const float *u_nodes,
+                                    float temperature, int max_depth, int32_t *path_nodes, int32_t *path_len,
+                                    int32_t *out_tokens, uint32_t *dev_status, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /*
  * spec_verify_linear with the library's own workspace.  The pages describe no

@@ -124,3 +124,27 @@ def compare_tree(gpu: dict, ora: dict) -> ParityReport:
                 b, gpu["path_len"][b], list(gpu["path_nodes"][b]), list(gpu["out_tokens"][b]),
                 ora["path_len"][b], list(ora["path_nodes"][b]), list(ora["out_tokens"][b])))
     return rep
+
+
+def compare_tree_sample(gpu: dict, ora: dict, u_nodes) -> ParityReport:
+    """Sampled tree walk: paths and tokens equal, except where a uniform at a node of
+    either path lies within NEAR_TIE of that node's draw interval (counted as a tie)."""
+    rep = ParityReport()
+    u_nodes = np.asarray(u_nodes, np.float64)
+    B = len(ora["path_len"])
+    rep.sequences = B
+    for b in range(B):
+        if (gpu["path_len"][b] == ora["path_len"][b] and np.array_equal(gpu["path_nodes"][b], ora["path_nodes"][b])
+                and np.array_equal(gpu["out_tokens"][b], ora["out_tokens"][b])):
+            rep.exact += 1
+            continue
+        nodes = {int(n) for n in gpu["path_nodes"][b] if n >= 0} | {int(n) for n in ora["path_nodes"][b] if n >= 0}
+        near = any(min(abs(u_nodes[b, n] - ora["node_cdf"][b, n, 0]), abs(u_nodes[b, n] - ora["node_cdf"][b, n, 1]))
+                   < NEAR_TIE for n in nodes)
+        if near:
+            rep.bonus_ties += 1
+        else:
+            rep.failures.append("b=%d sampled tree: gpu len %d nodes %s tokens %s; oracle len %d nodes %s tokens %s" % (
+                b, gpu["path_len"][b], list(gpu["path_nodes"][b]), list(gpu["out_tokens"][b]),
+                ora["path_len"][b], list(ora["path_nodes"][b]), list(ora["out_tokens"][b])))
+    return rep

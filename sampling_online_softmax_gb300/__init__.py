@@ -14,6 +14,8 @@ Entry points (same names as the C ABI):
   spec_sample_bonus    the extra token alone, given accept_len
   spec_verify_tree     greedy walk of a Medusa candidate tree
                        ("Speculative-Decoding / Medusa", section 三)
+  spec_verify_tree_sample  the same walk with the target's choice drawn at
+                       every node (the section's sampled variant)
 """
 from __future__ import annotations
 
@@ -70,6 +72,8 @@ def load_library():
         lib.spec_workspace_bytes_bonus.restype = u64
         lib.spec_workspace_bytes_tree.argtypes = [i32, i32, i32, i32]
         lib.spec_workspace_bytes_tree.restype = u64
+        lib.spec_workspace_bytes_tree_sample.argtypes = [i32, i32, i32, i32]
+        lib.spec_workspace_bytes_tree_sample.restype = u64
         lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
         lib.spec_verify_linear.restype = i32
         lib.spec_verify_linear_static.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P]
@@ -78,6 +82,8 @@ def load_library():
         lib.spec_sample_bonus.restype = i32
         lib.spec_verify_tree.argtypes = [P, i32, i32, i32, i32, P, P, i32, P, P, P, P, P, u64, P]
         lib.spec_verify_tree.restype = i32
+        lib.spec_verify_tree_sample.argtypes = [P, i32, i32, i32, i32, P, P, P, f32, i32, P, P, P, P, P, u64, P]
+        lib.spec_verify_tree_sample.restype = i32
         lib.spec_status_string.argtypes = [i32]
         lib.spec_status_string.restype = ctypes.c_char_p
         lib.spec_last_error.argtypes = []
@@ -160,6 +166,10 @@ def spec_workspace_bytes_bonus(B: int, V: int, dtype) -> int:
 
 def spec_workspace_bytes_tree(B: int, N: int, V: int, dtype) -> int:
     return int(load_library().spec_workspace_bytes_tree(int(B), int(N), int(V), _dtype_arg(dtype)))
+
+
+def spec_workspace_bytes_tree_sample(B: int, N: int, V: int, dtype) -> int:
+    return int(load_library().spec_workspace_bytes_tree_sample(int(B), int(N), int(V), _dtype_arg(dtype)))
 
 
 def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperature, *,
@@ -297,5 +307,37 @@ def spec_verify_tree(target, parents, node_tokens, max_depth, *, status=None, ou
         st = lib.spec_verify_tree(_ptr(target), _dtype_code(target), B, N, V, _ptr(parents), _ptr(node_tokens), D,
                                   _ptr(out["path_nodes"]), _ptr(out["path_len"]), _ptr(out["out_tokens"]),
                                   _ptr(status), _ptr(ws), ws.numel(), h)
+    _check(st)
+    return out
+
+
+def spec_verify_tree_sample(target, parents, node_tokens, u_nodes, temperature, max_depth, *, status=None,
+                            out=None, workspace=None, stream=None):
+    """Tree walk with the target's choice drawn at every node (u_nodes [B, N] fp32);
+    returns dict(path_nodes, path_len, out_tokens, status)."""
+    lib = load_library()
+    _cuda(target, "target")
+    B, N, V = target.shape
+    dev = target.device
+    _cuda(parents, "parents", torch.int32)
+    _cuda(node_tokens, "node_tokens", torch.int32)
+    _cuda(u_nodes, "u_nodes", torch.float32)
+    h, s = _stream_handle(dev, stream)
+    D = int(max_depth)
+    if out is None:
+        out = dict(path_nodes=torch.empty((B, D + 1), dtype=torch.int32, device=dev),
+                   path_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, D + 1), dtype=torch.int32, device=dev))
+    if status is None:
+        with torch.cuda.stream(s):
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out["status"] = status
+    nbytes = spec_workspace_bytes_tree_sample(B, N, V, target.dtype)
+    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_tree_sample(_ptr(target), _dtype_code(target), B, N, V, _ptr(parents),
+                                         _ptr(node_tokens), _ptr(u_nodes), float(temperature), D,
+                                         _ptr(out["path_nodes"]), _ptr(out["path_len"]), _ptr(out["out_tokens"]),
+                                         _ptr(status), _ptr(ws), ws.numel(), h)
     _check(st)
     return out

@@ -105,7 +105,8 @@ Slicing resid_slicing(int V, int eb) {
 struct WsLayout {
     size_t ctrl, unit_cnt, seq_cnt, seqmask, acc, val, part, tx, stats, rq, res_cnt, csum, total;
 };
-WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, bool draws) {
+WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, size_t entries) {
+    const bool draws = entries > 0;
     const size_t n_units = static_cast<size_t>(B) * units_per_seq;
     WsLayout w;
     w.ctrl = 0;
@@ -117,7 +118,6 @@ WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, bool draws) {
     w.part = w.val + align16(n_units * 4);
     w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
     w.stats = w.tx + align16(n_units * 16);
-    const size_t entries = draws ? static_cast<size_t>(B) : 0;
     w.rq = w.stats + (draws ? align16(n_units * 16) : 0);
     w.res_cnt = w.rq + 64;  // in the record's line
     w.csum = w.rq + entries * kEntWords * 4;
@@ -140,14 +140,20 @@ void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
     p.ws_csum = reinterpret_cast<unsigned long long *>(ws + wl.csum);
 }
 
+// One draw entry per sequence (linear, extra token alone), per node (sampled
+// tree), or none (greedy tree).
 WsLayout layout_linear(int B, int K, int V, int eb) {
-    return ws_layout(B, K, K + 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
+    return ws_layout(B, K, K + 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, static_cast<size_t>(B));
 }
 WsLayout layout_bonus(int B, int V, int eb) {
-    return ws_layout(B, 0, 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, true);
+    return ws_layout(B, 0, 1, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, static_cast<size_t>(B));
 }
 WsLayout layout_tree(int B, int N, int V, int eb) {
-    return ws_layout(B, 0, N, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, false);
+    return ws_layout(B, 0, N, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S, 0);
+}
+WsLayout layout_tree_sample(int B, int N, int V, int eb) {
+    return ws_layout(B, 0, N, stats_tiles_per_row(V, eb), resid_slicing(V, eb).S,
+                     static_cast<size_t>(B) * static_cast<size_t>(N));
 }
 
 // Resident blocks per SM for this kernel and shared-memory size (cached).
@@ -199,9 +205,10 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     p.Sr = rs.S;
     p.Lr = rs.L;
     p.stats_segs = static_cast<long long>(p.B) * p.rows_per_seq * p.nseg;
-    p.res_tiles = draws ? static_cast<long long>(p.B) * p.Sr : 0;
+    p.res_tiles = draws ? static_cast<long long>(MODE == kTreeSample ? p.n_units : p.B) * p.Sr : 0;
     // ring depth: the deepest ring that keeps kMinCtas CTAs on an SM
-    const size_t scratch = (MODE == kTreeGreedy) ? static_cast<size_t>(kWarps) * 3 * p.units_per_seq * 4 : 0;
+    const size_t scratch =
+        (MODE == kTreeGreedy || MODE == kTreeSample) ? static_cast<size_t>(kWarps) * 3 * p.units_per_seq * 4 : 0;
     int ns = 0, per_sm = 0;
     size_t dyn = 0;
     for (int cand : {SPEC_MAX_STAGES, 2}) {
@@ -277,6 +284,11 @@ extern "C" size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype) {
 extern "C" size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype) {
     if (B <= 0 || N < 1 || V < 1 || !valid_dtype(dtype)) return 0;
     return layout_tree(B, N, V, elt_bytes(dtype)).total;
+}
+
+extern "C" size_t spec_workspace_bytes_tree_sample(int B, int N, int V, spec_dtype dtype) {
+    if (B <= 0 || N < 1 || V < 1 || !valid_dtype(dtype)) return 0;
+    return layout_tree_sample(B, N, V, elt_bytes(dtype)).total;
 }
 
 extern "C" spec_status spec_verify_linear(const void *target_logits, const void *draft_logits,
@@ -420,6 +432,52 @@ extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dt
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the warp that finishes a sequence stages parents, node tokens and argmaxes (3 * N ints)
     return eb == 4 ? launch<4, kTreeGreedy>(p, false, s) : launch<2, kTreeGreedy>(p, false, s);
+}
+
+extern "C" spec_status spec_verify_tree_sample(const void *target_logits, spec_dtype dtype, int B, int N, int V,
+                                               const int32_t *parents, const int32_t *node_tokens,
+                                               const float *u_nodes, float temperature, int max_depth,
+                                               int32_t *path_nodes, int32_t *path_len, int32_t *out_tokens,
+                                               uint32_t *dev_status, void *workspace, size_t workspace_bytes,
+                                               void *stream) {
+    g_last_error[0] = '\0';
+    if (!valid_dtype(dtype)) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (B < 0 || N < 1 || V < 1 || max_depth < 0)
+        return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, N >= 1, V >= 1, max_depth >= 0");
+    float c = 0.f;
+    if (!valid_temperature(temperature, &c) || !(temperature > 0.0f))
+        return fail(SPEC_ERR_INVALID_ARG, "temperature must be finite and > 0");
+    if (B == 0) return SPEC_OK;
+    const int eb = elt_bytes(dtype);
+    if (!target_logits || !aligned(target_logits, eb)) return fail(SPEC_ERR_INVALID_ARG, "target_logits null or misaligned");
+    if (!parents || !node_tokens || !u_nodes || !path_nodes || !path_len || !out_tokens || !dev_status)
+        return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
+    if (static_cast<long long>(B) * N > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B * N too large");
+    const WsLayout wl = layout_tree_sample(B, N, V, eb);
+    if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
+        return fail(SPEC_ERR_WORKSPACE, "workspace needs %zu bytes, 16-byte aligned", wl.total);
+    Params p = {};
+    p.target = static_cast<const unsigned char *>(target_logits);
+    p.t_end = p.target + static_cast<size_t>(B) * N * static_cast<size_t>(V) * eb;
+    p.B = B;
+    p.K = N;
+    p.V = V;
+    p.t_rows = N;
+    p.units_per_seq = N;
+    p.rows_per_seq = N;
+    p.n_units = B * N;
+    p.c = c;
+    p.tokens = node_tokens;
+    p.u_bonus = u_nodes;  // one uniform per node: the draw of unit b * N + n
+    p.parents = parents;
+    p.max_depth = max_depth;
+    p.accept_len = path_len;
+    p.out_tokens = out_tokens;
+    p.path_nodes = path_nodes;
+    p.status = dev_status;
+    bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return eb == 4 ? launch<4, kTreeSample>(p, true, s) : launch<2, kTreeSample>(p, true, s);
 }
 
 // ---- spec_verify_linear_static: spec_verify_linear on a workspace compiled

@@ -103,6 +103,7 @@ enum Mode : int {
     kTreeGreedy = 2,
     kBonusSample = 3,
     kBonusGreedy = 4,
+    kTreeSample = 5,  // tree walk with the target's choice drawn at every node
 };
 
 enum TileKind : int { kTileNone = 0, kTileStats = 1, kTileResid = 2 };
@@ -619,7 +620,7 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
 // ---------------------------------------------------------- unit layout
 template <int MODE>
 struct Traits {
-    static constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample);
+    static constexpr bool kSample = (MODE == kLinearSample || MODE == kBonusSample || MODE == kTreeSample);
     static constexpr bool kBonus = (MODE == kBonusSample || MODE == kBonusGreedy);
 };
 
@@ -639,7 +640,7 @@ __device__ __forceinline__ int bonus_pos(const Params &p, int b) {
 // Rows of the unit at position pos (-1: an invalid length, one unused row).
 template <int MODE>
 __device__ __forceinline__ int unit_nrows(const Params &p, int pos) {
-    return (Traits<MODE>::kSample && pos >= 0 && pos < p.K) ? 2 : 1;
+    return (Traits<MODE>::kSample && MODE != kTreeSample && pos >= 0 && pos < p.K) ? 2 : 1;
 }
 
 // Row slot rs of a sequence in the stats tiling: its position, its row within
@@ -667,7 +668,7 @@ template <int MODE>
 __device__ __forceinline__ int row_id_of(const Params &p, int b, int pos, int r) {
     if (MODE == kLinearSample) return (pos < p.K) ? (pos * p.B + b) * 2 + r : 2 * p.K * p.B + b;
     if (MODE == kLinearGreedy) return pos * p.B + b;
-    if (MODE == kTreeGreedy) return b * p.rows_per_seq + pos;
+    if (MODE == kTreeGreedy || MODE == kTreeSample) return b * p.rows_per_seq + pos;
     if (MODE == kBonusSample) return b * 2 + r;
     return b;  // kBonusGreedy
 }
@@ -1336,7 +1337,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             if (fl) atomicOr(p.status, fl);
         }
         __syncwarp();
-        if (T::kBonus) {
+        if (T::kBonus || MODE == kTreeSample) {  // every unit draws: publish its entry
             if (T::kSample) push_entry(u, nrows == 2, pos < 0 || !finite);
             return;
         }
@@ -1551,7 +1552,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         int token = 0;
         if (!skip) {
             const float4 js = mine ? r_js : __ldcg(&p.ws_stats[u]);
-            const float ub = __ldg(&p.u_bonus[b]);
+            const float ub = __ldg(&p.u_bonus[MODE == kTreeSample ? u : b]);  // per node, or per sequence
             token = select_token(e, b, pos, pair, js, ub);
             if (token < 0 && pair) {
                 // the residual vanished through rounding: draw from p_j instead
@@ -1561,8 +1562,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             }
             if (token < 0) token = 0;
         }
+        int walk = 0;  // sampled tree: this was the sequence's last draw
         if (T::kBonus) {
             if (lane == 0) p.bonus_token[b] = (pos < 0) ? -1 : token;
+        } else if (MODE == kTreeSample) {
+            if (lane == 0) {
+                p.ws_val[u] = token;  // the target's choice at node pos
+                walk = (atom_add_acq_rel(&p.ws_seq_cnt[b], 1u) == static_cast<unsigned>(p.units_per_seq - 1)) ? 1 : 0;
+            }
+            walk = __shfl_sync(kFull, walk, 0);
         } else {
             emit_linear(b, pos, token, true);
         }
@@ -1575,6 +1583,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             p.ws_res_cnt[static_cast<size_t>(e) * kEntWords] = 0u;
         }
         __syncwarp();
+        if (MODE == kTreeSample && walk) {  // every node of sequence b is drawn
+            emit_tree(b);
+            if (lane == 0) p.ws_seq_cnt[b] = 0u;
+            __syncwarp();
+        }
     };
 
     // consume the pending counter increment

@@ -122,6 +122,26 @@ def test_bonus_and_tree_host_validation(lib):
     assert t(FAKE, 0, 0, 5, 10, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_OK
 
 
+def test_tree_sample_host_validation(lib):
+    t = lib.spec_verify_tree_sample
+    W = 1 << 20
+
+    def call(B=2, N=5, V=10, u=FAKE, T=1.0, D=3, ws=FAKE, wsb=W):
+        return t(FAKE, 0, B, N, V, FAKE, FAKE, u, T, D, FAKE, FAKE, FAKE, FAKE, ws, wsb, None)
+    assert call(T=0.0) == sv.SPEC_ERR_INVALID_ARG          # sampling needs T > 0
+    assert call(T=float("nan")) == sv.SPEC_ERR_INVALID_ARG
+    assert call(u=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(N=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(D=-1) == sv.SPEC_ERR_INVALID_ARG
+    assert call(ws=None) == sv.SPEC_ERR_WORKSPACE
+    need = sv.spec_workspace_bytes_tree_sample(2, 5, 10, sv.SPEC_F32)
+    assert call(wsb=need - 16) == sv.SPEC_ERR_WORKSPACE
+    assert call(B=0) == sv.SPEC_OK
+    # one draw entry and its chunk sums per node: more than the greedy walk needs
+    assert need > sv.spec_workspace_bytes_tree(2, 5, 10, sv.SPEC_F32)
+    assert sv.spec_workspace_bytes_tree_sample(0, 5, 10, sv.SPEC_F32) == 0
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     t = torch.zeros((1, 2, 8))

@@ -258,6 +258,92 @@ def test_chain_tree_equals_linear_greedy_on_gpu():
     assert torch.equal(tr["out_tokens"], lin["out_tokens"])
 
 
+# ------------------------------------------------------- sampled trees
+
+def _draws(target, T, u):
+    """Each node's draw from softmax(target / T) at uniform u (float64, on the host): used
+    only to build node tokens that make the walks long."""
+    x = target.float().cpu().double().numpy() / T
+    p = np.exp(x - x.max(-1, keepdims=True))
+    c = np.cumsum(p, -1)
+    want = u.cpu().double().numpy()[..., None] * c[..., -1:]
+    return np.minimum((c <= want).sum(-1), x.shape[-1] - 1)
+
+
+def _sampled_tree_inputs(t, parents, T, seed, hit=0.75):
+    B, N, V = t.shape
+    rng = np.random.default_rng(seed)
+    u = torch.from_numpy(rng.random((B, N)).astype(np.float32)).cuda()
+    dr = _draws(t, T, u)
+    par = parents.cpu().numpy()
+    children = [[c for c in range(N) if par[c] == n] for n in range(N)]
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for n in range(N):
+            ch = children[n]
+            if not ch:
+                continue
+            pool = [int(v) for v in rng.permutation(V)[:len(ch) + 1] if v != dr[b, n]]
+            if rng.random() < hit:
+                pool.insert(int(rng.integers(0, len(ch))), int(dr[b, n]))
+            for c, tok in zip(ch, pool):
+                tokens[b, c] = tok
+    return u, torch.from_numpy(tokens).cuda()
+
+
+def _tree_sample_parity(t, par, tok, u, T, depth):
+    r = sv.spec_verify_tree_sample(t, par, tok, u, T, depth)
+    torch.cuda.synchronize()
+    o = oracle.verify_tree_sample(to_oracle(t), to_oracle(par), to_oracle(tok), to_oracle(u), T, depth)
+    rep = compare.compare_tree_sample({k: v.cpu().numpy() for k, v in r.items()}, o, to_oracle(u))
+    print(rep.summary())
+    assert rep.ok, rep.failures[:5]
+    assert int(r["status"].item()) == 0
+    return r, o
+
+
+def test_medusa_tree_workload_sampled_full_size():
+    """The Medusa tree workload's shapes (B=16, 64 nodes, V=32000 fp32) with the choice drawn at T = 1."""
+    d = make_tree(4, device="cuda")
+    u, tok = _sampled_tree_inputs(d["target"], d["parents"], 1.0, seed=404)
+    r, o = _tree_sample_parity(d["target"], d["parents"], tok, u, 1.0, d["max_depth"])
+    assert o["path_len"].max() >= 2   # the walks go below the root
+
+
+@pytest.mark.parametrize("B,N,V,dtype,depth,T", [(8, 1, 1000, "f32", 3, 1.0), (12, 30, 5003, "bf16", 6, 0.7),
+                                                 (6, 100, 2048, "f32", 4, 1.5), (4, 20, 777, "f32", 0, 0.9),
+                                                 (3, 9, 7, "bf16", 5, 2.0)])
+def test_tree_sample_parity(B, N, V, dtype, depth, T):
+    t, par, _ = _random_tree_inputs(B, N, V, dtype, seed=N + V + 1)
+    u, tok = _sampled_tree_inputs(t, par, T, seed=N * V)
+    _tree_sample_parity(t, par, tok, u, T, depth)
+
+
+def test_tree_sample_with_dominant_logits_equals_greedy_walk():
+    t, par, tok = _random_tree_inputs(10, 25, 3000, "f32", seed=99)
+    am = torch.argmax(t, dim=-1, keepdim=True)
+    t = t.scatter(-1, am, 90.0).contiguous()     # every draw is the argmax
+    u = torch.rand((10, 25), device="cuda")
+    g = sv.spec_verify_tree(t, par, tok, 5)
+    s = sv.spec_verify_tree_sample(t, par, tok, u, 1.0, 5)
+    torch.cuda.synchronize()
+    for k in ("path_len", "path_nodes", "out_tokens"):
+        assert torch.equal(g[k], s[k]), k
+
+
+def test_tree_sample_workspace_left_zeroed_and_repeatable():
+    t, par, _ = _random_tree_inputs(5, 12, 4099, "bf16", seed=5)
+    u, tok = _sampled_tree_inputs(t, par, 0.8, seed=6)
+    nbytes = sv.spec_workspace_bytes_tree_sample(5, 12, 4099, t.dtype)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    a = sv.spec_verify_tree_sample(t, par, tok, u, 0.8, 4, workspace=ws)
+    b = sv.spec_verify_tree_sample(t, par, tok, u, 0.8, 4, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero().item()) == 0
+    for k in ("path_len", "path_nodes", "out_tokens"):
+        assert torch.equal(a[k], b[k]), k
+
+
 # -------------------------------------------------------------- status bits
 
 def test_bad_token_is_flagged_and_rejected():
