@@ -17,6 +17,12 @@ own independent batch (no collective on the data path; weak scaling).
 
 --impl reference times the float64 CPU oracle on this machine's host cores on the
 same workload (rank 0 only).
+
+--workload NAME (one GPU) times another configuration instead, one JSON line
+each: the kernel alone, calls replayed from a CUDA graph over rotating input
+copies, with the oracle timed beside it on a bounded sample.  NAME is one of
+small, small_greedy, mtp_greedy, mtp_sample, medusa_tree, medusa_tree_sample,
+stress, or all.
 """
 from __future__ import annotations
 
@@ -49,6 +55,8 @@ def parse():
                     help="untimed same-kernel loop before the timed region, so clock samples see the load")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="draft_target",
+                    help="draft_target (the headline), or another configuration: " + ", ".join(EXTRA) + ", all")
     return ap.parse_args()
 
 
@@ -353,8 +361,173 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------ other configurations
+# name: (workload number, temperature, kind)
+EXTRA = {
+    "small": (1, 1.0, "linear"),
+    "small_greedy": (1, 0.0, "linear"),
+    "mtp_greedy": (3, 0.0, "linear"),
+    "mtp_sample": (3, 1.0, "linear"),
+    "medusa_tree": (4, 0.0, "tree"),
+    "medusa_tree_sample": (4, 1.0, "tree_sample"),
+    "stress": (5, 0.7, "linear"),
+}
+
+
+def _extra_inputs(name, dev):
+    """Device inputs of one configuration (with a uniform per node for the sampled tree)."""
+    import numpy as np
+    import torch
+    from workloads import WORKLOADS, make_linear, make_tree
+    number, T, kind = EXTRA[name]
+    w = WORKLOADS[number]
+    if kind == "linear":
+        return w, T, kind, make_linear(number, T, device=dev)
+    d = make_tree(number, device=dev)
+    B, N = d["node_tokens"].shape
+    if kind == "tree_sample":
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed + 17)
+        d["u_nodes"] = torch.rand((B, N), generator=g, device=dev, dtype=torch.float32)
+        # the node tokens of the greedy workload name argmaxes; here a child carries the node's draw instead
+        x = d["target"].float().double() / T
+        p = torch.exp(x - x.amax(-1, keepdim=True))
+        c = torch.cumsum(p, -1)
+        draws = torch.clamp((c <= d["u_nodes"].double()[..., None] * c[..., -1:]).sum(-1), max=w.V - 1).cpu().numpy()
+        am = torch.argmax(d["target"].float(), dim=-1).cpu().numpy()
+        tok = d["node_tokens"].cpu().numpy()
+        par = d["parents"].cpu().numpy()
+        for b in range(B):
+            for c_ in range(1, N):
+                if tok[b, c_] == am[b, par[c_]]:
+                    tok[b, c_] = draws[b, par[c_]]
+        d["node_tokens"] = torch.from_numpy(np.ascontiguousarray(tok)).to(dev)
+    return w, T, kind, d
+
+
+def run_extra(args, name):
+    """One configuration, the kernel alone, replayed from a CUDA graph; plus the oracle beside it."""
+    import torch
+
+    import sampling_online_softmax_gb300 as sv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w, T, kind, d = _extra_inputs(name, dev)
+    bytes_per_step = w.logits_bytes(T)
+    rotate = max(1, min(4, int(2 * 129e6 // bytes_per_step) + 1))       # more than L2 over the copies
+    keys = ("target", "draft") if kind == "linear" else ("target",)
+    copies = [d] + [dict(d, **{k: d[k].clone() for k in keys if d.get(k) is not None}) for _ in range(rotate - 1)]
+    B = w.B
+    stream = torch.cuda.Stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def make_call(c):
+        if kind == "linear":
+            K = w.K
+            out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                       out_tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                       num_emitted=torch.empty(B, dtype=torch.int32, device=dev))
+            ws = torch.zeros(sv.spec_workspace_bytes_linear(B, K, w.V, c["target"].dtype), dtype=torch.uint8,
+                             device=dev)
+            return lambda: sv.spec_verify_linear(c["target"], c["draft"] if T > 0 else None, c["draft_tokens"],
+                                                 c["u_accept"], c["u_bonus"], T, out=out, status=status, workspace=ws,
+                                                 stream=stream)
+        N = c["node_tokens"].shape[1]
+        D = int(c["max_depth"])
+        out = dict(path_nodes=torch.empty((B, D + 1), dtype=torch.int32, device=dev),
+                   path_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, D + 1), dtype=torch.int32, device=dev))
+        if kind == "tree":
+            ws = torch.zeros(sv.spec_workspace_bytes_tree(B, N, w.V, c["target"].dtype), dtype=torch.uint8,
+                             device=dev)
+            return lambda: sv.spec_verify_tree(c["target"], c["parents"], c["node_tokens"], D, out=out,
+                                               status=status, workspace=ws, stream=stream)
+        ws = torch.zeros(sv.spec_workspace_bytes_tree_sample(B, N, w.V, c["target"].dtype), dtype=torch.uint8,
+                         device=dev)
+        return lambda: sv.spec_verify_tree_sample(c["target"], c["parents"], c["node_tokens"], c["u_nodes"], T, D,
+                                                  out=out, status=status, workspace=ws, stream=stream)
+
+    calls = [make_call(c) for c in copies]
+    with torch.cuda.stream(stream):
+        for k in range(max(args.warmup, 3) * rotate):  # first calls set the library's per-device state
+            calls[k % rotate]()
+    torch.cuda.synchronize()
+    per_graph = 8 * rotate
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(per_graph):
+            calls[k % rotate]()
+    torch.cuda.synchronize()
+    # a graph replays on the current stream: time it there
+    with torch.cuda.stream(stream):
+        est0, est1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        est0.record(stream)
+        graph.replay()
+        est1.record(stream)
+        torch.cuda.synchronize()
+        per_call = est0.elapsed_time(est1) / 1e3 / per_graph
+        reps = max(2, int(min(2.0, args.steps * per_call) / (per_call * per_graph)))
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    step_s = t0.elapsed_time(t1) / 1e3 / (reps * per_graph)
+    assert step_s > 1e-6, "the graph replay timed no work"
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+    peak, peak_kind = measured_peak()
+    gbps = bytes_per_step / step_s / 1e9
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        cores = len(os.sched_getaffinity(0))
+        oracle.threads(cores)
+        h = {k: to_oracle(v) for k, v in d.items() if hasattr(v, "detach")}
+        if kind == "linear":
+            f = lambda: oracle.verify_linear(h["target"], h["draft"] if T > 0 else None, h["draft_tokens"],  # noqa
+                                             h["u_accept"], h["u_bonus"], T)
+        elif kind == "tree":
+            f = lambda: oracle.verify_tree(h["target"], h["parents"], h["node_tokens"], int(d["max_depth"]))  # noqa
+        else:
+            f = lambda: oracle.verify_tree_sample(h["target"], h["parents"], h["node_tokens"], h["u_nodes"],  # noqa
+                                                  T, int(d["max_depth"]))
+        n, c0 = 0, time.perf_counter()
+        while True:
+            f()
+            n += 1
+            el = time.perf_counter() - c0
+            if el >= min(args.cpu_seconds, 20.0):
+                break
+        cpu = {"value": B * n / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+               "sample": "the full %d-sequence batch, %d repetitions in %.1f s" % (B, n, el)}
+
+    cfg = {"workload": name, "number": w.number, "kind": kind, "B": B, "K": w.K, "V": w.V,
+           "logits_dtype": w.dtype, "temperature": T, "logits_bytes_per_step": bytes_per_step,
+           "l2": "inputs rotate over %d copies (%.0f MB %s the 129 MB L2)"
+                 % (rotate, rotate * bytes_per_step / 1e6, ">" if rotate * bytes_per_step > 129e6 else "<"),
+           "seed": w.seed}
+    if kind != "linear":
+        cfg["N"] = int(d["node_tokens"].shape[1])
+    line = {"metric": METRIC, "value": B / step_s, "unit": "seqs/s", "n_gpus": 1, "ms_per_step": 1e3 * step_s,
+            "higher_is_better": True, "timing": "kernel alone, %d calls per CUDA graph replay, %d replays"
+            % (per_graph, reps), "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "achieved": gbps, "peak": peak, "unit": "GB/s", "frac": gbps / peak,
+                         "peak_kind": peak_kind},
+            "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload != "draft_target":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "--workload times the oracle beside our arm"}))
+            return
+        for name in (list(EXTRA) if args.workload == "all" else [args.workload]):
+            run_extra(args, name)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
