@@ -64,6 +64,8 @@ def _declare(lib):
     lib.oracle_verify_tree_sample.argtypes = [P, i32, i32, i32, i32, P, P, P, ctypes.c_float, i32,
                                               P, P, P, P]
     lib.oracle_verify_tree_sample.restype = i32
+    lib.oracle_sample_rows.argtypes = [P, i32, i32, i32, P, ctypes.c_float, P, P]
+    lib.oracle_sample_rows.restype = i32
     lib.oracle_threads.argtypes = [i32]
     lib.oracle_threads.restype = i32
     return lib
@@ -188,4 +190,21 @@ def verify_tree_sample(target, parents, node_tokens, u_nodes, temperature, max_d
                                        _ptr(out["path_len"]), _ptr(out["out_tokens"]), _ptr(out["node_cdf"]))
     if rc != 0:
         raise ValueError("oracle_verify_tree_sample rejected its arguments")
+    return out
+
+
+def sample_rows(logits, u, temperature, lib=None):
+    """One token per row of logits [B, V]: a draw from softmax(l / T) at u [B], or argmax when T == 0.
+    Returns dict(tokens [B], cdf [B, 2])."""
+    lib = lib or load()
+    logits, dt = _logits(logits)
+    B, V = logits.shape
+    uu = None if u is None else np.ascontiguousarray(u, dtype=np.float32).reshape(B)
+    if temperature > 0 and uu is None:
+        raise ValueError("sampling needs u")
+    out = dict(tokens=np.zeros(B, np.int32), cdf=np.zeros((B, 2), np.float64))
+    rc = lib.oracle_sample_rows(_ptr(logits), dt, B, V, _ptr(uu) if uu is not None else None, float(temperature),
+                                _ptr(out["tokens"]), _ptr(out["cdf"]))
+    if rc != 0:
+        raise ValueError("oracle_sample_rows rejected its arguments")
     return out

@@ -43,6 +43,9 @@
  *     take the first whose token equals argmax of the current node's target
  *     row; stop when none matches or max_depth nodes were accepted; the extra
  *     token is argmax at the last accepted node.
+ *   - one token per row (the draft side's own choice of its next token, or
+ *     any row a caller wants sampled): a draw from softmax(l / T) by inverse
+ *     CDF with the row's uniform, or argmax (lowest index) when T == 0.
  *   - tree, sampling mode (the page's "Greedy或者Sampling"): the target's
  *     choice at node n is a draw from softmax(target_n / T) by inverse CDF
  *     with the caller's uniform u[b, n]; the walk is the greedy walk with that
@@ -394,6 +397,35 @@ int oracle_verify_tree_sample(const void *target, int dtype, int B, int N, int V
         ot[depth] = draw[cur];
         free(p);
         free(draw);
+    }
+    return 0;
+}
+
+/*
+ * One token per row: logits [B, V]; u [B] (ignored when T == 0).
+ *   T > 0: inverse_cdf(softmax(row / T), u[b]); T == 0: argmax, lowest index.
+ * Outputs: tokens [B]; cdf [B, 2] (the draw's normalised cumulative interval;
+ * zeros when greedy) or NULL.
+ */
+int oracle_sample_rows(const void *logits, int dtype, int B, int V, const float *u, float temperature,
+                       int32_t *tokens, double *cdf) {
+    if (B < 0 || V < 1 || !(temperature >= 0.0f)) return 1;
+    const double T = (double)temperature;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int b = 0; b < B; ++b) {
+        double lo = 0.0, hi = 0.0;
+        if (temperature == 0.0f) {
+            tokens[b] = argmax_row(logits, dtype, (size_t)b, V);
+        } else {
+            double *p = (double *)malloc(sizeof(double) * (size_t)V);
+            softmax_row(logits, dtype, (size_t)b, V, T, p, NULL, NULL);
+            tokens[b] = inverse_cdf(p, V, (double)u[b], &lo, &hi);
+            free(p);
+        }
+        if (cdf) {
+            cdf[(size_t)b * 2 + 0] = lo;
+            cdf[(size_t)b * 2 + 1] = hi;
+        }
     }
     return 0;
 }

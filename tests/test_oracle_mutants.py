@@ -16,6 +16,7 @@ import pytest
 import oracle
 import test_oracle_pins as pins
 import test_tree_pins as tpins
+import test_row_sampler_pins as rpins
 import test_tree_sample_pins as spins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
@@ -50,6 +51,12 @@ MUTANTS = [
      "node_tokens[(size_t)b * N + c] == draw[0]"),
     ("tree_sample_extra_is_argmax", "ot[depth] = draw[cur];",
      "ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);"),
+    ("rows_temperature_dropped", "softmax_row(logits, dtype, (size_t)b, V, T, p, NULL, NULL);",
+     "softmax_row(logits, dtype, (size_t)b, V, 1.0, p, NULL, NULL);"),
+    ("rows_uniform_of_row_zero", "tokens[b] = inverse_cdf(p, V, (double)u[b], &lo, &hi);",
+     "tokens[b] = inverse_cdf(p, V, (double)u[0], &lo, &hi);"),
+    ("rows_greedy_from_row_zero", "tokens[b] = argmax_row(logits, dtype, (size_t)b, V);",
+     "tokens[b] = argmax_row(logits, dtype, (size_t)0, V);"),
     ("tree_sample_row_of_root", "softmax_row(target, dtype, (size_t)b * N + n, V, T, p, NULL, NULL);",
      "softmax_row(target, dtype, (size_t)b * N, V, T, p, NULL, NULL);"),
 ]
@@ -71,6 +78,9 @@ def _pin_suite(lib):
         ("tree_sample_freq", lambda: spins.check_draw_frequencies(lib, V=4, T=0.5, M=4000)),
         ("tree_sample_walk", lambda: spins.check_walk_brute_force(lib)),
         ("tree_sample_greedy", lambda: spins.check_dominant_logit_is_greedy(lib)),
+        ("rows_freq", lambda: rpins.check_frequencies(lib, V=5, T=0.7, M=5000)),
+        ("rows_greedy", lambda: rpins.check_greedy_is_argmax(lib)),
+        ("rows_scaling", lambda: rpins.check_temperature_scaling(lib)),
     ]
     for name, fn in checks:
         try:
