@@ -87,6 +87,9 @@ size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype);
 /* Bytes of workspace spec_sample_bonus needs for B sequences. */
 size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype);
 
+/* Bytes of workspace spec_sample_rows needs for B rows of V logits. */
+size_t spec_workspace_bytes_rows(int B, int V, spec_dtype dtype);
+
 /* Bytes of workspace spec_verify_tree needs for B sequences of N tree nodes. */
 size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype);
 
@@ -140,6 +143,22 @@ spec_status spec_sample_bonus(const void *target_logits, const void *draft_logit
                               const int32_t *accept_len, const float *u_bonus, float temperature,
                               int32_t *bonus_token, uint32_t *dev_status,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One token per row: the draft side's choice of its next draft token (the
+ * draft proposes tokens drawn from its own distribution q in the cited
+ * speculative-sampling method), or any row a caller wants sampled.
+ *   logits [B, V] (device, row-major, fp32 or bf16), u [B] fp32 in [0, 1)
+ *   (ignored, may be NULL, when temperature == 0), temperature T >= 0.
+ *   tokens [B] int32 (device, output): the first v whose cumulative weight of
+ *   softmax(l / T) exceeds u[b] * W (exact int64 sums, as in the extra token),
+ *   or the lowest-index argmax when T == 0.
+ *   workspace, workspace_bytes: spec_workspace_bytes_rows(B, V, dtype) bytes.
+ * It runs the extra-token path with no draft (K = 0).
+ */
+spec_status spec_sample_rows(const void *logits, spec_dtype dtype, int B, int V, const float *u, float temperature,
+                             int32_t *tokens, uint32_t *dev_status, void *workspace, size_t workspace_bytes,
+                             void *stream);
 
 /*
  * Greedy verify of a candidate tree ("Speculative-Decoding / Medusa" blog,

@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
                        ("Speculative-Decoding / Medusa", section 三)
   spec_verify_tree_sample  the same walk with the target's choice drawn at
                        every node (the section's sampled variant)
+  spec_sample_rows     one token per row (the draft side's next token)
 """
 from __future__ import annotations
 
@@ -73,6 +74,10 @@ def load_library():
         lib.spec_workspace_bytes_tree.argtypes = [i32, i32, i32, i32]
         lib.spec_workspace_bytes_tree.restype = u64
         lib.spec_workspace_bytes_tree_sample.argtypes = [i32, i32, i32, i32]
+        lib.spec_workspace_bytes_rows.argtypes = [i32, i32, i32]
+        lib.spec_workspace_bytes_rows.restype = u64
+        lib.spec_sample_rows.argtypes = [P, i32, i32, i32, P, f32, P, P, P, u64, P]
+        lib.spec_sample_rows.restype = i32
         lib.spec_workspace_bytes_tree_sample.restype = u64
         lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
         lib.spec_verify_linear.restype = i32
@@ -166,6 +171,10 @@ def spec_workspace_bytes_bonus(B: int, V: int, dtype) -> int:
 
 def spec_workspace_bytes_tree(B: int, N: int, V: int, dtype) -> int:
     return int(load_library().spec_workspace_bytes_tree(int(B), int(N), int(V), _dtype_arg(dtype)))
+
+
+def spec_workspace_bytes_rows(B: int, V: int, dtype) -> int:
+    return int(load_library().spec_workspace_bytes_rows(int(B), int(V), _dtype_arg(dtype)))
 
 
 def spec_workspace_bytes_tree_sample(B: int, N: int, V: int, dtype) -> int:
@@ -339,5 +348,29 @@ def spec_verify_tree_sample(target, parents, node_tokens, u_nodes, temperature, 
                                          _ptr(node_tokens), _ptr(u_nodes), float(temperature), D,
                                          _ptr(out["path_nodes"]), _ptr(out["path_len"]), _ptr(out["out_tokens"]),
                                          _ptr(status), _ptr(ws), ws.numel(), h)
+    _check(st)
+    return out
+
+
+def spec_sample_rows(logits, u, temperature, *, status=None, out=None, workspace=None, stream=None):
+    """One token per row of logits [B, V]: a draw from softmax(l / T) at u [B] (float32), or the
+    argmax when temperature == 0 (u may be None); returns dict(tokens [B], status)."""
+    lib = load_library()
+    _cuda(logits, "logits")
+    B, V = logits.shape
+    dev = logits.device
+    _cuda(u, "u", torch.float32)
+    h, s = _stream_handle(dev, stream)
+    if out is None:
+        out = dict(tokens=torch.empty(B, dtype=torch.int32, device=dev))
+    if status is None:
+        with torch.cuda.stream(s):
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out["status"] = status
+    nbytes = spec_workspace_bytes_rows(B, V, logits.dtype)
+    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    with torch.cuda.device(dev):
+        st = lib.spec_sample_rows(_ptr(logits), _dtype_code(logits), B, V, _ptr(u), float(temperature),
+                                  _ptr(out["tokens"]), _ptr(status), _ptr(ws), ws.numel(), h)
     _check(st)
     return out

@@ -286,6 +286,11 @@ extern "C" size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtyp
     return layout_tree(B, N, V, elt_bytes(dtype)).total;
 }
 
+extern "C" size_t spec_workspace_bytes_rows(int B, int V, spec_dtype dtype) {
+    if (B <= 0 || V < 1 || !valid_dtype(dtype)) return 0;
+    return layout_bonus(B, V, elt_bytes(dtype)).total;
+}
+
 extern "C" size_t spec_workspace_bytes_tree_sample(int B, int N, int V, spec_dtype dtype) {
     if (B <= 0 || N < 1 || V < 1 || !valid_dtype(dtype)) return 0;
     return layout_tree_sample(B, N, V, elt_bytes(dtype)).total;
@@ -348,11 +353,11 @@ extern "C" spec_status spec_verify_linear(const void *target_logits, const void 
     return eb == 4 ? launch<4, kLinearGreedy>(p, false, s) : launch<2, kLinearGreedy>(p, false, s);
 }
 
-extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits, spec_dtype dtype,
-                                         int B, int K, int V, const int32_t *accept_len, const float *u_bonus,
-                                         float temperature, int32_t *bonus_token, uint32_t *dev_status,
-                                         void *workspace, size_t workspace_bytes, void *stream) {
-    g_last_error[0] = '\0';
+// The extra token alone; accept_len == nullptr draws every sequence at position K.
+static spec_status sample_extra(const void *target_logits, const void *draft_logits, spec_dtype dtype, int B, int K,
+                                int V, const int32_t *accept_len, const float *u_bonus, float temperature,
+                                int32_t *bonus_token, uint32_t *dev_status, void *workspace, size_t workspace_bytes,
+                                void *stream) {
     if (!valid_dtype(dtype)) return fail(SPEC_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
     if (B < 0 || K < 0 || V < 1) return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, K >= 0, V >= 1");
     float c = 0.f;
@@ -364,7 +369,7 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     if (sample && K > 0 && (!draft_logits || !aligned(draft_logits, eb)))
         return fail(SPEC_ERR_INVALID_ARG, "draft_logits null or misaligned");
     if (sample && !u_bonus) return fail(SPEC_ERR_INVALID_ARG, "u_bonus is null");
-    if (!accept_len || !bonus_token || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
+    if (!bonus_token || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
     if (B > INT_MAX / 64) return fail(SPEC_ERR_UNSUPPORTED, "B too large");
     const WsLayout wl = layout_bonus(B, V, eb);
     if (!workspace || workspace_bytes < wl.total || !aligned(workspace, 16))
@@ -380,7 +385,7 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     p.V = V;
     p.t_rows = K + 1;
     p.units_per_seq = 1;
-    p.rows_per_seq = sample ? 2 : 1;
+    p.rows_per_seq = (sample && K > 0) ? 2 : 1;  // the draft row slot exists only with a draft
     p.n_units = B;
     p.c = c;
     p.u_bonus = u_bonus;
@@ -391,6 +396,25 @@ extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (sample) return eb == 4 ? launch<4, kBonusSample>(p, true, s) : launch<2, kBonusSample>(p, true, s);
     return eb == 4 ? launch<4, kBonusGreedy>(p, false, s) : launch<2, kBonusGreedy>(p, false, s);
+}
+
+extern "C" spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits, spec_dtype dtype,
+                                         int B, int K, int V, const int32_t *accept_len, const float *u_bonus,
+                                         float temperature, int32_t *bonus_token, uint32_t *dev_status,
+                                         void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    if (!accept_len && B > 0) return fail(SPEC_ERR_INVALID_ARG, "accept_len is null");
+    return sample_extra(target_logits, draft_logits, dtype, B, K, V, accept_len, u_bonus, temperature, bonus_token,
+                        dev_status, workspace, workspace_bytes, stream);
+}
+
+extern "C" spec_status spec_sample_rows(const void *logits, spec_dtype dtype, int B, int V, const float *u,
+                                        float temperature, int32_t *tokens, uint32_t *dev_status, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    // a row per sequence is the target tail of a zero-length draft: K = 0, no draft, no lengths
+    return sample_extra(logits, nullptr, dtype, B, 0, V, nullptr, u, temperature, tokens, dev_status, workspace,
+                        workspace_bytes, stream);
 }
 
 extern "C" spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B, int N, int V,

@@ -632,7 +632,9 @@ __device__ __forceinline__ const unsigned char *row_ptr(const Params &p, int b, 
 }
 
 // Position of sequence b's unit in the extra-token-alone modes; -1 if invalid.
+// Without lengths every sequence draws at position K (one row per sequence).
 __device__ __forceinline__ int bonus_pos(const Params &p, int b) {
+    if (p.accept_len_in == nullptr) return p.K;
     const int j = __ldg(&p.accept_len_in[b]);
     return (j < 0 || j > p.K) ? -1 : j;
 }
@@ -669,7 +671,7 @@ __device__ __forceinline__ int row_id_of(const Params &p, int b, int pos, int r)
     if (MODE == kLinearSample) return (pos < p.K) ? (pos * p.B + b) * 2 + r : 2 * p.K * p.B + b;
     if (MODE == kLinearGreedy) return pos * p.B + b;
     if (MODE == kTreeGreedy || MODE == kTreeSample) return b * p.rows_per_seq + pos;
-    if (MODE == kBonusSample) return b * 2 + r;
+    if (MODE == kBonusSample) return b * p.rows_per_seq + r;  // rows_per_seq is 1 when K == 0
     return b;  // kBonusGreedy
 }
 

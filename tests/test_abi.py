@@ -122,6 +122,23 @@ def test_bonus_and_tree_host_validation(lib):
     assert t(FAKE, 0, 0, 5, 10, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == sv.SPEC_OK
 
 
+def test_sample_rows_host_validation(lib):
+    f = lib.spec_sample_rows
+    W = 1 << 20
+    assert f(FAKE, 1, -1, 10, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, 1, 4, 0, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, 1, 4, 10, None, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG   # sampling needs u
+    assert f(FAKE, 1, 4, 10, FAKE, -1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, 1, 4, 10, FAKE, 1.0, None, FAKE, FAKE, W, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, 1, 4, 10, None, 0.0, FAKE, FAKE, None, W, None) == sv.SPEC_ERR_WORKSPACE  # greedy: no u
+    assert f(FAKE, 1, 0, 10, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == sv.SPEC_OK
+    assert sv.spec_workspace_bytes_rows(8, 1000, sv.SPEC_BF16) > 0
+    assert sv.spec_workspace_bytes_rows(0, 1000, sv.SPEC_BF16) == 0
+    # the extra-token-alone call still needs its lengths
+    assert lib.spec_sample_bonus(FAKE, FAKE, 1, 2, 2, 10, None, FAKE, 1.0, FAKE, FAKE, FAKE, W, None) == \
+        sv.SPEC_ERR_INVALID_ARG
+
+
 def test_tree_sample_host_validation(lib):
     t = lib.spec_verify_tree_sample
     W = 1 << 20

@@ -344,6 +344,40 @@ def test_tree_sample_workspace_left_zeroed_and_repeatable():
         assert torch.equal(a[k], b[k]), k
 
 
+# ------------------------------------------------------------- row sampler
+
+@pytest.mark.parametrize("B,V,dtype,T", [(64, 128256, "bf16", 0.7), (64, 128256, "bf16", 0.0), (300, 5003, "bf16", 1.3),
+                                         (7, 1, "f32", 1.0), (5, 33, "f32", 0.05), (40, 32000, "f32", 4.0)])
+def test_sample_rows_parity(B, V, dtype, T):
+    rng = np.random.default_rng(B * 7 + V)
+    x = torch.from_numpy((rng.standard_normal((B, V)) * 4.0).astype(np.float32))
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    x = x.cuda()
+    u = torch.from_numpy(rng.random(B).astype(np.float32)).cuda()
+    r = sv.spec_sample_rows(x, u if T > 0 else None, T)
+    torch.cuda.synchronize()
+    o = oracle.sample_rows(to_oracle(x), to_oracle(u) if T > 0 else None, T)
+    g = r["tokens"].cpu().numpy()
+    un = to_oracle(u)
+    bad = [b for b in range(B) if g[b] != o["tokens"][b]
+           and not (T > 0 and min(abs(un[b] - o["cdf"][b, 0]), abs(un[b] - o["cdf"][b, 1])) < compare.NEAR_TIE)]
+    assert not bad, [(b, int(g[b]), int(o["tokens"][b])) for b in bad[:5]]
+    assert int(r["status"].item()) == 0
+
+
+def test_sample_rows_equals_extra_token_at_the_tail():
+    """A zero-length draft: the extra token of each sequence is a draw from its one target row."""
+    rng = np.random.default_rng(77)
+    B, V = 20, 3001
+    x = torch.from_numpy(rng.standard_normal((B, V)).astype(np.float32) * 3).cuda()
+    u = torch.from_numpy(rng.random(B).astype(np.float32)).cuda()
+    rows = sv.spec_sample_rows(x, u, 0.9)
+    bonus = sv.spec_sample_bonus(x.view(B, 1, V), None, torch.zeros(B, dtype=torch.int32, device="cuda"), u, 0.9)
+    torch.cuda.synchronize()
+    assert torch.equal(rows["tokens"], bonus["bonus_token"])
+
+
 # -------------------------------------------------------------- status bits
 
 def test_bad_token_is_flagged_and_rejected():
