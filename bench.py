@@ -22,7 +22,8 @@ same workload (rank 0 only).
 each: the kernel alone, calls replayed from a CUDA graph over rotating input
 copies, with the oracle timed beside it on a bounded sample.  NAME is one of
 small, small_greedy, mtp_greedy, mtp_sample, medusa_tree, medusa_tree_sample,
-stress, or all.
+stress, draft_sampler, draft_sampler_greedy (one draft row per sequence of the
+draft-target workload: the draft side's next token), or all.
 """
 from __future__ import annotations
 
@@ -371,6 +372,8 @@ EXTRA = {
     "medusa_tree": (4, 0.0, "tree"),
     "medusa_tree_sample": (4, 1.0, "tree_sample"),
     "stress": (5, 0.7, "linear"),
+    "draft_sampler": (2, 0.7, "rows"),
+    "draft_sampler_greedy": (2, 0.0, "rows"),
 }
 
 
@@ -383,6 +386,9 @@ def _extra_inputs(name, dev):
     w = WORKLOADS[number]
     if kind == "linear":
         return w, T, kind, make_linear(number, T, device=dev)
+    if kind == "rows":
+        lin = make_linear(number, max(T, 0.7), device=dev)
+        return w, T, kind, dict(rows=lin["draft"][:, 0].contiguous(), u=lin["u_bonus"])
     d = make_tree(number, device=dev)
     B, N = d["node_tokens"].shape
     if kind == "tree_sample":
@@ -413,15 +419,20 @@ def run_extra(args, name):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     w, T, kind, d = _extra_inputs(name, dev)
-    bytes_per_step = w.logits_bytes(T)
+    bytes_per_step = d["rows"].numel() * d["rows"].element_size() if kind == "rows" else w.logits_bytes(T)
     rotate = max(1, min(4, int(2 * 129e6 // bytes_per_step) + 1))       # more than L2 over the copies
-    keys = ("target", "draft") if kind == "linear" else ("target",)
+    keys = {"linear": ("target", "draft"), "rows": ("rows",)}.get(kind, ("target",))
     copies = [d] + [dict(d, **{k: d[k].clone() for k in keys if d.get(k) is not None}) for _ in range(rotate - 1)]
     B = w.B
     stream = torch.cuda.Stream(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def make_call(c):
+        if kind == "rows":
+            out = dict(tokens=torch.empty(B, dtype=torch.int32, device=dev))
+            ws = torch.zeros(sv.spec_workspace_bytes_rows(B, w.V, c["rows"].dtype), dtype=torch.uint8, device=dev)
+            return lambda: sv.spec_sample_rows(c["rows"], c["u"] if T > 0 else None, T, out=out, status=status,
+                                               workspace=ws, stream=stream)
         if kind == "linear":
             K = w.K
             out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
@@ -485,7 +496,9 @@ def run_extra(args, name):
         cores = len(os.sched_getaffinity(0))
         oracle.threads(cores)
         h = {k: to_oracle(v) for k, v in d.items() if hasattr(v, "detach")}
-        if kind == "linear":
+        if kind == "rows":
+            f = lambda: oracle.sample_rows(h["rows"], h["u"] if T > 0 else None, T)  # noqa
+        elif kind == "linear":
             f = lambda: oracle.verify_linear(h["target"], h["draft"] if T > 0 else None, h["draft_tokens"],  # noqa
                                              h["u_accept"], h["u_bonus"], T)
         elif kind == "tree":
@@ -503,12 +516,12 @@ def run_extra(args, name):
         cpu = {"value": B * n / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
                "sample": "the full %d-sequence batch, %d repetitions in %.1f s" % (B, n, el)}
 
-    cfg = {"workload": name, "number": w.number, "kind": kind, "B": B, "K": w.K, "V": w.V,
+    cfg = {"workload": name, "number": w.number, "kind": kind, "B": B, "K": 0 if kind == "rows" else w.K, "V": w.V,
            "logits_dtype": w.dtype, "temperature": T, "logits_bytes_per_step": bytes_per_step,
            "l2": "inputs rotate over %d copies (%.0f MB %s the 129 MB L2)"
                  % (rotate, rotate * bytes_per_step / 1e6, ">" if rotate * bytes_per_step > 129e6 else "<"),
            "seed": w.seed}
-    if kind != "linear":
+    if kind in ("tree", "tree_sample"):
         cfg["N"] = int(d["node_tokens"].shape[1])
     line = {"metric": METRIC, "value": B / step_s, "unit": "seqs/s", "n_gpus": 1, "ms_per_step": 1e3 * step_s,
             "higher_is_better": True, "timing": "kernel alone, %d calls per CUDA graph replay, %d replays"

@@ -224,14 +224,16 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     }
     if (per_sm <= 0) return fail(SPEC_ERR_UNSUPPORTED, "kernel does not fit an SM (N=%d)", p.units_per_seq);
     p.nstage = ns;
-    // enough CTAs for every warp to get a tile, at most what is resident at once
-    const long long want = std::max<long long>(1, (p.stats_segs + kWarps - 1) / kWarps);
-    const long long grid = std::min<long long>(want, static_cast<long long>(per_sm) * di.sms);
-    const long long warps = grid * kWarps;
-    // small problems: a static split of the tiles, balanced to one tile; large ones: dynamic segments
+    // Small problems (up to kStaticTilesPerWarp tiles per resident warp): a static split of the tiles,
+    // balanced to one tile, over enough CTAs for every warp to get a tile.  Large ones: dynamic
+    // segments, over enough CTAs for every warp to get a segment.  Never more than is resident.
+    const long long resident = static_cast<long long>(per_sm) * di.sms;
     p.stats_tiles = static_cast<long long>(p.B) * p.rows_per_seq * p.S;
+    p.static_split = p.stats_tiles <= kStaticTilesPerWarp * resident * kWarps ? 1 : 0;
+    const long long units = p.static_split ? p.stats_tiles : p.stats_segs;
+    const long long grid = std::min<long long>(std::max<long long>(1, (units + kWarps - 1) / kWarps), resident);
+    const long long warps = grid * kWarps;
     p.nwarps = static_cast<int>(warps);
-    p.static_split = p.stats_tiles <= kStaticTilesPerWarp * warps ? 1 : 0;
     // Rows a residual pass may re-read, in stream order, up to 1/kKeepDiv of L2, are read at normal
     // L2 priority and everything else first-to-evict, so the first draws find their rows in L2:
     // the row pairs of the first positions (linear), or every row (extra token alone).
