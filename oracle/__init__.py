@@ -66,6 +66,8 @@ def _declare(lib):
     lib.oracle_verify_tree_sample.restype = i32
     lib.oracle_sample_rows.argtypes = [P, i32, i32, i32, P, ctypes.c_float, P, P]
     lib.oracle_sample_rows.restype = i32
+    lib.oracle_tree_mask.argtypes = [P, i32, P, P]
+    lib.oracle_tree_mask.restype = i32
     lib.oracle_threads.argtypes = [i32]
     lib.oracle_threads.restype = i32
     return lib
@@ -208,3 +210,24 @@ def sample_rows(logits, u, temperature, lib=None):
     if rc != 0:
         raise ValueError("oracle_sample_rows rejected its arguments")
     return out
+
+
+def tree_mask(parents, lib=None):
+    """Ancestor-or-self bitmask [N, ceil(N/32)] uint32 and depth [N] of a parent array.
+    Returns dict(mask, depth, bad) (bad: some parent was not an earlier node)."""
+    lib = lib or load()
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(-1)
+    N = len(par)
+    W = (N + 31) // 32
+    out = dict(mask=np.zeros((N, W), np.uint32), depth=np.zeros(N, np.int32))
+    rc = lib.oracle_tree_mask(_ptr(par), N, _ptr(out["mask"]), _ptr(out["depth"]))
+    if rc == 1:
+        raise ValueError("oracle_tree_mask rejected its arguments")
+    out["bad"] = rc == 2
+    return out
+
+
+def mask_bits(mask, N):
+    """The bitmask as a dense [N, N] 0/1 array."""
+    bits = np.unpackbits(np.ascontiguousarray(mask).view(np.uint8), axis=1, bitorder="little")
+    return bits[:, :N]

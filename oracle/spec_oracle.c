@@ -46,6 +46,10 @@
  *   - one token per row (the draft side's own choice of its next token, or
  *     any row a caller wants sampled): a draw from softmax(l / T) by inverse
  *     CDF with the row's uniform, or argmax (lowest index) when T == 0.
+ *   - tree attention mask (same page, section 三: a causal-style mask under
+ *     which no token attends to a token of another path): row i holds node
+ *     i and every ancestor of node i; depth[i] is the number of edges from
+ *     the root (the token's offset in position).
  *   - tree, sampling mode (the page's "Greedy或者Sampling"): the target's
  *     choice at node n is a draw from softmax(target_n / T) by inverse CDF
  *     with the caller's uniform u[b, n]; the walk is the greedy walk with that
@@ -428,6 +432,37 @@ int oracle_sample_rows(const void *logits, int dtype, int B, int V, const float 
         }
     }
     return 0;
+}
+
+/*
+ * Tree attention mask and depths from the parent array (parents[0] ignored;
+ * a node c >= 1 needs 0 <= parents[c] < c).  mask [N, W] uint32 words,
+ * W = ceil(N / 32): bit (j % 32) of word j / 32 of row i is set iff node j is
+ * node i or one of its ancestors.  depth [N].  Returns 0, or 2 if some parent
+ * breaks the rule (that node's walk stops there; its row and depth hold what
+ * was walked).
+ */
+int oracle_tree_mask(const int32_t *parents, int N, uint32_t *mask, int32_t *depth) {
+    if (N < 1) return 1;
+    const int W = (N + 31) / 32;
+    int bad = 0;
+    memset(mask, 0, sizeof(uint32_t) * (size_t)N * (size_t)W);
+    for (int i = 0; i < N; ++i) {
+        int cur = i, d = 0;
+        mask[(size_t)i * W + cur / 32] |= 1u << (cur % 32);
+        while (cur != 0) {
+            int par = parents[cur];
+            if (par < 0 || par >= cur) {
+                bad = 1;
+                break;
+            }
+            cur = par;
+            ++d;
+            mask[(size_t)i * W + cur / 32] |= 1u << (cur % 32);
+        }
+        depth[i] = d;
+    }
+    return bad ? 2 : 0;
 }
 
 /* Number of OpenMP threads the oracle runs with; n > 0 sets it first. */

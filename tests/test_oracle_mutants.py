@@ -57,6 +57,12 @@ MUTANTS = [
      "tokens[b] = inverse_cdf(p, V, (double)u[0], &lo, &hi);"),
     ("rows_greedy_from_row_zero", "tokens[b] = argmax_row(logits, dtype, (size_t)b, V);",
      "tokens[b] = argmax_row(logits, dtype, (size_t)0, V);"),
+    ("mask_self_dropped", "mask[(size_t)i * W + cur / 32] |= 1u << (cur % 32);\n        while (cur != 0) {",
+     "while (cur != 0) {"),
+    ("mask_wrong_bit", "            mask[(size_t)i * W + cur / 32] |= 1u << (cur % 32);\n        }",
+     "            mask[(size_t)i * W + cur / 32] |= 1u << ((cur + 1) % 32);\n        }"),
+    ("mask_depth_off_by_one", "        depth[i] = d;", "        depth[i] = d + 1;"),
+    ("mask_one_level_only", "            cur = par;\n            ++d;", "            cur = par;\n            ++d;\n            if (d > 1) break;"),
     ("tree_sample_row_of_root", "softmax_row(target, dtype, (size_t)b * N + n, V, T, p, NULL, NULL);",
      "softmax_row(target, dtype, (size_t)b * N, V, T, p, NULL, NULL);"),
 ]
@@ -78,6 +84,8 @@ def _pin_suite(lib):
         ("tree_sample_freq", lambda: spins.check_draw_frequencies(lib, V=4, T=0.5, M=4000)),
         ("tree_sample_walk", lambda: spins.check_walk_brute_force(lib)),
         ("tree_sample_greedy", lambda: spins.check_dominant_logit_is_greedy(lib)),
+        ("mask_chain", lambda: tpins.check_chain_mask_is_causal(lib)),
+        ("mask_paths", lambda: tpins.check_mask_against_path_enumeration(lib)),
         ("rows_freq", lambda: rpins.check_frequencies(lib, V=5, T=0.7, M=5000)),
         ("rows_greedy", lambda: rpins.check_greedy_is_argmax(lib)),
         ("rows_scaling", lambda: rpins.check_temperature_scaling(lib)),

@@ -173,3 +173,61 @@ def test_medusa_workload_mean_length_estimates_expected_length():
     L = r["path_len"].astype(np.float64)
     se = L.std() / np.sqrt(B)
     assert abs(L.mean() - el) < 4.5 * se, (L.mean(), el, se)
+
+
+# ------------------------------------------------------ tree attention mask
+# Section 三: the tree is flattened into one sequence, and a mask modelled on
+# the causal mask keeps tokens of different paths from attending to each other:
+# row i of the mask holds node i and its ancestors, and nothing else.
+
+def check_chain_mask_is_causal(lib):
+    N = 70
+    r = oracle.tree_mask(np.arange(-1, N - 1, dtype=np.int32), lib=lib)
+    np.testing.assert_array_equal(oracle.mask_bits(r["mask"], N), np.tril(np.ones((N, N), np.uint8)))
+    np.testing.assert_array_equal(r["depth"], np.arange(N))
+
+
+def check_mask_against_path_enumeration(lib, seed=61):
+    rng = np.random.default_rng(seed)
+    for trial in range(10):
+        N = int(rng.integers(1, 150))
+        parents = _random_tree(rng, N)
+        r = oracle.tree_mask(parents, lib=lib)
+        m = oracle.mask_bits(r["mask"], N)
+        for i in range(N):
+            path = [i]
+            while path[-1] != 0:
+                path.append(int(parents[path[-1]]))
+            want = np.zeros(N, np.uint8)
+            want[path] = 1
+            np.testing.assert_array_equal(m[i], want)
+            assert r["depth"][i] == len(path) - 1
+        assert not r["bad"]
+
+
+def test_chain_mask_is_the_causal_mask(oracle_lib):
+    check_chain_mask_is_causal(oracle_lib)
+
+
+def test_mask_rows_are_root_paths(oracle_lib):
+    check_mask_against_path_enumeration(oracle_lib)
+
+
+def test_cartesian_tree_mask_counts():
+    """Top-(s_1..s_K) Cartesian tree: every node's row holds depth + 1 bits; siblings never see each other."""
+    tree = medusa_tree.cartesian_tree([3, 2, 2])
+    par = np.array(tree.parents, np.int32)
+    r = oracle.tree_mask(par)
+    m = oracle.mask_bits(r["mask"], len(par))
+    np.testing.assert_array_equal(m.sum(1), r["depth"] + 1)
+    np.testing.assert_array_equal(r["depth"], np.array(tree.depth))
+    for c in range(1, len(par)):
+        for c2 in range(1, len(par)):
+            if c != c2 and par[c] == par[c2]:
+                assert m[c, c2] == 0
+
+
+def test_bad_parent_is_reported():
+    r = oracle.tree_mask(np.array([-1, 0, 5, 1], np.int32))
+    assert r["bad"]
+    assert r["depth"][3] == 2 and r["depth"][2] == 0
