@@ -23,7 +23,8 @@ each: the kernel alone, calls replayed from a CUDA graph over rotating input
 copies, with the oracle timed beside it on a bounded sample.  NAME is one of
 small, small_greedy, mtp_greedy, mtp_sample, medusa_tree, medusa_tree_sample,
 stress, draft_sampler, draft_sampler_greedy (one draft row per sequence of the
-draft-target workload: the draft side's next token), or all.
+draft-target workload: the draft side's next token), medusa_tree_mask (the
+tree attention mask of the 64-node tree), or all.
 """
 from __future__ import annotations
 
@@ -374,6 +375,7 @@ EXTRA = {
     "stress": (5, 0.7, "linear"),
     "draft_sampler": (2, 0.7, "rows"),
     "draft_sampler_greedy": (2, 0.0, "rows"),
+    "medusa_tree_mask": (4, 0.0, "mask"),
 }
 
 
@@ -386,6 +388,8 @@ def _extra_inputs(name, dev):
     w = WORKLOADS[number]
     if kind == "linear":
         return w, T, kind, make_linear(number, T, device=dev)
+    if kind == "mask":
+        return w, T, kind, dict(parents=make_tree(number, device=dev, B=1, V=64)["parents"])
     if kind == "rows":
         lin = make_linear(number, max(T, 0.7), device=dev)
         return w, T, kind, dict(rows=lin["draft"][:, 0].contiguous(), u=lin["u_bonus"])
@@ -419,15 +423,27 @@ def run_extra(args, name):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     w, T, kind, d = _extra_inputs(name, dev)
-    bytes_per_step = d["rows"].numel() * d["rows"].element_size() if kind == "rows" else w.logits_bytes(T)
+    if kind == "mask":
+        Nm = d["parents"].numel()
+        bytes_per_step = 4 * Nm * ((Nm + 31) // 32 + 2)  # mask words written, parents read, depths written
+    elif kind == "rows":
+        bytes_per_step = d["rows"].numel() * d["rows"].element_size()
+    else:
+        bytes_per_step = w.logits_bytes(T)
     rotate = max(1, min(4, int(2 * 129e6 // bytes_per_step) + 1))       # more than L2 over the copies
-    keys = {"linear": ("target", "draft"), "rows": ("rows",)}.get(kind, ("target",))
+    keys = {"linear": ("target", "draft"), "rows": ("rows",), "mask": ("parents",)}.get(kind, ("target",))
     copies = [d] + [dict(d, **{k: d[k].clone() for k in keys if d.get(k) is not None}) for _ in range(rotate - 1)]
-    B = w.B
+    B = 1 if kind == "mask" else w.B     # the mask is one per tree, shared by the batch
+    unit = "masks/s" if kind == "mask" else "seqs/s"
     stream = torch.cuda.Stream(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def make_call(c):
+        if kind == "mask":
+            Nm = c["parents"].numel()
+            out = dict(mask=torch.empty((Nm, (Nm + 31) // 32), dtype=torch.int32, device=dev),
+                       depth=torch.empty(Nm, dtype=torch.int32, device=dev))
+            return lambda: sv.spec_tree_mask(c["parents"], status=status, out=out, stream=stream)
         if kind == "rows":
             out = dict(tokens=torch.empty(B, dtype=torch.int32, device=dev))
             ws = torch.zeros(sv.spec_workspace_bytes_rows(B, w.V, c["rows"].dtype), dtype=torch.uint8, device=dev)
@@ -496,7 +512,9 @@ def run_extra(args, name):
         cores = len(os.sched_getaffinity(0))
         oracle.threads(cores)
         h = {k: to_oracle(v) for k, v in d.items() if hasattr(v, "detach")}
-        if kind == "rows":
+        if kind == "mask":
+            f = lambda: oracle.tree_mask(h["parents"])  # noqa
+        elif kind == "rows":
             f = lambda: oracle.sample_rows(h["rows"], h["u"] if T > 0 else None, T)  # noqa
         elif kind == "linear":
             f = lambda: oracle.verify_linear(h["target"], h["draft"] if T > 0 else None, h["draft_tokens"],  # noqa
@@ -513,7 +531,7 @@ def run_extra(args, name):
             el = time.perf_counter() - c0
             if el >= min(args.cpu_seconds, 20.0):
                 break
-        cpu = {"value": B * n / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+        cpu = {"value": B * n / el, "unit": unit, "cores": cores, "kind": "oracle",
                "sample": "the full %d-sequence batch, %d repetitions in %.1f s" % (B, n, el)}
 
     cfg = {"workload": name, "number": w.number, "kind": kind, "B": B, "K": 0 if kind == "rows" else w.K, "V": w.V,
@@ -523,7 +541,7 @@ def run_extra(args, name):
            "seed": w.seed}
     if kind in ("tree", "tree_sample"):
         cfg["N"] = int(d["node_tokens"].shape[1])
-    line = {"metric": METRIC, "value": B / step_s, "unit": "seqs/s", "n_gpus": 1, "ms_per_step": 1e3 * step_s,
+    line = {"metric": METRIC, "value": B / step_s, "unit": unit, "n_gpus": 1, "ms_per_step": 1e3 * step_s,
             "higher_is_better": True, "timing": "kernel alone, %d calls per CUDA graph replay, %d replays"
             % (per_graph, reps), "data": "synthetic", "config": cfg,
             "roofline": {"bound": "hbm", "achieved": gbps, "peak": peak, "unit": "GB/s", "frac": gbps / peak,

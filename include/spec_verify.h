@@ -207,6 +207,23 @@ spec_status spec_verify_tree_sample(const void *target_logits, spec_dtype dtype,
                                     size_t workspace_bytes, void *stream);
 
 /*
+ * The tree attention mask of a candidate tree ("Speculative-Decoding / Medusa"
+ * blog, section 三: the tree is flattened into one sequence and a mask modelled
+ * on the causal mask keeps tokens of different paths apart).  Row i holds node
+ * i and every ancestor of node i; depth[i] is the number of edges from the
+ * root (the token's position offset).
+ *   parents    [N] int32 (device): parents[0] ignored, 0 <= parents[c] < c.
+ *   mask_words [N, ceil(N/32)] uint32 (device, output): bit (j % 32) of word
+ *              j / 32 of row i is set iff node j is node i or its ancestor.
+ *   depth      [N] int32 (device, output).
+ *   dev_status [1]: SPEC_DEV_BAD_TREE when a parent breaks the rule; that
+ *              node's row and depth then hold the path up to the bad edge.
+ * 1 <= N <= 16384.  No workspace; one small launch.
+ */
+spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, int32_t *depth, uint32_t *dev_status,
+                           void *stream);
+
+/*
  * spec_verify_linear with the library's own workspace.  The pages describe no
  * such call: it exists for callers that cannot allocate device memory at the
  * point where they verify -- e.g. a host program embedded in an inference

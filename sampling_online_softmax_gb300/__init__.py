@@ -17,6 +17,7 @@ Entry points (same names as the C ABI):
   spec_verify_tree_sample  the same walk with the target's choice drawn at
                        every node (the section's sampled variant)
   spec_sample_rows     one token per row (the draft side's next token)
+  spec_tree_mask       the tree attention mask (ancestor bits) and depths
 """
 from __future__ import annotations
 
@@ -78,6 +79,8 @@ def load_library():
         lib.spec_workspace_bytes_rows.restype = u64
         lib.spec_sample_rows.argtypes = [P, i32, i32, i32, P, f32, P, P, P, u64, P]
         lib.spec_sample_rows.restype = i32
+        lib.spec_tree_mask.argtypes = [P, i32, P, P, P, P]
+        lib.spec_tree_mask.restype = i32
         lib.spec_workspace_bytes_tree_sample.restype = u64
         lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
         lib.spec_verify_linear.restype = i32
@@ -372,5 +375,28 @@ def spec_sample_rows(logits, u, temperature, *, status=None, out=None, workspace
     with torch.cuda.device(dev):
         st = lib.spec_sample_rows(_ptr(logits), _dtype_code(logits), B, V, _ptr(u), float(temperature),
                                   _ptr(out["tokens"]), _ptr(status), _ptr(ws), ws.numel(), h)
+    _check(st)
+    return out
+
+
+def spec_tree_mask(parents, *, status=None, out=None, stream=None):
+    """Tree attention mask of a parent array [N] (int32, CUDA): returns dict(mask [N, ceil(N/32)]
+    (int32 words holding uint32 bits: bit j % 32 of word j // 32 of row i is set iff node j is node
+    i or an ancestor), depth [N], status)."""
+    lib = load_library()
+    _cuda(parents, "parents", torch.int32)
+    N = parents.numel()
+    dev = parents.device
+    h, s = _stream_handle(dev, stream)
+    W = (N + 31) // 32
+    if out is None:
+        out = dict(mask=torch.empty((N, W), dtype=torch.int32, device=dev),
+                   depth=torch.empty(N, dtype=torch.int32, device=dev))
+    if status is None:
+        with torch.cuda.stream(s):
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out["status"] = status
+    with torch.cuda.device(dev):
+        st = lib.spec_tree_mask(_ptr(parents), N, _ptr(out["mask"]), _ptr(out["depth"]), _ptr(status), h)
     _check(st)
     return out

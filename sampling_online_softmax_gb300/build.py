@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
 SOURCES = [os.path.join(CSRC, "spec_verify.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("verify_kernels.cuh", "ptx.cuh")] + \
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("verify_kernels.cuh", "tree_mask.cuh", "ptx.cuh")] + \
     [os.path.join(INCLUDE, "spec_verify.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

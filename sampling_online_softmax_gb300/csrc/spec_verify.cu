@@ -16,6 +16,7 @@
 
 #include "spec_verify.h"
 #include "verify_kernels.cuh"
+#include "tree_mask.cuh"
 
 #ifndef SPEC_MAX_STAGES
 #define SPEC_MAX_STAGES 2
@@ -504,6 +505,28 @@ extern "C" spec_status spec_verify_tree_sample(const void *target_logits, spec_d
     bind_workspace(p, static_cast<unsigned char *>(workspace), wl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return eb == 4 ? launch<4, kTreeSample>(p, true, s) : launch<2, kTreeSample>(p, true, s);
+}
+
+extern "C" spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, int32_t *depth,
+                                      uint32_t *dev_status, void *stream) {
+    g_last_error[0] = '\0';
+    if (N < 1) return fail(SPEC_ERR_INVALID_ARG, "need N >= 1");
+    if (N > kMaxMaskNodes) return fail(SPEC_ERR_UNSUPPORTED, "N = %d > %d nodes", N, kMaxMaskNodes);
+    if (!parents || !mask_words || !depth || !dev_status) return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
+    if (!aligned(parents, 4) || !aligned(mask_words, 4) || !aligned(depth, 4) || !aligned(dev_status, 4))
+        return fail(SPEC_ERR_INVALID_ARG, "a pointer is misaligned");
+    DeviceInfo di;
+    int dev = 0;
+    spec_status st = device_info(&di, &dev);
+    if (st != SPEC_OK) return st;
+    const int W = (N + 31) / 32;
+    const int grid = std::min((N + kMaskWarps - 1) / kMaskWarps, di.sms * 8);
+    const size_t smem = static_cast<size_t>(kMaskWarps) * W * sizeof(uint32_t);
+    tree_mask_kernel<<<grid, kMaskWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(parents, N, W, mask_words,
+                                                                                         depth, dev_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "tree mask launch: %s", cudaGetErrorString(e));
+    return SPEC_OK;
 }
 
 // ---- spec_verify_linear_static: spec_verify_linear on a workspace compiled

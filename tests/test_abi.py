@@ -139,6 +139,15 @@ def test_sample_rows_host_validation(lib):
         sv.SPEC_ERR_INVALID_ARG
 
 
+def test_tree_mask_host_validation(lib):
+    f = lib.spec_tree_mask
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, 16385, FAKE, FAKE, FAKE, None) == sv.SPEC_ERR_UNSUPPORTED
+    assert f(None, 10, FAKE, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(FAKE, 10, FAKE, None, FAKE, None) == sv.SPEC_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(0x10002), 10, FAKE, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG   # misaligned
+
+
 def test_tree_sample_host_validation(lib):
     t = lib.spec_verify_tree_sample
     W = 1 << 20

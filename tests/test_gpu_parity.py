@@ -378,6 +378,34 @@ def test_sample_rows_equals_extra_token_at_the_tail():
     assert torch.equal(rows["tokens"], bonus["bonus_token"])
 
 
+# ------------------------------------------------------- tree attention mask
+
+def _mask_parity(parents_np):
+    par = torch.from_numpy(np.ascontiguousarray(parents_np, dtype=np.int32)).cuda()
+    r = sv.spec_tree_mask(par)
+    torch.cuda.synchronize()
+    o = oracle.tree_mask(parents_np)
+    np.testing.assert_array_equal(r["mask"].cpu().numpy().view(np.uint32), o["mask"])
+    np.testing.assert_array_equal(r["depth"].cpu().numpy(), o["depth"])
+    assert (int(r["status"].item()) & 16 != 0) == o["bad"]
+
+
+@pytest.mark.parametrize("N,seed", [(1, 0), (31, 1), (32, 2), (33, 3), (200, 4), (1000, 5), (4099, 6)])
+def test_tree_mask_parity(N, seed):
+    rng = np.random.default_rng(seed)
+    _mask_parity(np.array([-1] + [int(rng.integers(max(0, c - 6), c)) for c in range(1, N)], np.int32))
+
+
+def test_tree_mask_of_the_medusa_tree_and_a_chain():
+    d = make_tree(4, device="cpu", B=1, V=64)
+    _mask_parity(d["parents"].numpy())
+    _mask_parity(np.arange(-1, 700, dtype=np.int32))
+
+
+def test_tree_mask_flags_a_bad_parent():
+    _mask_parity(np.array([-1, 0, 7, 1, 2, 3], np.int32))
+
+
 # -------------------------------------------------------------- status bits
 
 def test_bad_token_is_flagged_and_rejected():

@@ -173,6 +173,9 @@ def make_tree(number: int = 4, device="cpu", B: int | None = None, V: int | None
     rng = np.random.default_rng((w.seed if seed is None else seed) + 7919)
     tokens = np.zeros((B, N), dtype=np.int32)
     children = tree.children()
+    if max(len(ch) for ch in children) + 1 > V:
+        raise ValueError("V = %d is too small for distinct sibling tokens (fan-out %d)"
+                         % (V, max(len(ch) for ch in children)))
     for n in range(N):
         ch = children[n]
         if not ch:
