@@ -40,8 +40,8 @@
  *   - All arithmetic on the device is fp32 (bf16 inputs are widened exactly);
  *     cumulative sums for the inverse CDF are exact int64 sums of the fp32
  *     weights of 16-byte groups of logits, in units of 2^-52.
- *   - Workspace: every entry point except spec_verify_linear_static needs a
- *     caller-owned device workspace of
+ *   - Workspace: every entry point except spec_verify_linear_static and
+ *     spec_tree_mask needs a caller-owned device workspace of
  *     spec_workspace_bytes_*() bytes, 16-byte aligned and zero-filled before
  *     its first use.  Every call leaves it zero-filled again, so one zeroing
  *     suffices for any number of calls, but one workspace must not be shared
