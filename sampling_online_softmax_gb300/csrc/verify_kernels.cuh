@@ -13,22 +13,26 @@
 // How (GB300 design): a streaming reduction in which every warp runs its own
 // pipeline and no warp waits on another while it holds unfinished work.
 //   * A "unit" is one (sequence, position): target row i with draft row i for
-//     linear sampling, otherwise one target row.  Every row is read as S tiles,
-//     8 KB windows on the 16-byte grid of global memory (only a row's first and
-//     last window can hold bytes of a neighbouring row), grouped into segments
-//     of kSegTiles tiles.  Linear rows are ordered position-major, so every
-//     sequence's first positions are decided early.
-//   * Persistent CTAs of twelve warps, one per SM.  A warp takes ranges of
-//     segments from a global counter (the next range is requested one range
-//     ahead, and ranges shrink as the work runs out) and keeps a ring of two
-//     stages filled with 1-D bulk copies (cp.async.bulk, one mbarrier and one
-//     descriptor per stage).
+//     linear sampling, otherwise one target row (a tree node, or the one row
+//     of an extra-token-alone call).  Every row is read as S tiles, 8 KB
+//     windows on the 16-byte grid of global memory (only a row's first and
+//     last window can hold bytes of a neighbouring row).  Linear rows are
+//     ordered position-major, tail rows last.
+//   * Persistent CTAs of twelve warps, one per SM.  Small problems (at most
+//     kStaticTilesPerWarp tiles per resident warp) split the tiles statically:
+//     warp w reduces tiles [T*w/W, T*(w+1)/W) as runs cut at row boundaries,
+//     with no counter on the issue side.  Large problems take ranges of
+//     kSegTiles-tile segments from a global counter (requested one range
+//     ahead; ranges shrink as the work runs out).  Every warp keeps a ring of
+//     two stages filled with 1-D bulk copies (cp.async.bulk, one mbarrier and
+//     one descriptor per stage).
 //   * Row statistics live in the log2-scaled domain: every lane keeps a running
 //     (mc, s), s = sum 2^(fma(l, c, -mc)), c = log2(e) / T, with packed fp32x2
 //     FMA/ADD and one MUFU ex2 per logit; mc is only an offset, re-based on the
 //     lane's max when a tile's terms grow past 2^64.  Greedy lanes keep (max,
-//     lowest argmax).  One warp reduces each whole segment and publishes one
-//     partial, so results do not depend on timing.
+//     lowest argmax).  One warp reduces each whole run (or segment) and
+//     publishes one partial; the runs depend only on the shape, so results do
+//     not depend on timing.
 //   * Publishing costs no fence: a partial (or the draft token's logit, or a
 //     residual chunk sum) is written once per call as a non-zero 64-bit value
 //     with a relaxed store and counted with a relaxed atomic.  The warp whose
@@ -36,14 +40,19 @@
 //     zero, decides the unit, and records it in the sequence's decided/accepted
 //     mask; the update that makes the first rejection known publishes a draw
 //     entry (or emits the sequence).
-//   * A draw entry names one row pair (or the tail row) and is cut into Sr
-//     residual tiles of at most 4 KB per row.  Warps take residual tiles once
-//     their stats work is exhausted (the stats stream has priority: the tail
-//     rows it ends with decide the last draws).  A residual tile sums the fp32
-//     weights max(0, p - q) (or p) of every 16-byte group exactly in int64
-//     fixed point (units of 2^-52) per 64-group chunk.  The warp that completes
-//     an entry's residual locates the token (a prefix over the chunk sums, then
-//     a rescan of one chunk) and emits the sequence.
+//   * A draw entry names one row pair (or one row: the tail, a tree node, a
+//     row to sample) and is cut into Sr residual tiles of at most 4 KB per
+//     row.  Warps claim residual tiles once their stats work is exhausted
+//     (the stats stream has priority: the tail rows it ends with decide the
+//     last draws).  A residual tile sums the fp32 weights max(0, p - q) (or p)
+//     of every 16-byte group exactly in int64 fixed point (units of 2^-52) per
+//     64-group chunk.  The warp that completes an entry's residual locates the
+//     token (a prefix over the chunk sums, then a rescan of one chunk) and
+//     emits it.
+//   * L2 policy: the rows a residual pass is likely to re-read (the first
+//     positions' row pairs in stream order, up to 1/kKeepDiv of L2) load at
+//     normal priority, everything else evict-first, so the re-reads mostly
+//     hit L2 and no high-priority line outlives the call.
 //   * No tensor cores (nothing here is a contraction).  Every wait is bounded
 //     and reports SPEC_DEV_TIMEOUT instead of trapping.
 #pragma once
