@@ -136,6 +136,13 @@ def _cuda(t, name, dtype=None):
     return t
 
 
+def _tree_shapes(parents, node_tokens, B, N):
+    if parents.numel() != N:
+        raise ValueError("parents must hold N = %d entries" % N)
+    if tuple(node_tokens.shape) != (B, N):
+        raise ValueError("node_tokens must be [B, N]")
+
+
 def _stream_handle(device, stream):
     s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream), s
@@ -207,6 +214,10 @@ def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperatu
         raise ValueError("draft must match target's dtype with shape [B, K, V]")
     if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
         raise ValueError("draft_tokens must be [B, K]")
+    if u_accept is not None and tuple(u_accept.shape) != (B, K):
+        raise ValueError("u_accept must be [B, K]")
+    if u_bonus is not None and tuple(u_bonus.shape) != (B,):
+        raise ValueError("u_bonus must be [B]")
     h, s = _stream_handle(dev, stream)
     if out is None:
         out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
@@ -252,6 +263,10 @@ def spec_verify_linear_static(target, draft, draft_tokens, u_accept, u_bonus, te
         raise ValueError("draft must match target's dtype with shape [B, K, V]")
     if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
         raise ValueError("draft_tokens must be [B, K]")
+    if u_accept is not None and tuple(u_accept.shape) != (B, K):
+        raise ValueError("u_accept must be [B, K]")
+    if u_bonus is not None and tuple(u_bonus.shape) != (B,):
+        raise ValueError("u_bonus must be [B]")
     for name in ("accept_len", "out_tokens", "num_emitted"):
         _cuda(out[name], name, torch.int32)
     _cuda(out.get("probs"), "probs", torch.float32)
@@ -278,6 +293,12 @@ def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status
     _cuda(draft, "draft")
     _cuda(accept_len, "accept_len", torch.int32)
     _cuda(u_bonus, "u_bonus", torch.float32)
+    if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
+        raise ValueError("draft must match target's dtype with shape [B, K, V]")
+    if accept_len is not None and tuple(accept_len.shape) != (B,):
+        raise ValueError("accept_len must be [B]")
+    if u_bonus is not None and tuple(u_bonus.shape) != (B,):
+        raise ValueError("u_bonus must be [B]")
     h, s = _stream_handle(dev, stream)
     if out is None:
         out = torch.empty(B, dtype=torch.int32, device=dev)
@@ -303,6 +324,7 @@ def spec_verify_tree(target, parents, node_tokens, max_depth, *, status=None, ou
     dev = target.device
     _cuda(parents, "parents", torch.int32)
     _cuda(node_tokens, "node_tokens", torch.int32)
+    _tree_shapes(parents, node_tokens, B, N)
     h, s = _stream_handle(dev, stream)
     D = int(max_depth)
     if out is None:
@@ -334,6 +356,9 @@ def spec_verify_tree_sample(target, parents, node_tokens, u_nodes, temperature, 
     _cuda(parents, "parents", torch.int32)
     _cuda(node_tokens, "node_tokens", torch.int32)
     _cuda(u_nodes, "u_nodes", torch.float32)
+    _tree_shapes(parents, node_tokens, B, N)
+    if tuple(u_nodes.shape) != (B, N):
+        raise ValueError("u_nodes must be [B, N]")
     h, s = _stream_handle(dev, stream)
     D = int(max_depth)
     if out is None:
@@ -363,6 +388,8 @@ def spec_sample_rows(logits, u, temperature, *, status=None, out=None, workspace
     B, V = logits.shape
     dev = logits.device
     _cuda(u, "u", torch.float32)
+    if u is not None and tuple(u.shape) != (B,):
+        raise ValueError("u must be [B]")
     h, s = _stream_handle(dev, stream)
     if out is None:
         out = dict(tokens=torch.empty(B, dtype=torch.int32, device=dev))
