@@ -32,6 +32,21 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99, with every entry point taken by address."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    names = [n for n in declared_functions()]
+    src = tmp_path / "abi.c"
+    src.write_text('#include "spec_verify.h"\ntypedef void (*fn)(void);\nint main(void) {\n  const fn f[] = {' +
+                   ", ".join("(fn)&%s" % n for n in names) + '};\n  return f[0] == 0;\n}\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-fsyntax-only", str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_every_declared_symbol_is_exported(lib):
     raw = ctypes.CDLL(sv.LIB_PATH)
     for name in declared_functions():
