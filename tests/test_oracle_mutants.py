@@ -37,6 +37,9 @@ MUTANTS = [
      "softmax_row(target, dtype, (size_t)b * (K + 1) + (j < K ? j : 0), V, T, pj, NULL, NULL);"),
     ("last_rejection_not_first", "j = i;\n                        decided = 1;", "j = i;"),
     ("inverse_cdf_not_strict", "if (C > target) {", "if (C >= target) {"),
+    ("softmax_max_not_subtracted", "        p[v] = exp((logit_at(logits, dtype, off + v) - m) / T);",
+     "        p[v] = exp(logit_at(logits, dtype, off + v) / T);"),
+    ("softmax_not_normalised", "    for (int v = 0; v < V; ++v) p[v] /= S;", "    for (int v = 0; v < V; ++v) p[v] /= 1.0;"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
     ("tree_extra_token_at_root", "ot[depth] = argmax_row(target, dtype, (size_t)b * N + cur, V);",
