@@ -39,6 +39,12 @@ MUTANTS = [
     ("inverse_cdf_not_strict", "if (C > target) {", "if (C >= target) {"),
     ("softmax_max_not_subtracted", "        p[v] = exp((logit_at(logits, dtype, off + v) - m) / T);",
      "        p[v] = exp(logit_at(logits, dtype, off + v) / T);"),
+    ("acceptance_not_strict", "!((double)u_accept[(size_t)b * K + i] < thr)",
+     "!((double)u_accept[(size_t)b * K + i] <= thr)"),
+    ("greedy_out_of_range_token_accepted", "                    if (x != am) { j = i; break; }",
+     "                    if (x != am && x >= 0) { j = i; break; }"),
+    ("threshold_unclamped", "                        thr = ratio < 1.0 ? ratio : 1.0;", "                        thr = ratio;"),
+    ("probs_p_and_q_swapped", "probs[((size_t)b * K + i) * 3 + 0] = px;", "probs[((size_t)b * K + i) * 3 + 0] = qx;"),
     ("softmax_not_normalised", "    for (int v = 0; v < V; ++v) p[v] /= S;", "    for (int v = 0; v < V; ++v) p[v] /= 1.0;"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
@@ -83,6 +89,8 @@ def _pin_suite(lib):
         ("zero_weight", lambda: pins.test_residual_zero_weight_token_never_drawn(lib)),
         ("bf16", lambda: pins.test_bf16_decoding_equals_fp32_values(lib)),
         ("spike", lambda: pins.test_spiked_constant_row_closed_form(lib, 1000, 5.0, 1.0)),
+        ("strict", lambda: pins.check_strict_acceptance_at_an_exact_ratio(lib)),
+        ("greedy_range", lambda: pins.check_greedy_rejects_an_out_of_range_token(lib)),
         ("tree", lambda: _tree_check(lib)),
         ("tree_sample_freq", lambda: spins.check_draw_frequencies(lib, V=4, T=0.5, M=4000)),
         ("tree_sample_walk", lambda: spins.check_walk_brute_force(lib)),

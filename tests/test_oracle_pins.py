@@ -372,3 +372,33 @@ def test_sample_bonus_matches_fused_extra_token(oracle_lib):
     j = r["accept_len"]
     np.testing.assert_array_equal(s["bonus_token"], r["out_tokens"][np.arange(B), j])
     np.testing.assert_array_equal(s["bonus_cdf"], r["bonus_cdf"])
+
+
+def check_strict_acceptance_at_an_exact_ratio(lib):
+    """u equal to min(1, p/q) rejects: the test is strict (the reading taken for the cited method).
+
+    V = 4, target logits all 0 (p = 1/4 each), draft logits (0, 0, -inf, -inf) (q = 1/2, 1/2, 0, 0):
+    for x = 0 the ratio p/q is exactly 1/2 in binary floating point, and u = 1/2 is exact too."""
+    target = np.zeros((2, 2, 4), np.float32)
+    draft = np.array([[[0.0, 0.0, -np.inf, -np.inf]]] * 2, np.float32)
+    tokens = np.zeros((2, 1), np.int32)
+    u = np.array([[0.5], [0.4999999]], np.float32)
+    r = oracle.verify_linear(target, draft, tokens, u, None, 1.0, lib=lib)
+    assert r["probs"][0, 0, 2] == 0.5
+    assert list(r["accept_len"]) == [0, 1]
+
+
+def check_greedy_rejects_an_out_of_range_token(lib):
+    target = np.zeros((3, 3, 5), np.float32)
+    target[:, :, 2] = 1.0                       # argmax 2 everywhere
+    tokens = np.array([[2, -1], [2, 5], [2, 2]], np.int32)
+    r = oracle.verify_linear(target, None, tokens, None, None, 0.0, lib=lib)
+    assert list(r["accept_len"]) == [1, 1, 2]
+
+
+def test_strict_acceptance_at_an_exact_ratio(oracle_lib):
+    check_strict_acceptance_at_an_exact_ratio(oracle_lib)
+
+
+def test_greedy_rejects_an_out_of_range_token(oracle_lib):
+    check_greedy_rejects_an_out_of_range_token(oracle_lib)
