@@ -45,6 +45,12 @@ MUTANTS = [
      "                    if (x != am && x >= 0) { j = i; break; }"),
     ("threshold_unclamped", "                        thr = ratio < 1.0 ? ratio : 1.0;", "                        thr = ratio;"),
     ("probs_p_and_q_swapped", "probs[((size_t)b * K + i) * 3 + 0] = px;", "probs[((size_t)b * K + i) * 3 + 0] = qx;"),
+    ("extra_alone_greedy_row_off", "                bonus_token[b] = argmax_row(target, dtype, (size_t)b * (K + 1) + j, V);",
+     "                bonus_token[b] = argmax_row(target, dtype, (size_t)b * (K + 1) + (j > 0 ? j - 1 : 0), V);"),
+    ("extra_alone_length_past_k_accepted", "            if (j < 0 || j > K) {\n                bonus_token[b] = -1;",
+     "            if (j < 0) {\n                bonus_token[b] = -1;"),
+    ("vanished_residual_not_redrawn", "        if (W > 0.0) return inverse_cdf(w, V, u, lo, hi);",
+     "        return inverse_cdf(w, V, u, lo, hi);"),
     ("softmax_not_normalised", "    for (int v = 0; v < V; ++v) p[v] /= S;", "    for (int v = 0; v < V; ++v) p[v] /= 1.0;"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
@@ -91,6 +97,8 @@ def _pin_suite(lib):
         ("spike", lambda: pins.test_spiked_constant_row_closed_form(lib, 1000, 5.0, 1.0)),
         ("strict", lambda: pins.check_strict_acceptance_at_an_exact_ratio(lib)),
         ("greedy_range", lambda: pins.check_greedy_rejects_an_out_of_range_token(lib)),
+        ("extra_alone", lambda: pins.check_extra_token_alone_rows_and_lengths(lib)),
+        ("vanished", lambda: pins.check_vanished_residual_draws_from_p(lib)),
         ("tree", lambda: _tree_check(lib)),
         ("tree_sample_freq", lambda: spins.check_draw_frequencies(lib, V=4, T=0.5, M=4000)),
         ("tree_sample_walk", lambda: spins.check_walk_brute_force(lib)),

@@ -402,3 +402,45 @@ def test_strict_acceptance_at_an_exact_ratio(oracle_lib):
 
 def test_greedy_rejects_an_out_of_range_token(oracle_lib):
     check_greedy_rejects_an_out_of_range_token(oracle_lib)
+
+
+def check_extra_token_alone_rows_and_lengths(lib):
+    """Greedy: the extra token at length j is numpy's argmax of target row j; a length outside
+    [0, K] gives -1 (the caller's error, reported by the token)."""
+    rng = np.random.default_rng(17)
+    B, K, V = 30, 3, 40
+    t = rng.integers(-4, 5, (B, K + 1, V)).astype(np.float32)
+    al = rng.integers(0, K + 1, B).astype(np.int32)
+    al[:3] = [-1, K + 1, K]
+    s = oracle.sample_bonus(t, None, al, None, 0.0, lib=lib)
+    for b in range(B):
+        want = -1 if (al[b] < 0 or al[b] > K) else int(t[b, al[b]].argmax())
+        assert s["bonus_token"][b] == want, (b, al[b])
+
+
+def check_vanished_residual_draws_from_p(lib):
+    """Identical target and draft rows leave max(0, p - q) = 0 everywhere: the draw falls back
+    to p_j itself (and is flagged), i.e. the first v whose cumulative p exceeds u."""
+    rng = np.random.default_rng(18)
+    B, K, V, T = 25, 2, 30, 0.8
+    t = (2.0 * rng.standard_normal((B, K + 1, V))).astype(np.float32)
+    d = t[:, :K].copy()
+    al = np.zeros(B, np.int32)
+    ub = rng.random(B).astype(np.float32)
+    s = oracle.sample_bonus(t, d, al, ub, T, lib=lib)
+    assert (s["flags"] & 1).all()
+    for b in range(B):
+        x = t[b, 0].astype(np.float64) / T
+        c = np.cumsum(np.exp(x - x.max()))
+        c /= c[-1]
+        if np.min(np.abs(c - ub[b])) < 1e-9:
+            continue
+        assert s["bonus_token"][b] == int(np.searchsorted(c, ub[b], side="right"))
+
+
+def test_extra_token_alone_rows_and_lengths(oracle_lib):
+    check_extra_token_alone_rows_and_lengths(oracle_lib)
+
+
+def test_vanished_residual_draws_from_p(oracle_lib):
+    check_vanished_residual_draws_from_p(oracle_lib)
