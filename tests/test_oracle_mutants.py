@@ -51,6 +51,17 @@ MUTANTS = [
      "            if (j < 0) {\n                bonus_token[b] = -1;"),
     ("vanished_residual_not_redrawn", "        if (W > 0.0) return inverse_cdf(w, V, u, lo, hi);",
      "        return inverse_cdf(w, V, u, lo, hi);"),
+    ("tree_greedy_depth_off", "        while (depth < max_depth) {\n            int want",
+     "        while (depth <= max_depth) {\n            int want"),
+    ("tree_greedy_last_matching_child",
+     "                if (parents[c] == cur && node_tokens[(size_t)b * N + c] == want) {\n                    next = c;\n                    break;",
+     "                if (parents[c] == cur && node_tokens[(size_t)b * N + c] == want) {\n                    next = c;"),
+    ("tree_sample_last_matching_child",
+     "                if (parents[c] == cur && node_tokens[(size_t)b * N + c] == draw[cur]) {\n                    next = c;\n                    break;",
+     "                if (parents[c] == cur && node_tokens[(size_t)b * N + c] == draw[cur]) {\n                    next = c;"),
+    ("tree_path_token_of_parent",
+     "            ot[depth] = node_tokens[(size_t)b * N + next];\n            ++depth;\n            pn[depth] = next;\n            cur = next;\n        }\n        path_len[b] = depth;\n        ot[depth] = argmax_row",
+     "            ot[depth] = node_tokens[(size_t)b * N + cur];\n            ++depth;\n            pn[depth] = next;\n            cur = next;\n        }\n        path_len[b] = depth;\n        ot[depth] = argmax_row"),
     ("softmax_not_normalised", "    for (int v = 0; v < V; ++v) p[v] /= S;", "    for (int v = 0; v < V; ++v) p[v] /= 1.0;"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
@@ -100,6 +111,8 @@ def _pin_suite(lib):
         ("extra_alone", lambda: pins.check_extra_token_alone_rows_and_lengths(lib)),
         ("vanished", lambda: pins.check_vanished_residual_draws_from_p(lib)),
         ("tree", lambda: _tree_check(lib)),
+        ("tree_brute", lambda: tpins.check_tree_walk_brute_force(lib)),
+        ("tree_duplicates", lambda: tpins.check_lowest_index_child_on_duplicate_tokens(lib)),
         ("tree_sample_freq", lambda: spins.check_draw_frequencies(lib, V=4, T=0.5, M=4000)),
         ("tree_sample_walk", lambda: spins.check_walk_brute_force(lib)),
         ("tree_sample_greedy", lambda: spins.check_dominant_logit_is_greedy(lib)),

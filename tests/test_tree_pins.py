@@ -114,8 +114,8 @@ def _brute_force_walk(target, parents, tokens, max_depth):
     return best, am[best[-1]]
 
 
-def test_tree_walk_matches_brute_force():
-    rng = np.random.default_rng(21)
+def check_tree_walk_brute_force(lib=None, seed=21):
+    rng = np.random.default_rng(seed)
     B, V = 60, 12
     for trial in range(8):
         N = int(rng.integers(1, 24))
@@ -135,7 +135,7 @@ def test_tree_walk_matches_brute_force():
                 for c, t in zip(ch[n], pool):
                     tokens[b, c] = t
         max_depth = int(rng.integers(0, 6))
-        r = oracle.verify_tree(target, parents, tokens, max_depth)
+        r = oracle.verify_tree(target, parents, tokens, max_depth, lib=lib)
         for b in range(B):
             path, bonus = _brute_force_walk(target[b], parents, tokens[b], max_depth)
             L = len(path) - 1
@@ -231,3 +231,31 @@ def test_bad_parent_is_reported():
     r = oracle.tree_mask(np.array([-1, 0, 5, 1], np.int32))
     assert r["bad"]
     assert r["depth"][3] == 2 and r["depth"][2] == 0
+
+
+def test_tree_walk_matches_brute_force(oracle_lib):
+    check_tree_walk_brute_force(oracle_lib)
+
+
+def check_lowest_index_child_on_duplicate_tokens(lib):
+    """When several children carry the target's choice, the walk takes the lowest-index one,
+    greedy and sampled (with a dominant logit every draw is the argmax)."""
+    # root 0 -> children 1, 2, 3 all carrying token 4 (the root's argmax); 1 -> 4, 2 -> 5, 3 -> 6
+    parents = np.array([-1, 0, 0, 0, 1, 2, 3], np.int32)
+    V = 8
+    target = np.zeros((1, 7, V), np.float32)
+    target[0, 0, 4] = 60.0                       # root: argmax 4
+    target[0, 1:, 6] = 60.0                      # every other node: argmax 6
+    tokens = np.array([[0, 4, 4, 4, 6, 6, 6]], np.int32)
+    g = oracle.verify_tree(target, parents, tokens, 3, lib=lib)
+    assert list(g["path_nodes"][0]) == [0, 1, 4, -1] and list(g["out_tokens"][0]) == [4, 6, 6, -1]
+    u = np.full((1, 7), 0.5, np.float32)
+    s = oracle.verify_tree_sample(target, parents, tokens, u, 1.0, 3, lib=lib)
+    assert list(s["path_nodes"][0]) == [0, 1, 4, -1] and list(s["out_tokens"][0]) == [4, 6, 6, -1]
+    # max_depth stops the walk even when a child would match
+    g1 = oracle.verify_tree(target, parents, tokens, 1, lib=lib)
+    assert list(g1["path_nodes"][0]) == [0, 1] and list(g1["out_tokens"][0]) == [4, 6]
+
+
+def test_lowest_index_child_on_duplicate_tokens(oracle_lib):
+    check_lowest_index_child_on_duplicate_tokens(oracle_lib)
