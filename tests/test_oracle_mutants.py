@@ -62,6 +62,15 @@ MUTANTS = [
     ("tree_path_token_of_parent",
      "            ot[depth] = node_tokens[(size_t)b * N + next];\n            ++depth;\n            pn[depth] = next;\n            cur = next;\n        }\n        path_len[b] = depth;\n        ot[depth] = argmax_row",
      "            ot[depth] = node_tokens[(size_t)b * N + cur];\n            ++depth;\n            pn[depth] = next;\n            cur = next;\n        }\n        path_len[b] = depth;\n        ot[depth] = argmax_row"),
+    ("residual_draft_row_off", "        softmax_row(draft, dtype, (size_t)b * K + j, V, T, qj, NULL, NULL);",
+     "        softmax_row(draft, dtype, (size_t)b * K + (j + 1 < K ? j + 1 : j), V, T, qj, NULL, NULL);"),
+    ("draft_logit_from_target", "double dx = logit_at(draft, dtype, ((size_t)b * K + i) * (size_t)V + x);",
+     "double dx = logit_at(target, dtype, ((size_t)b * (K + 1) + i) * (size_t)V + x);"),
+    ("uniform_of_position_zero", "!((double)u_accept[(size_t)b * K + i] < thr)", "!((double)u_accept[(size_t)b * K] < thr)"),
+    ("emitted_counts_missing_extra", "            } else {\n                num_emitted[b] = j;\n            }",
+     "            } else {\n                num_emitted[b] = j + 1;\n            }"),
+    ("draft_token_of_next_position", "                    int x = draft_tokens[(size_t)b * K + i];\n                    double px",
+     "                    int x = draft_tokens[(size_t)b * K + (i + 1 < K ? i + 1 : i)];\n                    double px"),
     ("softmax_not_normalised", "    for (int v = 0; v < V; ++v) p[v] /= S;", "    for (int v = 0; v < V; ++v) p[v] /= 1.0;"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),
