@@ -71,6 +71,14 @@ MUTANTS = [
      "            } else {\n                num_emitted[b] = j + 1;\n            }"),
     ("draft_token_of_next_position", "                    int x = draft_tokens[(size_t)b * K + i];\n                    double px",
      "                    int x = draft_tokens[(size_t)b * K + (i + 1 < K ? i + 1 : i)];\n                    double px"),
+    ("tree_sample_node_token_of_parent",
+     "            ot[depth] = node_tokens[(size_t)b * N + next];\n            ++depth;\n            pn[depth] = next;\n            cur = next;\n        }\n        path_len[b] = depth;\n        ot[depth] = draw[cur];",
+     "            ot[depth] = node_tokens[(size_t)b * N + cur];\n            ++depth;\n            pn[depth] = next;\n            cur = next;\n        }\n        path_len[b] = depth;\n        ot[depth] = draw[cur];"),
+    ("tree_sample_depth_off", "        while (depth < max_depth) {\n            int next = -1;",
+     "        while (depth <= max_depth) {\n            int next = -1;"),
+    ("rows_greedy_highest_index_on_ties", "            tokens[b] = argmax_row(logits, dtype, (size_t)b, V);",
+     "            { int bb = 0; double bv = -INFINITY; for (int v = 0; v < V; ++v) { double l = logit_at(logits, dtype, "
+     "(size_t)b * V + v); if (l >= bv) { bv = l; bb = v; } } tokens[b] = bb; }"),
     ("softmax_not_normalised", "    for (int v = 0; v < V; ++v) p[v] /= S;", "    for (int v = 0; v < V; ++v) p[v] /= 1.0;"),
     ("argmax_highest_index_on_ties", "if (l > bv) { bv = l; best = v; }", "if (l >= bv) { bv = l; best = v; }"),
     ("bf16_wrong_shift", "uint32_t w = ((uint32_t)h) << 16;", "uint32_t w = ((uint32_t)h) << 15;"),

@@ -231,6 +231,9 @@ def test_bad_parent_is_reported():
     r = oracle.tree_mask(np.array([-1, 0, 5, 1], np.int32))
     assert r["bad"]
     assert r["depth"][3] == 2 and r["depth"][2] == 0
+    # a node that is its own parent stops its walk too (a parent must precede its child)
+    r = oracle.tree_mask(np.array([-1, 0, 2, 2], np.int32))
+    assert r["bad"] and r["depth"][2] == 0 and r["depth"][3] == 1
 
 
 def test_tree_walk_matches_brute_force(oracle_lib):
