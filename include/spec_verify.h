@@ -43,9 +43,16 @@
  *   - Workspace: every entry point except spec_verify_linear_static and
  *     spec_tree_mask needs a caller-owned device workspace of
  *     spec_workspace_bytes_*() bytes, 16-byte aligned and zero-filled before
- *     its first use.  Every call leaves it zero-filled again, so one zeroing
- *     suffices for any number of calls, but one workspace must not be shared
- *     by calls that may run at the same time.
+ *     its first use.  Every call leaves it zero-filled again -- also a call
+ *     that reports SPEC_DEV_TIMEOUT: its last CTA then clears every byte the
+ *     call used -- so one zeroing suffices for any number of calls, but one
+ *     workspace must not be shared by calls that may run at the same time.
+ *   - Residency: the verify kernel's warps wait (bounded) on values that
+ *     warps of other CTAs publish, so it is launched cooperatively: all its
+ *     CTAs (at most one per SM) are resident at once, or the launch fails and
+ *     the call returns SPEC_ERR_CUDA.  A launch can fail that way when other
+ *     work holds SMs (an MPS client limited to part of the GPU, a green
+ *     context); it never deadlocks waiting for a CTA that cannot start.
  *   - The functions keep no mutable global state apart from a per-thread copy
  *     of the last error message; they may be called from several host threads.
  */
@@ -54,6 +61,14 @@
 
 #include <stddef.h>
 #include <stdint.h>
+
+/* Exported symbols: the library is built with hidden visibility, and only the
+ * functions declared here are exported from it. */
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -75,27 +90,27 @@ typedef enum spec_dtype {
 /* Bits OR-ed into *dev_status by the kernels. */
 #define SPEC_DEV_BAD_TOKEN     1u  /* a draft token outside [0, V): treated as rejected */
 #define SPEC_DEV_NONFINITE     2u  /* a row whose max or exp-sum is not finite; outputs unspecified */
-#define SPEC_DEV_TIMEOUT       4u  /* a bounded wait on a copy gave up; outputs unspecified */
+#define SPEC_DEV_TIMEOUT       4u  /* a bounded wait (a copy, or a value another warp publishes) gave up; outputs unspecified, workspace cleared */
 #define SPEC_DEV_ZERO_RESIDUAL 8u  /* residual weight W == 0 at a rejection: drew from p_j instead */
 #define SPEC_DEV_BAD_TREE     16u  /* parents[] not topological (0 <= parents[c] < c): edge ignored */
 #define SPEC_DEV_BAD_LENGTH   32u  /* spec_sample_bonus: accept_len[b] outside [0, K]; token -1 */
 
 /* Bytes of workspace spec_verify_linear needs for B sequences of K draft
  * tokens over a vocabulary of V logits of `dtype` (0 for invalid sizes). */
-size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype);
+SPEC_API size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype);
 
 /* Bytes of workspace spec_sample_bonus needs for B sequences. */
-size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype);
+SPEC_API size_t spec_workspace_bytes_bonus(int B, int V, spec_dtype dtype);
 
 /* Bytes of workspace spec_sample_rows needs for B rows of V logits. */
-size_t spec_workspace_bytes_rows(int B, int V, spec_dtype dtype);
+SPEC_API size_t spec_workspace_bytes_rows(int B, int V, spec_dtype dtype);
 
 /* Bytes of workspace spec_verify_tree needs for B sequences of N tree nodes. */
-size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype);
+SPEC_API size_t spec_workspace_bytes_tree(int B, int N, int V, spec_dtype dtype);
 
 /* Bytes of workspace spec_verify_tree_sample needs (one draw per node: grows
  * with B * N * V). */
-size_t spec_workspace_bytes_tree_sample(int B, int N, int V, spec_dtype dtype);
+SPEC_API size_t spec_workspace_bytes_tree_sample(int B, int N, int V, spec_dtype dtype);
 
 /*
  * Linear verify and (optionally) the extra token, in one launch.
@@ -121,7 +136,7 @@ size_t spec_workspace_bytes_tree_sample(int B, int N, int V, spec_dtype dtype);
  *   dev_status    [1]      SPEC_DEV_* bits OR-ed in.
  *   workspace, workspace_bytes: see the conventions above.
  */
-spec_status spec_verify_linear(const void *target_logits, const void *draft_logits,
+SPEC_API spec_status spec_verify_linear(const void *target_logits, const void *draft_logits,
                                spec_dtype dtype, int B, int K, int V,
                                const int32_t *draft_tokens, const float *u_accept,
                                const float *u_bonus, float temperature,
@@ -138,7 +153,7 @@ spec_status spec_verify_linear(const void *target_logits, const void *draft_logi
  *               range (and SPEC_DEV_BAD_LENGTH is set).
  *   workspace, workspace_bytes: spec_workspace_bytes_bonus(B, V, dtype) bytes.
  */
-spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits,
+SPEC_API spec_status spec_sample_bonus(const void *target_logits, const void *draft_logits,
                               spec_dtype dtype, int B, int K, int V,
                               const int32_t *accept_len, const float *u_bonus, float temperature,
                               int32_t *bonus_token, uint32_t *dev_status,
@@ -156,7 +171,7 @@ spec_status spec_sample_bonus(const void *target_logits, const void *draft_logit
  *   workspace, workspace_bytes: spec_workspace_bytes_rows(B, V, dtype) bytes.
  * It runs the extra-token path with no draft (K = 0).
  */
-spec_status spec_sample_rows(const void *logits, spec_dtype dtype, int B, int V, const float *u, float temperature,
+SPEC_API spec_status spec_sample_rows(const void *logits, spec_dtype dtype, int B, int V, const float *u, float temperature,
                              int32_t *tokens, uint32_t *dev_status, void *workspace, size_t workspace_bytes,
                              void *stream);
 
@@ -176,7 +191,7 @@ spec_status spec_sample_rows(const void *logits, spec_dtype dtype, int B, int V,
  *   path_len   [B]               number of accepted non-root nodes
  *   out_tokens [B, max_depth+1]  tokens of n_1..n_len, then the extra token
  */
-spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B, int N, int V,
+SPEC_API spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B, int N, int V,
                              const int32_t *parents, const int32_t *node_tokens, int max_depth,
                              int32_t *path_nodes, int32_t *path_len, int32_t *out_tokens,
                              uint32_t *dev_status, void *workspace, size_t workspace_bytes,
@@ -200,7 +215,7 @@ spec_status spec_verify_tree(const void *target_logits, spec_dtype dtype, int B,
  *   max_depth, path_nodes, path_len, out_tokens, dev_status: as spec_verify_tree.
  *   workspace, workspace_bytes: spec_workspace_bytes_tree_sample(B, N, V, dtype).
  */
-spec_status spec_verify_tree_sample(const void *target_logits, spec_dtype dtype, int B, int N, int V,
+SPEC_API spec_status spec_verify_tree_sample(const void *target_logits, spec_dtype dtype, int B, int N, int V,
                                     const int32_t *parents, const int32_t *node_tokens, const float *u_nodes,
                                     float temperature, int max_depth, int32_t *path_nodes, int32_t *path_len,
                                     int32_t *out_tokens, uint32_t *dev_status, void *workspace,
@@ -220,7 +235,7 @@ spec_status spec_verify_tree_sample(const void *target_logits, spec_dtype dtype,
  *              node's row and depth then hold the path up to the bad edge.
  * 1 <= N <= 16384.  No workspace; one small launch.
  */
-spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, int32_t *depth, uint32_t *dev_status,
+SPEC_API spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, int32_t *depth, uint32_t *dev_status,
                            void *stream);
 
 /*
@@ -240,8 +255,11 @@ spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, 
  *
  * First call on each device: it looks up the array's device address
  * (cudaGetSymbolAddress, with that device current; this may also load the
- * library's kernels onto the device).  Make one call on every device you will
- * use before you begin any stream capture on it.
+ * library's kernels onto the device) and keeps it for the life of the
+ * process.  Make one call on every device you will use before you begin any
+ * stream capture on it.  Resetting a device (cudaDeviceReset) after that
+ * first call is not supported: the kept address would name memory of the
+ * destroyed context.
  *
  * Every call clears the part of the array it uses with cudaMemsetAsync on
  * `stream` before its kernel, so no earlier call's leftovers matter.  There is
@@ -254,7 +272,7 @@ spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, 
  */
 #define SPEC_STATIC_WORKSPACE_BYTES (16u << 20)
 
-spec_status spec_verify_linear_static(const void *target_logits, const void *draft_logits,
+SPEC_API spec_status spec_verify_linear_static(const void *target_logits, const void *draft_logits,
                                       spec_dtype dtype, int B, int K, int V,
                                       const int32_t *draft_tokens, const float *u_accept,
                                       const float *u_bonus, float temperature,
@@ -262,10 +280,10 @@ spec_status spec_verify_linear_static(const void *target_logits, const void *dra
                                       float *probs_out, uint32_t *dev_status, void *stream);
 
 /* Static text for a status code. */
-const char *spec_status_string(spec_status status);
+SPEC_API const char *spec_status_string(spec_status status);
 
 /* Detail of the last error returned on the calling host thread ("" if none). */
-const char *spec_last_error(void);
+SPEC_API const char *spec_last_error(void);
 
 #ifdef __cplusplus
 }

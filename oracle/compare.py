@@ -22,6 +22,16 @@ import numpy as np
 NEAR_TIE = 1e-6
 PROB_ATOL = 1e-5
 
+# Every report made in this process, with the label the caller set (the test
+# session prints them, so near ties are reported, not only counted).
+LOG = []
+LABEL = [""]
+
+
+def _logged(rep, kind):
+    LOG.append((LABEL[0], kind, rep))
+    return rep
+
 
 @dataclasses.dataclass
 class ParityReport:
@@ -92,7 +102,7 @@ def compare_linear(gpu: dict, ora: dict, u_accept, u_bonus, temperature: float, 
         else:
             rep.failures.append("b=%d extra token gpu %d oracle %d (u_b=%.9g, interval [%.9g, %.9g))" % (
                 b, gpu["out_tokens"][b, jo], ora["out_tokens"][b, jo], u_bonus[b], lo, hi))
-    return rep
+    return _logged(rep, "linear")
 
 
 def compare_bonus(gpu_tokens, ora: dict, u_bonus, temperature: float) -> ParityReport:
@@ -108,7 +118,7 @@ def compare_bonus(gpu_tokens, ora: dict, u_bonus, temperature: float) -> ParityR
             rep.bonus_ties += 1
         else:
             rep.failures.append("b=%d extra token gpu %d oracle %d" % (b, g, o))
-    return rep
+    return _logged(rep, "extra token")
 
 
 def compare_tree(gpu: dict, ora: dict) -> ParityReport:
@@ -123,12 +133,25 @@ def compare_tree(gpu: dict, ora: dict) -> ParityReport:
             rep.failures.append("b=%d tree: gpu len %d nodes %s tokens %s; oracle len %d nodes %s tokens %s" % (
                 b, gpu["path_len"][b], list(gpu["path_nodes"][b]), list(gpu["out_tokens"][b]),
                 ora["path_len"][b], list(ora["path_nodes"][b]), list(ora["out_tokens"][b])))
-    return rep
+    return _logged(rep, "tree")
+
+
+def _diverging_node(gp, op, tokens_equal_on_path):
+    """The node whose draw decided where two sampled walks part: the last node the
+    two root paths share (if the paths differ), else the last node (if only the
+    extra token, the draw at the last node, differs)."""
+    common = 0
+    while common < min(len(gp), len(op)) and gp[common] == op[common]:
+        common += 1
+    if len(gp) == len(op) == common and tokens_equal_on_path:
+        return gp[-1]
+    return gp[common - 1] if common > 0 else 0
 
 
 def compare_tree_sample(gpu: dict, ora: dict, u_nodes) -> ParityReport:
-    """Sampled tree walk: paths and tokens equal, except where a uniform at a node of
-    either path lies within NEAR_TIE of that node's draw interval (counted as a tie)."""
+    """Sampled tree walk: paths and tokens equal, except where the walks part at a
+    node whose uniform lies within NEAR_TIE of an end of that node's draw interval
+    in the oracle (counted as a tie).  Only that first diverging node is tested."""
     rep = ParityReport()
     u_nodes = np.asarray(u_nodes, np.float64)
     B = len(ora["path_len"])
@@ -138,13 +161,35 @@ def compare_tree_sample(gpu: dict, ora: dict, u_nodes) -> ParityReport:
                 and np.array_equal(gpu["out_tokens"][b], ora["out_tokens"][b])):
             rep.exact += 1
             continue
-        nodes = {int(n) for n in gpu["path_nodes"][b] if n >= 0} | {int(n) for n in ora["path_nodes"][b] if n >= 0}
-        near = any(min(abs(u_nodes[b, n] - ora["node_cdf"][b, n, 0]), abs(u_nodes[b, n] - ora["node_cdf"][b, n, 1]))
-                   < NEAR_TIE for n in nodes)
-        if near:
+        gl, ol = int(gpu["path_len"][b]), int(ora["path_len"][b])
+        gp = [int(n) for n in gpu["path_nodes"][b][:gl + 1]]
+        op = [int(n) for n in ora["path_nodes"][b][:ol + 1]]
+        same_path_tokens = gl == ol and np.array_equal(gpu["out_tokens"][b][:gl], ora["out_tokens"][b][:ol])
+        n = _diverging_node(gp, op, same_path_tokens)
+        lo, hi = ora["node_cdf"][b, n]
+        if min(abs(u_nodes[b, n] - lo), abs(u_nodes[b, n] - hi)) < NEAR_TIE:
             rep.bonus_ties += 1
         else:
-            rep.failures.append("b=%d sampled tree: gpu len %d nodes %s tokens %s; oracle len %d nodes %s tokens %s" % (
-                b, gpu["path_len"][b], list(gpu["path_nodes"][b]), list(gpu["out_tokens"][b]),
-                ora["path_len"][b], list(ora["path_nodes"][b]), list(ora["out_tokens"][b])))
-    return rep
+            rep.failures.append("b=%d sampled tree: gpu len %d nodes %s tokens %s; oracle len %d nodes %s tokens %s "
+                                "(walks part at node %d, u=%.9g, interval [%.9g, %.9g))" % (
+                                    b, gl, gp, list(gpu["out_tokens"][b]), ol, op, list(ora["out_tokens"][b]),
+                                    n, u_nodes[b, n], lo, hi))
+    return _logged(rep, "sampled tree")
+
+
+def compare_rows(gpu_tokens, ora: dict, u, temperature: float) -> ParityReport:
+    """One token per row: equal, except a sampled token whose uniform lies within NEAR_TIE
+    of either end of the oracle's interval (counted as a tie)."""
+    rep = ParityReport()
+    gpu_tokens = np.asarray(gpu_tokens)
+    rep.sequences = len(gpu_tokens)
+    for b, g in enumerate(gpu_tokens):
+        o = ora["tokens"][b]
+        if g == o:
+            rep.exact += 1
+        elif temperature > 0 and u is not None and (abs(float(u[b]) - ora["cdf"][b, 0]) < NEAR_TIE
+                                                     or abs(float(u[b]) - ora["cdf"][b, 1]) < NEAR_TIE):
+            rep.bonus_ties += 1
+        else:
+            rep.failures.append("b=%d row token gpu %d oracle %d" % (b, g, o))
+    return _logged(rep, "rows")

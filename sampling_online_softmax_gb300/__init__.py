@@ -124,11 +124,13 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError("logits must be float32 or bfloat16, got %s" % t.dtype)
 
 
-def _cuda(t, name, dtype=None):
+def _cuda(t, name, dtype=None, device=None):
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the logits on %s" % (name, t.device, device))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
@@ -136,11 +138,69 @@ def _cuda(t, name, dtype=None):
     return t
 
 
+def _outputs(out, shapes, device):
+    """Check caller-provided output tensors: every name present, int32/float32 as
+    given, on `device`, contiguous, with exactly the shape the kernel writes."""
+    for name, (shape, dtype) in shapes.items():
+        t = out.get(name)
+        if t is None:
+            raise ValueError("out[%r] is missing" % name)
+        _cuda(t, "out[%r]" % name, dtype, device)
+        if tuple(t.shape) != tuple(shape):
+            raise ValueError("out[%r] must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return out
+
+
+def _status(status, device, stream):
+    if status is None:
+        with torch.cuda.stream(stream):
+            return torch.zeros(1, dtype=torch.int32, device=device)
+    _cuda(status, "status", torch.int32, device)
+    if status.numel() < 1:
+        raise ValueError("status must hold at least one int32")
+    return status
+
+
+def _ws(workspace, nbytes, device, stream):
+    if workspace is None:
+        return _workspace(device, stream, nbytes)
+    _cuda(workspace, "workspace", None, device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace needs %d bytes" % nbytes)
+    return workspace
+
+
 def _tree_shapes(parents, node_tokens, B, N):
     if parents.numel() != N:
         raise ValueError("parents must hold N = %d entries" % N)
     if tuple(node_tokens.shape) != (B, N):
         raise ValueError("node_tokens must be [B, N]")
+
+
+def _tree_inputs(target, parents, node_tokens):
+    """Check the inputs of a tree verify; returns (B, N, V, device)."""
+    _cuda(target, "target")
+    if target.dim() != 3:
+        raise ValueError("target must be [B, N, V]")
+    B, N, V = target.shape
+    dev = target.device
+    if parents is None or node_tokens is None:
+        raise ValueError("parents and node_tokens are required")
+    _cuda(parents, "parents", torch.int32, dev)
+    _cuda(node_tokens, "node_tokens", torch.int32, dev)
+    _tree_shapes(parents, node_tokens, B, N)
+    return B, N, V, dev
+
+
+def _tree_outputs(out, B, D, dev):
+    if D < 0:
+        raise ValueError("max_depth must be >= 0")
+    if out is None:
+        out = dict(path_nodes=torch.empty((B, D + 1), dtype=torch.int32, device=dev),
+                   path_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   out_tokens=torch.empty((B, D + 1), dtype=torch.int32, device=dev))
+    return _outputs(out, {"path_nodes": ((B, D + 1), torch.int32), "path_len": ((B,), torch.int32),
+                          "out_tokens": ((B, D + 1), torch.int32)}, dev)
 
 
 def _stream_handle(device, stream):
@@ -191,6 +251,37 @@ def spec_workspace_bytes_tree_sample(B: int, N: int, V: int, dtype) -> int:
     return int(load_library().spec_workspace_bytes_tree_sample(int(B), int(N), int(V), _dtype_arg(dtype)))
 
 
+def _linear_inputs(target, draft, draft_tokens, u_accept, u_bonus):
+    """Check the inputs of a linear verify; returns (B, K, V, device)."""
+    _cuda(target, "target")
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    _cuda(draft, "draft", None, dev)
+    _cuda(draft_tokens, "draft_tokens", torch.int32, dev)
+    _cuda(u_accept, "u_accept", torch.float32, dev)
+    _cuda(u_bonus, "u_bonus", torch.float32, dev)
+    if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
+        raise ValueError("draft must match target's dtype with shape [B, K, V]")
+    if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
+        raise ValueError("draft_tokens must be [B, K]")
+    if u_accept is not None and tuple(u_accept.shape) != (B, K):
+        raise ValueError("u_accept must be [B, K]")
+    if u_bonus is not None and tuple(u_bonus.shape) != (B,):
+        raise ValueError("u_bonus must be [B]")
+    return B, K, V, dev
+
+
+def _linear_outputs(out, B, K, dev):
+    shapes = {"accept_len": ((B,), torch.int32), "out_tokens": ((B, K + 1), torch.int32),
+              "num_emitted": ((B,), torch.int32)}
+    if out.get("probs") is not None:
+        shapes["probs"] = ((B, K, 3), torch.float32)
+    return _outputs(out, shapes, dev)
+
+
 def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperature, *,
                        probs: bool = False, status=None, out=None, workspace=None, stream=None):
     """Verify K draft tokens per sequence; returns a dict of device tensors.
@@ -202,22 +293,7 @@ def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperatu
     (SPEC_DEV_* bits, int32), and probs [B, K, 3] when requested.
     """
     lib = load_library()
-    _cuda(target, "target")
-    B, K1, V = target.shape
-    K = K1 - 1
-    dev = target.device
-    _cuda(draft, "draft")
-    _cuda(draft_tokens, "draft_tokens", torch.int32)
-    _cuda(u_accept, "u_accept", torch.float32)
-    _cuda(u_bonus, "u_bonus", torch.float32)
-    if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
-        raise ValueError("draft must match target's dtype with shape [B, K, V]")
-    if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
-        raise ValueError("draft_tokens must be [B, K]")
-    if u_accept is not None and tuple(u_accept.shape) != (B, K):
-        raise ValueError("u_accept must be [B, K]")
-    if u_bonus is not None and tuple(u_bonus.shape) != (B,):
-        raise ValueError("u_bonus must be [B]")
+    B, K, V, dev = _linear_inputs(target, draft, draft_tokens, u_accept, u_bonus)
     h, s = _stream_handle(dev, stream)
     if out is None:
         out = dict(accept_len=torch.empty(B, dtype=torch.int32, device=dev),
@@ -225,12 +301,11 @@ def spec_verify_linear(target, draft, draft_tokens, u_accept, u_bonus, temperatu
                    num_emitted=torch.empty(B, dtype=torch.int32, device=dev))
         if probs:
             out["probs"] = torch.empty((B, K, 3), dtype=torch.float32, device=dev)
-    if status is None:
-        with torch.cuda.stream(s):
-            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _linear_outputs(out, B, K, dev)
+    status = _status(status, dev, s)
     out["status"] = status
     nbytes = spec_workspace_bytes_linear(B, K, V, target.dtype)
-    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    ws = _ws(workspace, nbytes, dev, s)
     with torch.cuda.device(dev):
         st = lib.spec_verify_linear(
             _ptr(target), _ptr(draft), _dtype_code(target), B, K, V, _ptr(draft_tokens), _ptr(u_accept),
@@ -251,26 +326,13 @@ def spec_verify_linear_static(target, draft, draft_tokens, u_accept, u_bonus, te
     share the one workspace and race; keep them on one stream.
     """
     lib = load_library()
-    _cuda(target, "target")
-    B, K1, V = target.shape
-    K = K1 - 1
-    dev = target.device
-    _cuda(draft, "draft")
-    _cuda(draft_tokens, "draft_tokens", torch.int32)
-    _cuda(u_accept, "u_accept", torch.float32)
-    _cuda(u_bonus, "u_bonus", torch.float32)
-    if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
-        raise ValueError("draft must match target's dtype with shape [B, K, V]")
-    if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
-        raise ValueError("draft_tokens must be [B, K]")
-    if u_accept is not None and tuple(u_accept.shape) != (B, K):
-        raise ValueError("u_accept must be [B, K]")
-    if u_bonus is not None and tuple(u_bonus.shape) != (B,):
-        raise ValueError("u_bonus must be [B]")
-    for name in ("accept_len", "out_tokens", "num_emitted"):
-        _cuda(out[name], name, torch.int32)
-    _cuda(out.get("probs"), "probs", torch.float32)
-    _cuda(status, "status", torch.int32)
+    B, K, V, dev = _linear_inputs(target, draft, draft_tokens, u_accept, u_bonus)
+    _linear_outputs(out, B, K, dev)
+    if status is None:
+        raise ValueError("status must be passed in (nothing is allocated here)")
+    _cuda(status, "status", torch.int32, dev)
+    if status.numel() < 1:
+        raise ValueError("status must hold at least one int32")
     h, _ = _stream_handle(dev, stream)
     with torch.cuda.device(dev):
         st = lib.spec_verify_linear_static(
@@ -287,12 +349,14 @@ def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status
     """The extra token alone at row accept_len[b]; returns dict(bonus_token [B], status [1])."""
     lib = load_library()
     _cuda(target, "target")
+    if target.dim() != 3:
+        raise ValueError("target must be [B, K+1, V]")
     B, K1, V = target.shape
     K = K1 - 1
     dev = target.device
-    _cuda(draft, "draft")
-    _cuda(accept_len, "accept_len", torch.int32)
-    _cuda(u_bonus, "u_bonus", torch.float32)
+    _cuda(draft, "draft", None, dev)
+    _cuda(accept_len, "accept_len", torch.int32, dev)
+    _cuda(u_bonus, "u_bonus", torch.float32, dev)
     if draft is not None and (draft.dtype != target.dtype or tuple(draft.shape) != (B, K, V)):
         raise ValueError("draft must match target's dtype with shape [B, K, V]")
     if accept_len is not None and tuple(accept_len.shape) != (B,):
@@ -302,11 +366,10 @@ def spec_sample_bonus(target, draft, accept_len, u_bonus, temperature, *, status
     h, s = _stream_handle(dev, stream)
     if out is None:
         out = torch.empty(B, dtype=torch.int32, device=dev)
-    if status is None:
-        with torch.cuda.stream(s):
-            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _outputs(dict(bonus_token=out), {"bonus_token": ((B,), torch.int32)}, dev)
+    status = _status(status, dev, s)
     nbytes = spec_workspace_bytes_bonus(B, V, target.dtype)
-    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    ws = _ws(workspace, nbytes, dev, s)
     with torch.cuda.device(dev):
         st = lib.spec_sample_bonus(_ptr(target), _ptr(draft), _dtype_code(target), B, K, V, _ptr(accept_len),
                                    _ptr(u_bonus), float(temperature), _ptr(out), _ptr(status), _ptr(ws),
@@ -319,24 +382,14 @@ def spec_verify_tree(target, parents, node_tokens, max_depth, *, status=None, ou
                      stream=None):
     """Greedy tree walk; returns dict(path_nodes, path_len, out_tokens, status)."""
     lib = load_library()
-    _cuda(target, "target")
-    B, N, V = target.shape
-    dev = target.device
-    _cuda(parents, "parents", torch.int32)
-    _cuda(node_tokens, "node_tokens", torch.int32)
-    _tree_shapes(parents, node_tokens, B, N)
+    B, N, V, dev = _tree_inputs(target, parents, node_tokens)
     h, s = _stream_handle(dev, stream)
     D = int(max_depth)
-    if out is None:
-        out = dict(path_nodes=torch.empty((B, D + 1), dtype=torch.int32, device=dev),
-                   path_len=torch.empty(B, dtype=torch.int32, device=dev),
-                   out_tokens=torch.empty((B, D + 1), dtype=torch.int32, device=dev))
-    if status is None:
-        with torch.cuda.stream(s):
-            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = _tree_outputs(out, B, D, dev)
+    status = _status(status, dev, s)
     out["status"] = status
     nbytes = spec_workspace_bytes_tree(B, N, V, target.dtype)
-    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    ws = _ws(workspace, nbytes, dev, s)
     with torch.cuda.device(dev):
         st = lib.spec_verify_tree(_ptr(target), _dtype_code(target), B, N, V, _ptr(parents), _ptr(node_tokens), D,
                                   _ptr(out["path_nodes"]), _ptr(out["path_len"]), _ptr(out["out_tokens"]),
@@ -350,27 +403,19 @@ def spec_verify_tree_sample(target, parents, node_tokens, u_nodes, temperature, 
     """Tree walk with the target's choice drawn at every node (u_nodes [B, N] fp32);
     returns dict(path_nodes, path_len, out_tokens, status)."""
     lib = load_library()
-    _cuda(target, "target")
-    B, N, V = target.shape
-    dev = target.device
-    _cuda(parents, "parents", torch.int32)
-    _cuda(node_tokens, "node_tokens", torch.int32)
-    _cuda(u_nodes, "u_nodes", torch.float32)
-    _tree_shapes(parents, node_tokens, B, N)
+    B, N, V, dev = _tree_inputs(target, parents, node_tokens)
+    if u_nodes is None:
+        raise ValueError("u_nodes is required")
+    _cuda(u_nodes, "u_nodes", torch.float32, dev)
     if tuple(u_nodes.shape) != (B, N):
         raise ValueError("u_nodes must be [B, N]")
     h, s = _stream_handle(dev, stream)
     D = int(max_depth)
-    if out is None:
-        out = dict(path_nodes=torch.empty((B, D + 1), dtype=torch.int32, device=dev),
-                   path_len=torch.empty(B, dtype=torch.int32, device=dev),
-                   out_tokens=torch.empty((B, D + 1), dtype=torch.int32, device=dev))
-    if status is None:
-        with torch.cuda.stream(s):
-            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = _tree_outputs(out, B, D, dev)
+    status = _status(status, dev, s)
     out["status"] = status
     nbytes = spec_workspace_bytes_tree_sample(B, N, V, target.dtype)
-    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    ws = _ws(workspace, nbytes, dev, s)
     with torch.cuda.device(dev):
         st = lib.spec_verify_tree_sample(_ptr(target), _dtype_code(target), B, N, V, _ptr(parents),
                                          _ptr(node_tokens), _ptr(u_nodes), float(temperature), D,
@@ -385,20 +430,21 @@ def spec_sample_rows(logits, u, temperature, *, status=None, out=None, workspace
     argmax when temperature == 0 (u may be None); returns dict(tokens [B], status)."""
     lib = load_library()
     _cuda(logits, "logits")
+    if logits.dim() != 2:
+        raise ValueError("logits must be [B, V]")
     B, V = logits.shape
     dev = logits.device
-    _cuda(u, "u", torch.float32)
+    _cuda(u, "u", torch.float32, dev)
     if u is not None and tuple(u.shape) != (B,):
         raise ValueError("u must be [B]")
     h, s = _stream_handle(dev, stream)
     if out is None:
         out = dict(tokens=torch.empty(B, dtype=torch.int32, device=dev))
-    if status is None:
-        with torch.cuda.stream(s):
-            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _outputs(out, {"tokens": ((B,), torch.int32)}, dev)
+    status = _status(status, dev, s)
     out["status"] = status
     nbytes = spec_workspace_bytes_rows(B, V, logits.dtype)
-    ws = workspace if workspace is not None else _workspace(dev, s, nbytes)
+    ws = _ws(workspace, nbytes, dev, s)
     with torch.cuda.device(dev):
         st = lib.spec_sample_rows(_ptr(logits), _dtype_code(logits), B, V, _ptr(u), float(temperature),
                                   _ptr(out["tokens"]), _ptr(status), _ptr(ws), ws.numel(), h)
@@ -419,9 +465,8 @@ def spec_tree_mask(parents, *, status=None, out=None, stream=None):
     if out is None:
         out = dict(mask=torch.empty((N, W), dtype=torch.int32, device=dev),
                    depth=torch.empty(N, dtype=torch.int32, device=dev))
-    if status is None:
-        with torch.cuda.stream(s):
-            status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _outputs(out, {"mask": ((N, W), torch.int32), "depth": ((N,), torch.int32)}, dev)
+    status = _status(status, dev, s)
     out["status"] = status
     with torch.cuda.device(dev):
         st = lib.spec_tree_mask(_ptr(parents), N, _ptr(out["mask"]), _ptr(out["depth"]), _ptr(status), h)

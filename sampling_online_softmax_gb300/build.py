@@ -1,6 +1,12 @@
-"""Compile libspecverify.so (the CUDA kernels and their C ABI) in-tree for sm_103a."""
+"""Compile libspecverify.so (the CUDA kernels and their C ABI) in-tree for sm_103a.
+
+The kernel's modes live in separate translation units (csrc/kern_*.cu), which
+are compiled in parallel and linked with the host side (csrc/spec_verify.cu).
+"""
 from __future__ import annotations
 
+import concurrent.futures
+import glob
 import os
 import shutil
 import subprocess
@@ -10,12 +16,12 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
-SOURCES = [os.path.join(CSRC, "spec_verify.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("verify_kernels.cuh", "tree_mask.cuh", "ptx.cuh")] + \
+SOURCES = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+DEPENDS = SOURCES + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + \
     [os.path.join(INCLUDE, "spec_verify.h")]
 
-NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-              "-Xcompiler", "-fPIC", "-shared", "-Xptxas", "-v"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+COMPILE_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-v"]
 
 
 def nvcc() -> str:
@@ -36,14 +42,33 @@ def build(force: bool = False, out: str = LIB_PATH, extra_flags=(), verbose: boo
     """Build the shared library (skipped when newer than its sources)."""
     if not force and up_to_date(out):
         return out
-    tmp = out + ".tmp.%d" % os.getpid()
-    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-o", tmp, *SOURCES]
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    if verbose:
-        print(res.stdout + res.stderr)
-    os.replace(tmp, out)
+    objdir = out + ".objs.%d" % os.getpid()
+    os.makedirs(objdir, exist_ok=True)
+    try:
+        def compile_one(src):
+            obj = os.path.join(objdir, os.path.basename(src) + ".o")
+            cmd = [nvcc(), *COMPILE_FLAGS, *extra_flags, "-I", INCLUDE, "-c", "-o", obj, src]
+            res = subprocess.run(cmd, capture_output=True, text=True)
+            return src, obj, res
+
+        workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
+        with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+            results = list(ex.map(compile_one, SOURCES))
+        log = []
+        for src, obj, res in results:
+            log.append(res.stdout + res.stderr)
+            if res.returncode != 0:
+                raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, res.stdout, res.stderr))
+        tmp = out + ".tmp.%d" % os.getpid()
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[obj for _, obj, _ in results]]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
+        if verbose:
+            print("".join(log))
+        os.replace(tmp, out)
+    finally:
+        shutil.rmtree(objdir, ignore_errors=True)
     return out
 
 

@@ -1,5 +1,6 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: thread-block clusters,
-// distributed shared memory, mbarriers and 1-D bulk (TMA) copies.
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, 1-D bulk (TMA)
+// copies with L2 cache policies, and the few arithmetic instructions the
+// kernels name directly.
 #pragma once
 #include <cstdint>
 
@@ -8,66 +9,6 @@ namespace ptx {
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// ---- cluster geometry
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-// Full cluster barrier: every thread of every CTA of the cluster arrives
-// (release) and waits (acquire).  All threads must call it (aligned form).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// ---- distributed shared memory: map a local shared address to CTA `rank`
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ double ld_dsmem_f64(uint32_t addr) {
-    double v;
-    asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ long long ld_dsmem_s64(uint32_t addr) {
-    long long v;
-    asm volatile("ld.shared::cluster.s64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_dsmem_s32(uint32_t addr, int v) {
-    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // ---- mbarrier (CTA-local) and 1-D bulk copy global -> shared

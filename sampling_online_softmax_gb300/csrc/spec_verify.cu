@@ -1,6 +1,7 @@
 // spec_verify.cu -- host side of libspecverify.so: the C ABI declared in
-// include/spec_verify.h (argument checks, workspace layout, tiling and launch
-// shape, and the launches of the kernel in verify_kernels.cuh).
+// include/spec_verify.h (argument checks, workspace layout, device attributes)
+// and the tree-mask launch.  The verify kernel's launches go through
+// launch<EB, MODE> (launch.cuh), instantiated one mode per kern_*.cu unit.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -14,20 +15,14 @@
 #include <mutex>
 #include <tuple>
 
+#include "host.h"
 #include "spec_verify.h"
-#include "verify_kernels.cuh"
 #include "tree_mask.cuh"
 
-#ifndef SPEC_MAX_STAGES
-#define SPEC_MAX_STAGES 2
-#endif
-
 namespace spec {
-namespace {
 
 thread_local char g_last_error[512] = "";
 
-spec_status fail(spec_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 spec_status fail(spec_status s, const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -36,20 +31,10 @@ spec_status fail(spec_status s, const char *fmt, ...) {
     return s;
 }
 
-inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
-inline bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
-
-constexpr int kMaxDevices = 64;
-
-struct DeviceInfo {
-    int sms = 0;
-    size_t max_dyn = 0;  // opt-in dynamic shared memory per block
-    size_t l2 = 0;       // L2 cache bytes
-};
-
+namespace {
 DeviceInfo g_dev[kMaxDevices];
 std::once_flag g_dev_once[kMaxDevices];
-std::mutex g_attr_mutex;
+}  // namespace
 
 spec_status device_info(DeviceInfo *out, int *dev_out) {
     int dev = 0;
@@ -72,20 +57,11 @@ spec_status device_info(DeviceInfo *out, int *dev_out) {
     return SPEC_OK;
 }
 
-// Stats tiling: a row is read as kTileBytes windows on the 16-byte grid of
-// global memory; every row gets the same number of tiles (the count for the
-// worst alignment; a spare last window is empty).
 int stats_tiles_per_row(int V, int eb) {
     return static_cast<int>((static_cast<long long>(V) * eb + 30 + kTileBytes - 1) / kTileBytes);
 }
 int segments_per_row(int V, int eb) { return (stats_tiles_per_row(V, eb) + kSegTiles - 1) / kSegTiles; }
 
-// Residual slices of a row: at most kResidSliceBytes each, a whole number of
-// 16-byte groups long, none empty.  A function of V and the element size only.
-struct Slicing {
-    int S;  // slices per row
-    int L;  // elements per slice
-};
 Slicing resid_slicing(int V, int eb) {
     const int G = 16 / eb;
     const long long row_bytes = static_cast<long long>(V) * eb;
@@ -96,8 +72,56 @@ Slicing resid_slicing(int V, int eb) {
     return {S, L};
 }
 
+int blocks_per_sm(int dev, const void *kernel, size_t dyn) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, size_t>, int> cache;
+    const auto key = std::make_tuple(dev, kernel, dyn);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, dyn) != cudaSuccess) {
+        cudaGetLastError();  // clear the (non-sticky) error
+        n = 0;
+    }
+    cache[key] = n;
+    return n;
+}
+
+spec_status allow_max_dyn_smem(int dev, const void *kernel, DeviceInfo *di) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> done;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(dev, kernel);
+    auto it = done.find(key);
+    if (it == done.end()) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+        if (fa.sharedSizeBytes >= di->max_dyn) return fail(SPEC_ERR_UNSUPPORTED, "static shared memory too large");
+        const size_t m = di->max_dyn - fa.sharedSizeBytes;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(m));
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        it = done.emplace(key, m).first;
+    }
+    di->max_dyn = it->second;
+    return SPEC_OK;
+}
+
+#ifdef SPEC_TEST_HOOKS
+namespace {
+std::atomic<int> g_test_withhold{-1};
+}
+int test_withhold_unit() { return g_test_withhold.load(); }
+#endif
+
+namespace {
+
+inline size_t align16(size_t n) { return (n + 15) & ~size_t(15); }
+inline bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
 // Workspace layout (16-byte aligned parts):
-//   [counters: 4 u32][stats tiles per unit: n_units u32][units per sequence: B u32]
+//   [control: kCtrlWords u32][stats tiles per unit: n_units u32][units per sequence: B u32]
 //   [decided / accepted masks: B u64]
 //   [accept bits: B*K i32][argmax: n_units i32][run partials: n_units*2*S u64]
 //   [t(x), d(x): n_units * 2 u64][draw statistics: n_units float4]
@@ -111,7 +135,7 @@ WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, size_t entrie
     const size_t n_units = static_cast<size_t>(B) * units_per_seq;
     WsLayout w;
     w.ctrl = 0;
-    w.unit_cnt = 16;
+    w.unit_cnt = kCtrlWords * 4;
     w.seq_cnt = w.unit_cnt + align16(n_units * 4);
     w.seqmask = w.seq_cnt + align16(static_cast<size_t>(B) * 4);
     w.acc = w.seqmask + align16(static_cast<size_t>(B) * 8);
@@ -127,6 +151,8 @@ WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, size_t entrie
 }
 
 void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
+    p.ws_base = ws;
+    p.ws_bytes = wl.total;
     p.ws_ctrl = reinterpret_cast<uint32_t *>(ws + wl.ctrl);
     p.ws_unit_cnt = reinterpret_cast<uint32_t *>(ws + wl.unit_cnt);
     p.ws_seq_cnt = reinterpret_cast<uint32_t *>(ws + wl.seq_cnt);
@@ -157,103 +183,6 @@ WsLayout layout_tree_sample(int B, int N, int V, int eb) {
                      static_cast<size_t>(B) * static_cast<size_t>(N));
 }
 
-// Resident blocks per SM for this kernel and shared-memory size (cached).
-int blocks_per_sm(int dev, const void *kernel, size_t dyn) {
-    static std::mutex mu;
-    static std::map<std::tuple<int, const void *, size_t>, int> cache;
-    const auto key = std::make_tuple(dev, kernel, dyn);
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, dyn) != cudaSuccess) {
-        cudaGetLastError();  // clear the (non-sticky) error
-        n = 0;
-    }
-    cache[key] = n;
-    return n;
-}
-
-// Fill in the tiling of p0 (rows_per_seq and the problem sizes already set),
-// choose the ring depth and grid, and launch.
-template <int EB, int MODE>
-spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
-    DeviceInfo di;
-    int dev = 0;
-    spec_status st = device_info(&di, &dev);
-    if (st != SPEC_OK) return st;
-    auto kernel = spec_verify_kernel<EB, MODE>;
-    {
-        // per device and kernel, once: allow the largest dynamic shared memory next to the static part
-        static size_t max_dyn[kMaxDevices] = {};
-        std::lock_guard<std::mutex> lock(g_attr_mutex);
-        if (max_dyn[dev] == 0) {
-            cudaFuncAttributes fa;
-            cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kernel));
-            if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
-            if (fa.sharedSizeBytes >= di.max_dyn) return fail(SPEC_ERR_UNSUPPORTED, "static shared memory too large");
-            const size_t m = di.max_dyn - fa.sharedSizeBytes;
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(m));
-            if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-            max_dyn[dev] = m;
-        }
-        di.max_dyn = max_dyn[dev];
-    }
-    Params p = p0;
-    const Slicing rs = resid_slicing(p.V, EB);
-    p.S = stats_tiles_per_row(p.V, EB);
-    p.nseg = segments_per_row(p.V, EB);
-    p.Sr = rs.S;
-    p.Lr = rs.L;
-    p.stats_segs = static_cast<long long>(p.B) * p.rows_per_seq * p.nseg;
-    p.res_tiles = draws ? static_cast<long long>(MODE == kTreeSample ? p.n_units : p.B) * p.Sr : 0;
-    // ring depth: the deepest ring that keeps kMinCtas CTAs on an SM
-    const size_t scratch =
-        (MODE == kTreeGreedy || MODE == kTreeSample) ? static_cast<size_t>(kWarps) * 3 * p.units_per_seq * 4 : 0;
-    int ns = 0, per_sm = 0;
-    size_t dyn = 0;
-    for (int cand : {SPEC_MAX_STAGES, 2}) {
-        const size_t d = static_cast<size_t>(kWarps) * cand * kStageBytes + scratch;
-        if (d > di.max_dyn) continue;
-        const int b = blocks_per_sm(dev, reinterpret_cast<const void *>(kernel), d);
-        if (b >= kMinCtas || (cand == 2 && b >= 1)) {
-            ns = cand;
-            per_sm = b;
-            dyn = d;
-            break;
-        }
-    }
-    if (per_sm <= 0) return fail(SPEC_ERR_UNSUPPORTED, "kernel does not fit an SM (N=%d)", p.units_per_seq);
-    p.nstage = ns;
-    // Small problems (up to kStaticTilesPerWarp tiles per resident warp): a static split of the tiles,
-    // balanced to one tile, over enough CTAs for every warp to get a tile.  Large ones: dynamic
-    // segments, over enough CTAs for every warp to get a segment.  Never more than is resident.
-    const long long resident = static_cast<long long>(per_sm) * di.sms;
-    p.stats_tiles = static_cast<long long>(p.B) * p.rows_per_seq * p.S;
-    p.static_split = p.stats_tiles <= kStaticTilesPerWarp * resident * kWarps ? 1 : 0;
-    const long long units = p.static_split ? p.stats_tiles : p.stats_segs;
-    const long long grid = std::min<long long>(std::max<long long>(1, (units + kWarps - 1) / kWarps), resident);
-    const long long warps = grid * kWarps;
-    p.nwarps = static_cast<int>(warps);
-    // Rows a residual pass may re-read, in stream order, up to 1/kKeepDiv of L2, are read at normal
-    // L2 priority and everything else first-to-evict, so the first draws find their rows in L2:
-    // the row pairs of the first positions (linear), or every row (extra token alone).
-    p.keep_rows = 0;
-    if (draws) {
-        const long long budget = static_cast<long long>(di.l2 / kKeepDiv) / (static_cast<long long>(p.V) * EB);
-        const long long cand = (MODE == kLinearSample) ? 2ll * p.K * p.B : static_cast<long long>(p.B) * p.rows_per_seq;
-        p.keep_rows = static_cast<int>(std::min(budget, cand));
-    }
-    if (p.stats_segs + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxClaim >= (1ll << 31))
-        return fail(SPEC_ERR_UNSUPPORTED, "too many tiles (B=%d, V=%d)", p.B, p.V);
-    spec_verify_kernel<EB, MODE><<<static_cast<unsigned>(grid), kThreads, dyn, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return fail(SPEC_ERR_CUDA, "launch (grid=%lld, stages=%d, smem=%zu): %s", grid, ns, dyn,
-                    cudaGetErrorString(e));
-    return SPEC_OK;
-}
-
 bool valid_temperature(float T, float *c_out) {
     if (!(T >= 0.0f) || !std::isfinite(T)) return false;
     if (T == 0.0f) {
@@ -273,6 +202,14 @@ bool valid_dtype(spec_dtype dtype) { return dtype == SPEC_F32 || dtype == SPEC_B
 }  // namespace spec
 
 using namespace spec;
+
+#ifdef SPEC_TEST_HOOKS
+// Test builds only: the unit whose first partial the next launches withhold (-1: none), so
+// that a bounded wait runs out on purpose.
+extern "C" __attribute__((visibility("default"))) void spec_test_set_withhold(int unit) {
+    g_test_withhold.store(unit);
+}
+#endif
 
 extern "C" size_t spec_workspace_bytes_linear(int B, int K, int V, spec_dtype dtype) {
     if (B <= 0 || K < 0 || V < 1 || !valid_dtype(dtype)) return 0;

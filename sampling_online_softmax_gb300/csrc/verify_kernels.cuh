@@ -60,116 +60,11 @@
 #include <climits>
 #include <cstdint>
 
+#include "params.cuh"
 #include "ptx.cuh"
 #include "spec_verify.h"
 
 namespace spec {
-
-#ifndef SPEC_WARPS
-#define SPEC_WARPS 12
-#endif
-constexpr int kWarps = SPEC_WARPS;  // streaming warps per CTA
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxStages = 4;
-#ifndef SPEC_TILE_KB
-#define SPEC_TILE_KB 8
-#endif
-#ifndef SPEC_MIN_CTAS
-#define SPEC_MIN_CTAS 1
-#endif
-constexpr int kMinCtas = SPEC_MIN_CTAS;              // CTAs resident per SM
-constexpr int kTileBytes = SPEC_TILE_KB * 1024;      // stats tile: a window of one row on the 16-byte grid
-constexpr int kResidSliceBytes = kTileBytes / 2;     // at most this many bytes of each row per residual tile
-constexpr int kRowBuf = kResidSliceBytes + 64;       // residual row buffer: a slice plus its ragged groups
-constexpr int kStageBytes = 2 * kRowBuf;
-constexpr int kChunk = 64;                           // 16-byte groups per residual chunk
-constexpr int kCpt = (kResidSliceBytes / 16 + 2 + kChunk - 1) / kChunk;  // residual chunks per tile
-static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout");
-#ifndef SPEC_SEG_TILES
-#define SPEC_SEG_TILES 4
-#endif
-constexpr int kSegTiles = SPEC_SEG_TILES;  // stats tiles per segment: one partial each, never split between warps
-constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
-#ifndef SPEC_MAX_CLAIM
-#define SPEC_MAX_CLAIM 4
-#endif
-constexpr int kMaxClaim = SPEC_MAX_CLAIM;  // residual tiles claimed at once (at most)
-constexpr int kTailZone = 4;            // below this many segments per warp left, grab without reserve
-#ifndef SPEC_KEEP_DIV
-#define SPEC_KEEP_DIV 4
-#endif
-constexpr int kKeepDiv = SPEC_KEEP_DIV;  // rows kept in L2 for a residual pass: at most 1/kKeepDiv of L2
-constexpr int kEntWords = 32;           // a draw entry's record and counter share one 128-byte line of their own
-constexpr int kHold = 12;               // chunk sums per lane held in registers while an extra token is located
-constexpr long long kStaticTilesPerWarp = 32;  // up to this many stats tiles per warp: a static split
-constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kSpinLimit = 1u << 21;
-constexpr unsigned kFull = 0xffffffffu;
-
-enum Mode : int {
-    kLinearSample = 0,
-    kLinearGreedy = 1,
-    kTreeGreedy = 2,
-    kBonusSample = 3,
-    kBonusGreedy = 4,
-    kTreeSample = 5,  // tree walk with the target's choice drawn at every node
-};
-
-enum TileKind : int { kTileNone = 0, kTileStats = 1, kTileResid = 2 };
-
-// A draw entry: (unit + 1) | pair | skip.
-constexpr uint32_t kRecUnit = (1u << 30) - 1;
-constexpr uint32_t kRecPair = 1u << 30;  // weights max(0, p - q); else p
-constexpr uint32_t kRecSkip = 1u << 31;  // nothing to draw (non-finite row, bad length)
-
-struct Params {
-    const unsigned char *target;   // [B, t_rows, V]
-    const unsigned char *draft;    // [B, K, V] (sampling) or null
-    const unsigned char *t_end;    // one past the last byte of target
-    const unsigned char *d_end;    // one past the last byte of draft
-    int B, K, V;
-    int t_rows;                    // target rows per sequence: K+1 (linear), N (tree)
-    int rows_per_seq;              // row slots per sequence in the stats tiling
-    int units_per_seq;             // K+1 (linear), N (tree), 1 (extra token alone)
-    int n_units;
-    int S;                         // stats tiles per row (windows of kTileBytes on the 16-byte grid)
-    int nseg;                      // segments per row: ceil(S / kSegTiles) (dynamic mode)
-    int static_split;              // 1: warp w reduces stats tiles [T*w/W, T*(w+1)/W) (small problems)
-    long long stats_tiles;         // T = rows * S
-    int nwarps;                    // W = grid * kWarps
-    int keep_rows;                 // stats rows with id < keep_rows are read at normal L2 priority (the
-                                   // rest first-to-evict), so that a residual pass finds them in L2
-    int Sr, Lr;                    // residual slices per entry, elements per slice
-    int nstage;                    // stages per warp ring (2..kMaxStages)
-    long long stats_segs;          // B * rows_per_seq * nseg
-    long long res_tiles;           // (draw entries: B or 0) * Sr
-    float c;                       // log2(e) / T  (sampling modes)
-    const int32_t *tokens;         // [B, K] draft tokens, or [B, N] node tokens
-    const float *u_accept;         // [B, K]
-    const float *u_bonus;          // [B] or null
-    const int32_t *accept_len_in;  // [B] (extra token alone)
-    const int32_t *parents;        // [N] (tree)
-    int max_depth;                 // tree
-    int32_t *accept_len;           // [B] accept_len / path_len
-    int32_t *out_tokens;           // [B, K+1] or [B, max_depth+1]
-    int32_t *num_emitted;          // [B]
-    float *probs;                  // [B, K, 3] or null
-    int32_t *path_nodes;           // [B, max_depth+1]
-    int32_t *bonus_token;          // [B]
-    uint32_t *status;              // [1]
-    uint32_t *ws_ctrl;             // [0] stats segments taken, [1] CTAs finished, [2] draw entries, [3] residual tiles taken
-    uint32_t *ws_unit_cnt;         // [n_units] stats tiles published per unit
-    uint32_t *ws_seq_cnt;          // [B] units decided per sequence (K >= 32 and trees)
-    unsigned long long *ws_seqmask;  // [B] decided bits 0..31, accepted bits 32..63 (linear, K < 32)
-    int32_t *ws_acc;               // [B*K] accept bits
-    int32_t *ws_val;               // [B*units_per_seq] argmax per unit (greedy)
-    unsigned long long *ws_part;   // [n_units * 2 * S] run partials at the run's first tile: (mc | s << 32) or (max | (index + 1) << 32)
-    unsigned long long *ws_txw;    // [n_units * 2] the draft token's logit in each row: bits | 1 << 32
-    float4 *ws_stats;              // [n_units] (MCt, 1/St, MCd, 1/Sd) of units that may draw
-    uint32_t *ws_rq;               // draw entry e's record: ws_rq[e * kEntWords]
-    uint32_t *ws_res_cnt;          // its residual tiles counted: ws_res_cnt[e * kEntWords] (same line)
-    unsigned long long *ws_csum;   // [B * Sr * kCpt] residual chunk sums, stored plus one
-};
 
 // One stage's tile: {kTileStats, tile} or {kTileResid, residual tile, entry record}.
 struct __align__(16) WarpCtl {
@@ -252,10 +147,12 @@ __device__ __forceinline__ void fence_proxy_async() {
 // conversion rounds only weights below 2^-29.
 __device__ __forceinline__ long long fixq(float w) { return __float2ll_rn(w * 4503599627370496.0f); }
 
+// Every lane waits for the stage's copy; the answer is the warp's, so a wait
+// that gives up leaves the warp converged.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it)
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-    return false;
+    bool ok = false;
+    for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = ptx::mbar_try_wait(bar, parity);
+    return __all_sync(kFull, ok);
 }
 
 // ---- packed fp32 pairs (sm_100+ fma/add .f32x2)
@@ -1266,8 +1163,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 if (!has[r]) continue;
                 bool late = false;
                 if (w[r] == 0ull) w[r] = await64(slot[r], late);  // every run publishes once
-                if (late) {
-                    atomicOr(p.status, SPEC_DEV_TIMEOUT);
+                if (late) {  // reported (and the workspace cleared) at the end of the kernel
+                    timed_out = true;
                     continue;
                 }
                 *slot[r] = 0ull;
@@ -1307,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     bool late = false;
                     if (txw[0] == 0ull) txw[0] = await64(&txs[0], late);
                     if (txw[1] == 0ull) txw[1] = await64(&txs[1], late);
-                    if (late) fl |= SPEC_DEV_TIMEOUT;
+                    if (late) timed_out = true;
                     txs[0] = 0ull;
                     txs[1] = 0ull;
                     txv = make_float2(__uint_as_float(static_cast<unsigned>(txw[0])),
@@ -1442,7 +1339,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         const long long tot = __shfl_sync(kFull, incl, 31);
         if (__any_sync(kFull, late)) {
-            if (lane == 0) atomicOr(p.status, SPEC_DEV_TIMEOUT);
+            timed_out = true;
             return -1;
         }
         if (tot <= 0) return -1;
@@ -1633,6 +1530,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (lane == 0) {
             const uint2 part = T::kSample ? make_uint2(__float_as_uint(am), __float_as_uint(as))
                                           : make_uint2(__float_as_uint(am), static_cast<unsigned>(ai) + 1u);
+#ifdef SPEC_TEST_HOOKS
+            if (!(prow.unit == p.test_withhold && prow.r == 0 && run_k0 == 0))
+#endif
             st_relaxed64(&p.ws_part[(static_cast<size_t>(prow.unit) * 2 + prow.r) * S + run_k0],
                          static_cast<unsigned long long>(part.x) | (static_cast<unsigned long long>(part.y) << 32));
             if (hasx)
@@ -1810,16 +1710,38 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
     }
 
-    if (lane == 0 && timed_out) atomicOr(p.status, SPEC_DEV_TIMEOUT);
-    // ---- the last CTA to finish leaves the counters zeroed
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (atom_add_acq_rel(&p.ws_ctrl[1], 1u) == gridDim.x - 1) {
-            p.ws_ctrl[0] = 0u;
-            p.ws_ctrl[1] = 0u;
-            p.ws_ctrl[2] = 0u;
-            p.ws_ctrl[3] = 0u;
+    // A wait that gave up can leave bulk copies in flight into this warp's ring:
+    // let them land (each wait bounded again) before the CTA may exit.
+    while (handled < issued) {
+        (void)wait_bar(ptx::smem_addr(&wc.full[hslot]), hphase);
+        ++handled;
+        if (++hslot == NS) {
+            hslot = 0;
+            hphase ^= 1u;
         }
+    }
+    timed_out = __any_sync(kFull, timed_out);
+    if (lane == 0 && timed_out) {
+        atomicOr(p.status, SPEC_DEV_TIMEOUT);
+        atomicOr(&p.ws_ctrl[4], 1u);  // leftovers anywhere: the last CTA clears the whole workspace
+    }
+    // ---- the last CTA to finish leaves the workspace zeroed: the counters always,
+    //      everything else after a timed-out wait (whose values may have landed late,
+    //      or never been consumed)
+    __shared__ int s_last;
+    __threadfence();  // this CTA's workspace writes precede its count
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atom_add_acq_rel(&p.ws_ctrl[1], 1u) == gridDim.x - 1) ? 1 : 0;
+    __syncthreads();
+    if (s_last) {
+        if (__ldcg(&p.ws_ctrl[4]) != 0u) {
+            uint4 *w = reinterpret_cast<uint4 *>(p.ws_base + kCtrlWords * 4);
+            const unsigned long long n = (p.ws_bytes - kCtrlWords * 4) / 16;
+            for (unsigned long long i = threadIdx.x; i < n; i += blockDim.x) w[i] = make_uint4(0u, 0u, 0u, 0u);
+            __threadfence();
+        }
+        __syncthreads();
+        if (threadIdx.x < kCtrlWords) p.ws_ctrl[threadIdx.x] = 0u;
     }
 }
 

@@ -53,6 +53,19 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(raw, name), name
 
 
+def test_only_the_declared_entry_points_are_exported(lib):
+    """The library is built with hidden visibility: its exported spec_* symbols are
+    exactly the header's functions (no C++ internals a second copy could bind to)."""
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("no nm")
+    r = subprocess.run(["nm", "-D", "--defined-only", sv.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = sorted({ln.split()[-1] for ln in r.stdout.splitlines() if ln.split()[-1].startswith("spec_")})
+    assert exported == declared_functions()
+    assert not [ln for ln in r.stdout.splitlines() if "_ZN4spec" in ln]
+
+
 def test_status_strings(lib):
     for code in range(5):
         s = lib.spec_status_string(code).decode()

@@ -9,10 +9,11 @@ import bench
 import oracle
 
 
-@pytest.mark.parametrize("name", ["small", "small_greedy", "medusa_tree", "medusa_tree_sample", "medusa_tree_mask"])
-def test_extra_inputs_build_on_cpu(name):
-    w, T, kind, d = bench._extra_inputs(name, torch.device("cpu"))
-    assert kind == bench.EXTRA[name][2] and T == bench.EXTRA[name][1]
+@pytest.mark.parametrize("name", ["small_T1", "small_greedy", "medusa_tree_greedy", "medusa_tree_sampled_T1",
+                                  "medusa_tree_mask"])
+def test_config_inputs_build_on_cpu(name):
+    w, T, kind, d = bench.config_inputs(name, torch.device("cpu"))
+    assert kind == bench.CONFIGS[name][2] and T == bench.CONFIGS[name][1]
     if kind == "linear":
         assert tuple(d["target"].shape) == (w.B, w.K + 1, w.V)
     elif kind == "mask":
@@ -29,5 +30,35 @@ def test_extra_inputs_build_on_cpu(name):
             assert o["path_len"].max() >= 1
 
 
-def test_every_extra_name_has_a_kind():
-    assert set(k for _, _, k in bench.EXTRA.values()) <= {"linear", "tree", "tree_sample", "rows", "mask"}
+def test_every_config_name_has_a_kind_and_a_kernel():
+    kinds = set(k for _, _, k in bench.CONFIGS.values())
+    assert kinds <= set(bench.CONFIG_KERNELS)
+    assert set(bench.CONFIG_PROFILES) <= set(bench.CONFIGS)
+
+
+def test_clock_summary_reads_nvidia_smi_lines():
+    lines = ["0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 2055, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "0, 2070, 2070, 1250.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "garbage"]
+    s = bench.summarize_clocks(lines)
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert bench.summarize_clocks([])["samples"] == 0
+
+
+def test_small_config_parity_counts_on_the_cpu():
+    """The per-config parity leg: the oracle's own outputs compared with themselves are exact."""
+    w, T, kind, d = bench.config_inputs("small_T1", torch.device("cpu"))
+    h = {k: bench.to_oracle(v) for k, v in d.items() if hasattr(v, "detach")}
+    o = bench.oracle_call(kind, T, h, d)()
+    g = {k: o[k] for k in ("accept_len", "out_tokens", "num_emitted")}
+    p = bench.config_parity(kind, T, h, o, g)
+    assert p["exact"] == w.B and p["failures"] == 0
+
+
+def test_source_hash_covers_every_kernel_source():
+    import os
+    h1 = bench.kernel_source_hash()
+    assert len(h1) == 16 and int(h1, 16) >= 0
+    csrc = os.path.join(bench.ROOT, "sampling_online_softmax_gb300", "csrc")
+    assert any(f.startswith("kern_") for f in os.listdir(csrc))

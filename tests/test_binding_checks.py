@@ -4,7 +4,9 @@ Every binding checks dtypes and shapes before it hands pointers to the
 library, so that a short tensor raises instead of being read past its end on
 the device.  Here the CUDA-tensor check, the stream and the library are
 replaced by stand-ins, so the checks run without a GPU: valid calls must
-reach the library, and every mismatched shape must raise ValueError.
+reach the library, and every mismatched shape must raise ValueError.  Outputs the
+caller passes in (`out=`, `status=`, `workspace=`) are checked the same way:
+a short output would be written past its end on the device.
 """
 import contextlib
 import ctypes
@@ -29,8 +31,12 @@ def fake(monkeypatch):
     lib = FakeLib()
     monkeypatch.setattr(sv, "load_library", lambda: lib)
 
-    def cpu_cuda(t, name, dtype=None):
-        if t is not None and dtype is not None and t.dtype != dtype:
+    def cpu_cuda(t, name, dtype=None, device=None):
+        if t is None:
+            return None
+        if device is not None and t.device != device:
+            raise ValueError(name)
+        if dtype is not None and t.dtype != dtype:
             raise TypeError(name)
         return t
 
@@ -89,3 +95,78 @@ def test_rows_and_mask(fake):
         sv.spec_sample_rows(x, torch.zeros(B + 2), 1.0)
     with pytest.raises(TypeError):
         sv.spec_sample_rows(x, torch.zeros(B, dtype=torch.float64), 1.0)
+
+
+def _linear_args():
+    return (torch.zeros((B, K + 1, V)), torch.zeros((B, K, V)), torch.zeros((B, K), dtype=i32),
+            torch.zeros((B, K)), torch.zeros(B))
+
+
+def _linear_out(**over):
+    out = dict(accept_len=torch.zeros(B, dtype=i32), out_tokens=torch.zeros((B, K + 1), dtype=i32),
+               num_emitted=torch.zeros(B, dtype=i32))
+    out.update(over)
+    return out
+
+
+def test_linear_outputs_passed_in_are_checked(fake):
+    args = _linear_args()
+    st = torch.zeros(1, dtype=i32)
+    sv.spec_verify_linear(*args, 1.0, out=_linear_out(), status=st)
+    sv.spec_verify_linear_static(*args, 1.0, out=_linear_out(), status=st)
+    assert "spec_verify_linear_static" in fake
+    bad = [dict(accept_len=torch.zeros(B - 1, dtype=i32)), dict(out_tokens=torch.zeros((B, K), dtype=i32)),
+           dict(num_emitted=torch.zeros(B + 1, dtype=i32)), dict(probs=torch.zeros((B, K, 2))),
+           dict(out_tokens=None)]
+    for over in bad:
+        out = _linear_out(**over)
+        if over.get("out_tokens", 0) is None:
+            del out["out_tokens"]
+        for f in (sv.spec_verify_linear, sv.spec_verify_linear_static):
+            with pytest.raises(ValueError):
+                f(*args, 1.0, out=dict(out), status=st)
+    with pytest.raises(TypeError):
+        sv.spec_verify_linear(*args, 1.0, out=_linear_out(accept_len=torch.zeros(B, dtype=torch.int64)), status=st)
+    for f in (sv.spec_verify_linear, sv.spec_verify_linear_static):
+        with pytest.raises(ValueError):
+            f(*args, 1.0, out=_linear_out(), status=torch.zeros(0, dtype=i32))
+    with pytest.raises(ValueError):
+        sv.spec_verify_linear_static(*args, 1.0, out=_linear_out(), status=None)
+    with pytest.raises(ValueError):
+        sv.spec_verify_linear(*args, 1.0, workspace=torch.zeros(8, dtype=torch.uint8))
+
+
+def test_inputs_and_outputs_on_another_device_are_refused(fake):
+    """Every tensor must sit on the logits' device (here: a meta tensor stands for another device)."""
+    t, d, tok, ua, ub = _linear_args()
+    other = dict(tok=tok.to("meta"), ua=ua.to("meta"), ub=ub.to("meta"), d=d.to("meta"))
+    for k in other:
+        a = dict(d=d, tok=tok, ua=ua, ub=ub)
+        a[k] = other[k]
+        with pytest.raises(ValueError):
+            sv.spec_verify_linear(t, a["d"], a["tok"], a["ua"], a["ub"], 1.0)
+    with pytest.raises(ValueError):
+        sv.spec_verify_linear(t, d, tok, ua, ub, 1.0, out=_linear_out(num_emitted=torch.zeros(B, dtype=i32,
+                                                                                                device="meta")))
+
+
+def test_other_outputs_passed_in_are_checked(fake):
+    t, d, ub = torch.zeros((B, K + 1, V)), torch.zeros((B, K, V)), torch.zeros(B)
+    with pytest.raises(ValueError):
+        sv.spec_sample_bonus(t, d, torch.zeros(B, dtype=i32), ub, 1.0, out=torch.zeros(B - 1, dtype=i32))
+    tt, par, nt = torch.zeros((B, N, V)), torch.zeros(N, dtype=i32), torch.zeros((B, N), dtype=i32)
+    good = dict(path_nodes=torch.zeros((B, 4), dtype=i32), path_len=torch.zeros(B, dtype=i32),
+                out_tokens=torch.zeros((B, 4), dtype=i32))
+    sv.spec_verify_tree(tt, par, nt, 3, out=dict(good))
+    for k, shape in (("path_nodes", (B, 3)), ("path_len", (B + 1,)), ("out_tokens", (B, 5))):
+        out = dict(good)
+        out[k] = torch.zeros(shape, dtype=i32)
+        with pytest.raises(ValueError):
+            sv.spec_verify_tree(tt, par, nt, 3, out=out)
+        with pytest.raises(ValueError):
+            sv.spec_verify_tree_sample(tt, par, nt, torch.zeros((B, N)), 1.0, 3, out=out)
+    with pytest.raises(ValueError):
+        sv.spec_sample_rows(torch.zeros((B, V)), torch.zeros(B), 1.0, out=dict(tokens=torch.zeros(B + 1, dtype=i32)))
+    with pytest.raises(ValueError):
+        sv.spec_tree_mask(torch.zeros(N, dtype=i32), out=dict(mask=torch.zeros((N, 2), dtype=i32),
+                                                             depth=torch.zeros(N, dtype=i32)))

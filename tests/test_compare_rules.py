@@ -79,3 +79,32 @@ def test_sampled_tree_tie_only_on_a_path_node():
     u2 = np.array([[0.9, 0.9, 0.55, 0.1 + 3e-7]])
     assert not compare.compare_tree_sample(g, ora, u2).ok
     assert compare.compare_tree_sample(_tree([1], [[0, 2, -1]], [[4, 6, -1]]), ora, u2).exact == 1
+
+
+def test_sampled_tree_tie_only_at_the_node_where_the_walks_part():
+    """The walks share the root and node 1, then part: only node 1's draw may be a near tie.
+    A uniform at the root that sits on an interval edge, where the walks agreed, forgives
+    nothing (the looser rule counted any node on either path)."""
+    ora = _tree([2], [[0, 1, 5, -1]], [[10, 11, 12, -1]])
+    ora["node_cdf"] = np.zeros((1, 8, 2))
+    ora["node_cdf"][0, 0] = [0.3, 0.4]
+    ora["node_cdf"][0, 1] = [0.7, 0.8]
+    g = _tree([1], [[0, 1, -1, -1]], [[10, 13, -1, -1]])   # at node 1 the GPU drew a token no child carries
+    assert compare.compare_tree_sample(g, ora, np.array([[0.35, 0.8 - 2e-7, 0, 0, 0, 0, 0, 0]])).bonus_ties == 1
+    rep = compare.compare_tree_sample(g, ora, np.array([[0.3 + 1e-7, 0.75, 0, 0, 0, 0, 0, 0]]))
+    assert not rep.ok and "part at node 1" in rep.failures[0]
+    # the GPU walk goes further than the oracle's: the last shared node decides
+    g2 = _tree([3], [[0, 1, 5, 6]], [[10, 11, 12, 14]])
+    ora2 = dict(ora, path_len=np.array([2], np.int32))
+    ora2["node_cdf"][0, 5] = [0.2, 0.25]
+    assert compare.compare_tree_sample(g2, ora2, np.array([[0.5, 0.5, 0, 0, 0, 0.25 - 1e-7, 0, 0]])).bonus_ties == 1
+    assert not compare.compare_tree_sample(g2, ora2, np.array([[0.5, 0.7 + 1e-7, 0, 0, 0, 0.22, 0, 0]])).ok
+
+
+def test_every_report_is_logged_with_its_label():
+    compare.LABEL[0] = "unit-test-label"
+    n = len(compare.LOG)
+    ora = _tree([0], [[0, -1]], [[3, -1]])
+    compare.compare_tree(ora, ora)
+    assert len(compare.LOG) == n + 1 and compare.LOG[-1][0] == "unit-test-label" and compare.LOG[-1][1] == "tree"
+    compare.LOG.pop()
