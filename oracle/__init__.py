@@ -68,6 +68,8 @@ def _declare(lib):
     lib.oracle_sample_rows.restype = i32
     lib.oracle_tree_mask.argtypes = [P, i32, P, P]
     lib.oracle_tree_mask.restype = i32
+    lib.oracle_mtp_plug.argtypes = [P, i32, i32, P, P, ctypes.c_int32, P, P]
+    lib.oracle_mtp_plug.restype = i32
     lib.oracle_threads.argtypes = [i32]
     lib.oracle_threads.restype = i32
     return lib
@@ -231,3 +233,20 @@ def mask_bits(mask, N):
     """The bitmask as a dense [N, N] 0/1 array."""
     bits = np.unpackbits(np.ascontiguousarray(mask).view(np.uint8), axis=1, bitorder="little")
     return bits[:, :N]
+
+
+def mtp_plug(in_tokens, out_tokens, num_emitted, pad=0, seq_lens=None, lib=None):
+    """MTP token plug-in: the draft's next input tokens from the target's input
+    tokens [B, K+1] and a linear verify's out_tokens [B, K+1] and num_emitted [B].
+    Returns dict(next_tokens [B, K+1], seq_lens [B] or None, bad)."""
+    lib = lib or load()
+    inp = np.ascontiguousarray(in_tokens, dtype=np.int32)
+    B, W = inp.shape
+    ot = np.ascontiguousarray(out_tokens, dtype=np.int32).reshape(B, W)
+    ne = np.ascontiguousarray(num_emitted, dtype=np.int32).reshape(B)
+    nxt = np.zeros((B, W), np.int32)
+    sl = None if seq_lens is None else np.array(seq_lens, dtype=np.int32).reshape(B)
+    rc = lib.oracle_mtp_plug(_ptr(inp), B, W - 1, _ptr(ot), _ptr(ne), int(pad), _ptr(nxt), _ptr(sl))
+    if rc == 1:
+        raise ValueError("oracle_mtp_plug rejected its arguments")
+    return dict(next_tokens=nxt, seq_lens=sl, bad=rc == 2)

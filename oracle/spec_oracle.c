@@ -50,6 +50,20 @@
  *     which no token attends to a token of another path): row i holds node
  *     i and every ancestor of node i; depth[i] is the number of edges from
  *     the root (the token's offset in position).
+ *   - MTP token plug-in ("Beschleunigung von Sonar durch Spekulation",
+ *     sections "MTP" and "MTP-Zeitplan für ein einzelnes Token"): the draft
+ *     layer at position i reads the target's hidden state H_i together with
+ *     the token that follows position i, so its input tokens are the target's
+ *     input tokens of the step shifted left by one; after verification a
+ *     kernel writes the target's next tokens into their places, and the
+ *     draft runs over the same positions as the target (work past the
+ *     accepted prefix is redundant).  Reading: row b of the target's input is
+ *     (the token the step started from, x_0 .. x_{K-1}); the draft's input row
+ *     is next[i] = in[i + 1] for i < K and next[K] = pad, and then the n_b
+ *     emitted tokens (x_0 .. x_{j-1} and the extra token) overwrite positions
+ *     0 .. n_b - 1; the sequence length grows by n_b, on the device, with no
+ *     host round trip.  A count outside [0, K + 1] leaves the row shifted,
+ *     the length unchanged, and is reported.
  *   - tree, sampling mode (the page's "Greedy或者Sampling"): the target's
  *     choice at node n is a draw from softmax(target_n / T) by inverse CDF
  *     with the caller's uniform u[b, n]; the walk is the greedy walk with that
@@ -461,6 +475,36 @@ int oracle_tree_mask(const int32_t *parents, int N, uint32_t *mask, int32_t *dep
             mask[(size_t)i * W + cur / 32] |= 1u << (cur % 32);
         }
         depth[i] = d;
+    }
+    return bad ? 2 : 0;
+}
+
+/*
+ * MTP token plug-in (see the reading above).  in_tokens [B, K+1], out_tokens
+ * [B, K+1] and num_emitted [B] (a linear verify's outputs), pad: the token
+ * written at the last position when nothing is shifted into it.
+ * Outputs: next_tokens [B, K+1]; seq_lens [B] (incremented in place; NULL to
+ * skip).  Returns 0, or 2 if some num_emitted[b] was outside [0, K + 1].
+ */
+int oracle_mtp_plug(const int32_t *in_tokens, int B, int K, const int32_t *out_tokens, const int32_t *num_emitted,
+                    int32_t pad, int32_t *next_tokens, int32_t *seq_lens) {
+    if (B < 0 || K < 0) return 1;
+    const int W = K + 1;
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *in = in_tokens + (size_t)b * W;
+        int32_t *nx = next_tokens + (size_t)b * W;
+        /* shift left by one: position i takes the token that follows it */
+        for (int i = 0; i < K; ++i) nx[i] = in[i + 1];
+        nx[K] = pad;
+        const int n = num_emitted[b];
+        if (n < 0 || n > W) {
+            bad = 1;
+            continue;
+        }
+        /* the target's next tokens go to their places */
+        for (int i = 0; i < n; ++i) nx[i] = out_tokens[(size_t)b * W + i];
+        if (seq_lens) seq_lens[b] += n;
     }
     return bad ? 2 : 0;
 }

@@ -18,6 +18,7 @@ import test_oracle_pins as pins
 import test_tree_pins as tpins
 import test_row_sampler_pins as rpins
 import test_tree_sample_pins as spins
+import test_mtp_pins as mpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
 
@@ -108,6 +109,16 @@ MUTANTS = [
     ("mask_one_level_only", "            cur = par;\n            ++d;", "            cur = par;\n            ++d;\n            if (d > 1) break;"),
     ("tree_sample_row_of_root", "softmax_row(target, dtype, (size_t)b * N + n, V, T, p, NULL, NULL);",
      "softmax_row(target, dtype, (size_t)b * N, V, T, p, NULL, NULL);"),
+    ("mtp_no_shift", "for (int i = 0; i < K; ++i) nx[i] = in[i + 1];", "for (int i = 0; i < K; ++i) nx[i] = in[i];"),
+    ("mtp_shift_right", "for (int i = 0; i < K; ++i) nx[i] = in[i + 1];",
+     "for (int i = 1; i <= K; ++i) nx[i] = in[i - 1];"),
+    ("mtp_pad_first", "        nx[K] = pad;", "        nx[0] = pad;"),
+    ("mtp_plug_one_short", "for (int i = 0; i < n; ++i) nx[i] = out_tokens[(size_t)b * W + i];",
+     "for (int i = 0; i + 1 < n; ++i) nx[i] = out_tokens[(size_t)b * W + i];"),
+    ("mtp_plug_one_place_late", "for (int i = 0; i < n; ++i) nx[i] = out_tokens[(size_t)b * W + i];",
+     "for (int i = 0; i < n && i < K; ++i) nx[i + 1] = out_tokens[(size_t)b * W + i];"),
+    ("mtp_length_without_extra", "        if (seq_lens) seq_lens[b] += n;", "        if (seq_lens) seq_lens[b] += n > 0 ? n - 1 : 0;"),
+    ("mtp_plug_from_row_zero", "nx[i] = out_tokens[(size_t)b * W + i];", "nx[i] = out_tokens[i];"),
 ]
 
 
@@ -138,6 +149,11 @@ def _pin_suite(lib):
         ("rows_freq", lambda: rpins.check_frequencies(lib, V=5, T=0.7, M=5000)),
         ("rows_greedy", lambda: rpins.check_greedy_is_argmax(lib)),
         ("rows_scaling", lambda: rpins.check_temperature_scaling(lib)),
+        ("mtp_single", lambda: mpins.check_hand_worked_single_token(lib)),
+        ("mtp_k2", lambda: mpins.check_hand_worked_k2(lib)),
+        ("mtp_align", lambda: mpins.check_alignment_with_decoded_sequences(lib)),
+        ("mtp_shift", lambda: mpins.check_nothing_emitted_is_the_shift(lib)),
+        ("mtp_range", lambda: mpins.check_counts_out_of_range(lib)),
     ]
     for name, fn in checks:
         try:
