@@ -70,6 +70,8 @@ def _declare(lib):
     lib.oracle_tree_mask.restype = i32
     lib.oracle_mtp_plug.argtypes = [P, i32, i32, P, P, ctypes.c_int32, P, P]
     lib.oracle_mtp_plug.restype = i32
+    lib.oracle_build_sparse_tree.argtypes = [P, i32, i32, i32, P, P, P, P, P]
+    lib.oracle_build_sparse_tree.restype = i32
     lib.oracle_threads.argtypes = [i32]
     lib.oracle_threads.restype = i32
     return lib
@@ -250,3 +252,23 @@ def mtp_plug(in_tokens, out_tokens, num_emitted, pad=0, seq_lens=None, lib=None)
     if rc == 1:
         raise ValueError("oracle_mtp_plug rejected its arguments")
     return dict(next_tokens=nxt, seq_lens=sl, bad=rc == 2)
+
+
+def build_sparse_tree(accuracy, n_nodes, lib=None):
+    """Greedy sparse candidate tree from an accuracy table [K, S] (a_k^(i) at [k-1, i-1]) with
+    n_nodes nodes (root included; fewer when the full tree is smaller).
+    Returns dict(parents, depth, rank, expected_len)."""
+    lib = lib or load()
+    acc = np.ascontiguousarray(accuracy, dtype=np.float64)
+    K, S = acc.shape
+    par = np.zeros(n_nodes, np.int32)
+    dep = np.zeros(n_nodes, np.int32)
+    rk = np.zeros(n_nodes, np.int32)
+    nb = ctypes.c_int(0)
+    el = ctypes.c_double(0.0)
+    rc = lib.oracle_build_sparse_tree(_ptr(acc), K, S, int(n_nodes), _ptr(par), _ptr(dep), _ptr(rk),
+                                      ctypes.byref(nb), ctypes.byref(el))
+    if rc != 0:
+        raise ValueError("oracle_build_sparse_tree rejected its arguments")
+    n = nb.value
+    return dict(parents=par[:n], depth=dep[:n], rank=rk[:n], expected_len=el.value)

@@ -64,6 +64,17 @@
  *     0 .. n_b - 1; the sequence length grows by n_b, on the device, with no
  *     host round trip.  A count outside [0, K + 1] leaves the row shifted,
  *     the length unchanged, and is reported.
+ *   - sparse candidate tree ("Speculative-Decoding / Medusa" blog, section
+ *     四): with a_k^(i) the accuracy of head k's i-th ranked token, taken as
+ *     independent, the node reached by the rank path [i_1 .. i_m] is accepted
+ *     with probability prod_j a_j^(i_j), E[L] is the sum of that product over
+ *     the tree's non-root nodes, and the tree is grown from the root by adding,
+ *     one node at a time, the candidate (a child of a node already in the
+ *     tree) whose product is largest, up to a fixed node count.  Readings:
+ *     the product is taken left to right from 1; equal products go to the
+ *     smaller depth, then to the lexicographically smaller rank path; nodes
+ *     are numbered by (depth, rank path), so every parent precedes its
+ *     children; a node count above the full tree's size gives the full tree.
  *   - tree, sampling mode (the page's "Greedy或者Sampling"): the target's
  *     choice at node n is a draw from softmax(target_n / T) by inverse CDF
  *     with the caller's uniform u[b, n]; the walk is the greedy walk with that
@@ -507,6 +518,106 @@ int oracle_mtp_plug(const int32_t *in_tokens, int B, int K, const int32_t *out_t
         if (seq_lens) seq_lens[b] += n;
     }
     return bad ? 2 : 0;
+}
+
+/* prod_j a_j^(i_j) along a rank path, left to right from 1 (a: [K][S], ranks 1-based). */
+static double path_product(const double *acc, int S, const int *path, int m) {
+    double v = 1.0;
+    for (int j = 0; j < m; ++j) v *= acc[(size_t)j * S + (path[j] - 1)];
+    return v;
+}
+
+/* Is rank path a (length ma) before rank path b (length mb) in (depth, lexicographic) order? */
+static int path_before(const int *a, int ma, const int *b, int mb) {
+    if (ma != mb) return ma < mb;
+    for (int j = 0; j < ma; ++j)
+        if (a[j] != b[j]) return a[j] < b[j];
+    return 0;
+}
+
+/*
+ * Greedy sparse tree (see the reading above).  acc [K * S]: acc[(k-1) * S +
+ * (i-1)] = a_k^(i).  n_nodes >= 1 counts the root.  Outputs (n_nodes entries,
+ * the first *n_built used): parents (parents[0] = -1), depth, rank (1-based,
+ * 0 for the root); *expected_len = E[L].  Returns 0 or 1 (bad arguments).
+ */
+int oracle_build_sparse_tree(const double *acc, int K, int S, int n_nodes, int32_t *parents, int32_t *depth,
+                             int32_t *rank, int *n_built, double *expected_len) {
+    if (K < 1 || S < 1 || n_nodes < 1) return 1;
+    /* chosen rank paths, K ints each; the root is the empty path */
+    int *paths = (int *)calloc((size_t)n_nodes * K, sizeof(int));
+    int *len = (int *)calloc((size_t)n_nodes, sizeof(int));
+    int *cand = (int *)malloc(sizeof(int) * (size_t)K);
+    int *best = (int *)malloc(sizeof(int) * (size_t)K);
+    int n = 1;
+    while (n < n_nodes) {
+        int found = 0, best_m = 0;
+        double best_v = 0.0;
+        /* every child of every chosen node that is not chosen yet */
+        for (int p = 0; p < n; ++p) {
+            const int m = len[p];
+            if (m >= K) continue;
+            for (int i = 1; i <= S; ++i) {
+                memcpy(cand, paths + (size_t)p * K, sizeof(int) * (size_t)m);
+                cand[m] = i;
+                int taken = 0;
+                for (int q = 0; q < n && !taken; ++q)
+                    if (len[q] == m + 1 && memcmp(paths + (size_t)q * K, cand, sizeof(int) * (size_t)(m + 1)) == 0)
+                        taken = 1;
+                if (taken) continue;
+                const double v = path_product(acc, S, cand, m + 1);
+                if (!found || v > best_v || (v == best_v && path_before(cand, m + 1, best, best_m))) {
+                    found = 1;
+                    best_v = v;
+                    best_m = m + 1;
+                    memcpy(best, cand, sizeof(int) * (size_t)best_m);
+                }
+            }
+        }
+        if (!found) break; /* the full tree is smaller than n_nodes */
+        memcpy(paths + (size_t)n * K, best, sizeof(int) * (size_t)best_m);
+        len[n] = best_m;
+        ++n;
+    }
+    /* number the nodes by (depth, rank path): a selection sort into order[] */
+    int *order = (int *)malloc(sizeof(int) * (size_t)n);
+    int *used = (int *)calloc((size_t)n, sizeof(int));
+    for (int r = 0; r < n; ++r) {
+        int pick = -1;
+        for (int q = 0; q < n; ++q)
+            if (!used[q] && (pick < 0 || path_before(paths + (size_t)q * K, len[q], paths + (size_t)pick * K, len[pick])))
+                pick = q;
+        used[pick] = 1;
+        order[r] = pick;
+    }
+    double e = 0.0;
+    for (int r = 0; r < n; ++r) {
+        const int q = order[r];
+        const int m = len[q];
+        depth[r] = m;
+        rank[r] = m > 0 ? paths[(size_t)q * K + m - 1] : 0;
+        parents[r] = -1;
+        if (m > 0) {
+            /* the parent is the chosen node whose path is this one without its last rank */
+            for (int t = 0; t < r; ++t) {
+                const int pq = order[t];
+                if (len[pq] == m - 1 && memcmp(paths + (size_t)pq * K, paths + (size_t)q * K, sizeof(int) * (size_t)(m - 1)) == 0) {
+                    parents[r] = t;
+                    break;
+                }
+            }
+            e += path_product(acc, S, paths + (size_t)q * K, m);
+        }
+    }
+    *n_built = n;
+    if (expected_len) *expected_len = e;
+    free(paths);
+    free(len);
+    free(cand);
+    free(best);
+    free(order);
+    free(used);
+    return 0;
 }
 
 /* Number of OpenMP threads the oracle runs with; n > 0 sets it first. */

@@ -19,6 +19,7 @@ import test_tree_pins as tpins
 import test_row_sampler_pins as rpins
 import test_tree_sample_pins as spins
 import test_mtp_pins as mpins
+import test_tree_builder_pins as bpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
 
@@ -119,6 +120,16 @@ MUTANTS = [
      "for (int i = 0; i < n && i < K; ++i) nx[i + 1] = out_tokens[(size_t)b * W + i];"),
     ("mtp_length_without_extra", "        if (seq_lens) seq_lens[b] += n;", "        if (seq_lens) seq_lens[b] += n > 0 ? n - 1 : 0;"),
     ("mtp_plug_from_row_zero", "nx[i] = out_tokens[(size_t)b * W + i];", "nx[i] = out_tokens[i];"),
+    ("builder_ties_to_deeper", "    if (ma != mb) return ma < mb;", "    if (ma != mb) return ma > mb;"),
+    ("builder_ties_to_larger_rank", "        if (a[j] != b[j]) return a[j] < b[j];", "        if (a[j] != b[j]) return a[j] > b[j];"),
+    ("builder_last_factor_dropped", "    for (int j = 0; j < m; ++j) v *= acc[(size_t)j * S + (path[j] - 1)];",
+     "    for (int j = 0; j + 1 < m; ++j) v *= acc[(size_t)j * S + (path[j] - 1)];"),
+    ("builder_heads_reversed", "    for (int j = 0; j < m; ++j) v *= acc[(size_t)j * S + (path[j] - 1)];",
+     "    for (int j = 0; j < m; ++j) v *= acc[(size_t)(m - 1 - j) * S + (path[j] - 1)];"),
+    ("builder_smallest_first", "if (!found || v > best_v ||", "if (!found || v < best_v ||"),
+    ("builder_parent_is_root", "                    parents[r] = t;", "                    parents[r] = 0;"),
+    ("builder_expected_len_first_level", "            e += path_product(acc, S, paths + (size_t)q * K, m);",
+     "            e += path_product(acc, S, paths + (size_t)q * K, 1);"),
 ]
 
 
@@ -154,11 +165,18 @@ def _pin_suite(lib):
         ("mtp_align", lambda: mpins.check_alignment_with_decoded_sequences(lib)),
         ("mtp_shift", lambda: mpins.check_nothing_emitted_is_the_shift(lib)),
         ("mtp_range", lambda: mpins.check_counts_out_of_range(lib)),
+        ("builder_count", lambda: bpins.check_post_node_count(lib)),
+        ("builder_full", lambda: bpins.check_full_tree_counts(lib)),
+        ("builder_brute", lambda: bpins.check_optimal_by_brute_force(lib, 2, 3, 4, 0)),
+        ("builder_brute2", lambda: bpins.check_optimal_by_brute_force(lib, 3, 3, 5, 3)),
+        ("builder_chain", lambda: bpins.check_chain_closed_form(lib)),
+        ("builder_ties", lambda: bpins.check_exact_ties_order(lib)),
+        ("builder_dominate", lambda: bpins.check_chosen_dominate_candidates(lib)),
     ]
     for name, fn in checks:
         try:
             fn()
-        except AssertionError:
+        except Exception:  # a failed assertion, or a pin that cannot even read the mutant's output
             failed.append(name)
     return failed
 
