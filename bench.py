@@ -440,6 +440,8 @@ CONFIGS = {
     "draft_sampler_T0.7": (2, 0.7, "rows"),
     "draft_sampler_greedy": (2, 0.0, "rows"),
     "medusa_tree_mask": (4, 0.0, "mask"),
+    "mtp_plug_T1": (3, 1.0, "plug"),
+    "medusa_tree_build": (4, 0.0, "build"),
 }
 # committed ncu summaries (profiles/) behind each configuration's traffic figure
 CONFIG_PROFILES = {
@@ -451,6 +453,7 @@ CONFIG_PROFILES = {
     "medusa_tree_sampled_T1": "spec_verify_kernel_tree_sample_medusa.md",
     "draft_sampler_T0.7": "spec_verify_kernel_bonus_sample_draft_rows.md",
     "medusa_tree_mask": "tree_mask_kernel_medusa.md",
+    "mtp_plug_T1": "mtp_plug_kernel_mtp.md",
 }
 CONFIG_KERNELS = {
     "linear": "spec_verify_kernel<EB, kLinearSample or kLinearGreedy>",
@@ -458,6 +461,8 @@ CONFIG_KERNELS = {
     "tree_sample": "spec_verify_kernel<4, kTreeSample>",
     "rows": "spec_verify_kernel<2, kBonusSample or kBonusGreedy>",
     "mask": "tree_mask_kernel",
+    "plug": "mtp_plug_kernel",
+    "build": "spec_build_sparse_tree (host)",
 }
 
 
@@ -472,6 +477,18 @@ def config_inputs(name, dev):
         return w, T, kind, make_linear(number, T, device=dev)
     if kind == "mask":
         return w, T, kind, dict(parents=make_tree(number, device=dev, B=1, V=64)["parents"])
+    if kind == "plug":
+        # a T=1 verify of the MTP workload supplies the plug-in's inputs (made once, not timed)
+        import sampling_online_softmax_gb300 as sv
+        lin = make_linear(number, T, device=dev)
+        r = sv.spec_verify_linear(lin["target"], lin["draft"], lin["draft_tokens"], lin["u_accept"], lin["u_bonus"], T)
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed + 29)
+        start = torch.randint(0, w.V, (w.B, 1), generator=g, device=dev, dtype=torch.int32)
+        torch.cuda.synchronize()
+        return w, T, kind, dict(in_tokens=torch.cat([start, lin["draft_tokens"]], dim=1).contiguous(),
+                                out_tokens=r["out_tokens"], num_emitted=r["num_emitted"],
+                                seq_lens=torch.randint(1, 4000, (w.B,), generator=g, device=dev, dtype=torch.int32))
     if kind == "rows":
         lin = make_linear(number, max(T, 0.7), device=dev)
         return w, T, kind, dict(rows=lin["draft"][:, 0].contiguous(), u=lin["u_bonus"])
@@ -503,6 +520,9 @@ def config_bytes(w, T, kind, d):
         return 4 * n * ((n + 31) // 32 + 2)  # mask words written, parents read, depths written
     if kind == "rows":
         return d["rows"].numel() * d["rows"].element_size()
+    if kind == "plug":
+        B, W = d["in_tokens"].shape
+        return 4 * B * (3 * W + 3)  # in, out_tokens, num_emitted, lengths read; next tokens, lengths written
     return w.logits_bytes(T)
 
 
@@ -510,6 +530,10 @@ def make_call(sv, kind, w, T, c, dev, stream, status):
     """A closure that launches one call of this configuration on `stream`, and its outputs."""
     import torch
     B = w.B
+    if kind == "plug":
+        out = torch.empty_like(c["in_tokens"])
+        return (lambda: sv.spec_mtp_plug(c["in_tokens"], c["out_tokens"], c["num_emitted"], 0, c["seq_lens"],
+                                         out=out, status=status, stream=stream)), dict(next_tokens=out)
     if kind == "mask":
         n = c["parents"].numel()
         out = dict(mask=torch.empty((n, (n + 31) // 32), dtype=torch.int32, device=dev),
@@ -546,6 +570,8 @@ def make_call(sv, kind, w, T, c, dev, stream, status):
 def oracle_call(kind, T, h, d):
     """The oracle on host copies h of one configuration's inputs."""
     import oracle
+    if kind == "plug":
+        return lambda: oracle.mtp_plug(h["in_tokens"], h["out_tokens"], h["num_emitted"], 0, None)
     if kind == "mask":
         return lambda: oracle.tree_mask(h["parents"])
     if kind == "rows":
@@ -572,6 +598,9 @@ def config_parity(kind, T, h, o, g):
     if kind == "rows":
         rep = compare.compare_rows(g["tokens"], o, h["u"] if T > 0 else None, T)
         return parity_dict(rep)
+    if kind == "plug":
+        eq = np.all(g["next_tokens"] == o["next_tokens"], axis=1)
+        return {"sequences": int(len(eq)), "exact": int(eq.sum()), "failures": int((~eq).sum())}
     same = bool(np.array_equal(g["mask"].view(np.uint32), o["mask"]) and np.array_equal(g["depth"], o["depth"]))
     return {"rows": int(len(o["depth"])), "exact": same, "failures": 0 if same else 1}
 
@@ -588,9 +617,55 @@ def time_oracle(f, seconds, cores):
             return n, el
 
 
+def run_build_config(args, name, in_line=False):
+    """The sparse-tree builder runs on the host: trees per second, the oracle's builder beside it,
+    and node-for-node parity of the two trees."""
+    import numpy as np
+
+    import oracle
+    import sampling_online_softmax_gb300 as sv
+    from workloads import WORKLOADS, medusa_tree
+    w = WORKLOADS[CONFIGS[name][0]]
+    acc = np.array([[medusa_tree.synthetic_accuracy(k, i) for i in range(1, 9)] for k in range(1, w.K + 1)])
+    n_nodes = w.N
+
+    def timed(f, seconds):
+        f()
+        n, c0 = 0, time.perf_counter()
+        while True:
+            f()
+            n += 1
+            el = time.perf_counter() - c0
+            if el >= seconds:
+                return n / el
+
+    rate = timed(lambda: sv.spec_build_sparse_tree(acc, n_nodes), 0.5)
+    got = sv.spec_build_sparse_tree(acc, n_nodes)
+    cpu = parity = None
+    if not args.no_cpu_baseline:
+        want = oracle.build_sparse_tree(acc, n_nodes)
+        eq = all(np.array_equal(got[k], want[k]) for k in ("parents", "depth", "rank"))
+        parity = {"nodes": int(len(want["parents"])), "exact": bool(eq), "failures": 0 if eq else 1,
+                  "expected_len": want["expected_len"]}
+        cpu = {"value": timed(lambda: oracle.build_sparse_tree(acc, n_nodes), args.config_cpu_seconds),
+               "unit": "trees/s", "cores": 1, "kind": "oracle",
+               "sample": "the %d-node tree of the %dx8 accuracy table, repeated" % (n_nodes, w.K)}
+    entry = {"us_per_call": 1e6 / rate, "value": rate, "unit": "trees/s",
+             "timing": "host code (the tree is built once per accuracy table, not per step), wall clock",
+             "config": {"workload": name, "K": w.K, "S": 8, "n_nodes": n_nodes,
+                        "accuracy": "a_k^(i) = 0.6 * 0.8^k * 0.5^i"},
+             "roofline": None, "clocks": None, "cpu_baseline": cpu, "parity": parity}
+    if not in_line:
+        entry.update({"metric": "sparse candidate trees built per second (host)", "higher_is_better": True})
+        print(json.dumps(entry), flush=True)
+    return entry
+
+
 def run_config(args, name, in_line=False):
     """One configuration, the kernel alone, replayed from a CUDA graph; clocks, roofline, oracle beside it."""
     import torch
+    if CONFIGS[name][2] == "build":
+        return run_build_config(args, name, in_line)
 
     import sampling_online_softmax_gb300 as sv
     dev = torch.device("cuda", 0)
@@ -598,7 +673,8 @@ def run_config(args, name, in_line=False):
     w, T, kind, d = config_inputs(name, dev)
     bytes_per_step = config_bytes(w, T, kind, d)
     rotate = max(1, min(4, int(2 * L2_BYTES // bytes_per_step) + 1))   # more than L2 over the copies
-    keys = {"linear": ("target", "draft"), "rows": ("rows",), "mask": ("parents",)}.get(kind, ("target",))
+    keys = {"linear": ("target", "draft"), "rows": ("rows",), "mask": ("parents",),
+            "plug": ("in_tokens", "out_tokens")}.get(kind, ("target",))
     copies = [d] + [dict(d, **{k: d[k].clone() for k in keys if d.get(k) is not None}) for _ in range(rotate - 1)]
     B = 1 if kind == "mask" else w.B     # the mask is one per tree, shared by the batch
     unit = "masks/s" if kind == "mask" else "seqs/s"

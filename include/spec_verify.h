@@ -93,7 +93,8 @@ typedef enum spec_dtype {
 #define SPEC_DEV_TIMEOUT       4u  /* a bounded wait (a copy, or a value another warp publishes) gave up; outputs unspecified, workspace cleared */
 #define SPEC_DEV_ZERO_RESIDUAL 8u  /* residual weight W == 0 at a rejection: drew from p_j instead */
 #define SPEC_DEV_BAD_TREE     16u  /* parents[] not topological (0 <= parents[c] < c): edge ignored */
-#define SPEC_DEV_BAD_LENGTH   32u  /* spec_sample_bonus: accept_len[b] outside [0, K]; token -1 */
+#define SPEC_DEV_BAD_LENGTH   32u  /* spec_sample_bonus: accept_len[b] outside [0, K] (token -1);
+                                      spec_mtp_plug: num_emitted[b] outside [0, K+1] */
 
 /* Bytes of workspace spec_verify_linear needs for B sequences of K draft
  * tokens over a vocabulary of V logits of `dtype` (0 for invalid sizes). */
@@ -237,6 +238,71 @@ SPEC_API spec_status spec_verify_tree_sample(const void *target_logits, spec_dty
  */
 SPEC_API spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *mask_words, int32_t *depth, uint32_t *dev_status,
                            void *stream);
+
+/*
+ * Sparse candidate tree ("Speculative-Decoding / Medusa" blog, section 四,
+ * optimized tree construction).  With a_k^(i) the accuracy of head k's i-th
+ * ranked token (taken as independent), the node reached by the rank path
+ * [i_1 .. i_m] is accepted with probability prod_j a_j^(i_j), and E[L] is the
+ * sum of that product over the tree's non-root nodes.  The tree grows from
+ * the root one node at a time by the candidate (a child of a node already in
+ * the tree) of largest product, until it holds n_nodes nodes or no candidate
+ * is left.  Equal products go to the smaller depth, then to the
+ * lexicographically smaller rank path.  Nodes are numbered by (depth, rank
+ * path), so 0 <= parents[c] < c and the result feeds spec_tree_mask and
+ * spec_verify_tree / spec_verify_tree_sample as it is.
+ *
+ * Unlike every other entry point this one runs on the HOST (all pointers are
+ * host memory, no stream): the tree has a few dozen nodes and is built once
+ * per accuracy table, not per decode step.
+ *   accuracy     [K * S] double: accuracy[(k-1) * S + (i-1)] = a_k^(i), in [0, 1].
+ *   K            heads (the tree's depth limit), 1 <= K <= 64.
+ *   S            ranked tokens per head, 1 <= S <= 4096.
+ *   n_nodes      nodes wanted, the root included, 1 <= n_nodes <= 16384.
+ * Outputs (n_nodes entries each; the first *n_built are written):
+ *   parents      parents[0] = -1, else the parent's number.
+ *   depth        the node's depth (0 for the root).
+ *   rank         the rank i of the node's token among its head's candidates
+ *                (1-based; 0 for the root).
+ *   n_built      min(n_nodes, the full tree's size).
+ *   expected_len E[L] of the tree, or NULL.
+ * Errors: SPEC_ERR_INVALID_ARG for sizes out of range, a null pointer, or an
+ * accuracy that is not a finite value in [0, 1].
+ */
+SPEC_API spec_status spec_build_sparse_tree(const double *accuracy, int K, int S, int n_nodes, int32_t *parents,
+                                            int32_t *depth, int32_t *rank, int *n_built, double *expected_len);
+
+/*
+ * MTP token plug-in ("Beschleunigung von Sonar durch Spekulation", sections
+ * "MTP" and "MTP-Zeitplan für ein einzelnes Token"): the draft layer at
+ * position i reads the target's hidden state H_i with the token that follows
+ * position i, so its input is the target's input shifted left by one; after
+ * verification the target's next tokens go into their places on the device,
+ * and the sequence lengths advance, with no host round trip.
+ *
+ *   in_tokens   [B, K+1] int32  the target's input tokens of the step: row b is
+ *                               (the token the step started from, x_0 .. x_{K-1});
+ *                               for single-token MTP (K = 1) these are the 2 * B
+ *                               tokens the target scored.
+ *   out_tokens  [B, K+1] int32  spec_verify_linear's out_tokens (accepted draft
+ *                               tokens, then the extra token).
+ *   num_emitted [B] int32       spec_verify_linear's num_emitted.
+ *   pad                         the token written at position K when nothing is
+ *                               shifted into it (only when fewer than K + 1 tokens
+ *                               were emitted).
+ * Outputs (device, caller-owned):
+ *   next_tokens [B, K+1] int32  next[b, i] = out_tokens[b, i] for i < n_b, else
+ *                               in_tokens[b, i + 1] for i < K, else pad; it may be
+ *                               in_tokens itself (in place), but not out_tokens.
+ *   seq_lens    [B] int32       incremented by num_emitted[b] in place; NULL to skip.
+ *   dev_status  [1]             SPEC_DEV_BAD_LENGTH when num_emitted[b] is outside
+ *                               [0, K+1] (that row is only shifted, its length unchanged).
+ * B >= 0, K >= 0, every pointer 4-byte aligned.  No workspace; one small launch
+ * (one warp per sequence), ordered after the verify on the same stream.
+ */
+SPEC_API spec_status spec_mtp_plug(const int32_t *in_tokens, int B, int K, const int32_t *out_tokens,
+                                   const int32_t *num_emitted, int32_t pad, int32_t *next_tokens,
+                                   int32_t *seq_lens, uint32_t *dev_status, void *stream);
 
 /*
  * spec_verify_linear with the library's own workspace.  The pages describe no

@@ -18,6 +18,12 @@ Entry points (same names as the C ABI):
                        every node (the section's sampled variant)
   spec_sample_rows     one token per row (the draft side's next token)
   spec_tree_mask       the tree attention mask (ancestor bits) and depths
+  spec_build_sparse_tree  the greedy sparse candidate tree from per-head top-i
+                       accuracies (the blog's section 四; host code)
+  spec_mtp_plug        the MTP draft layer's next input tokens from a verify's
+                       outputs, and the advanced lengths, on the device
+                       ("Beschleunigung von Sonar durch Spekulation", sections
+                       "MTP" and "MTP-Zeitplan für ein einzelnes Token")
 """
 from __future__ import annotations
 
@@ -81,6 +87,10 @@ def load_library():
         lib.spec_sample_rows.restype = i32
         lib.spec_tree_mask.argtypes = [P, i32, P, P, P, P]
         lib.spec_tree_mask.restype = i32
+        lib.spec_build_sparse_tree.argtypes = [P, i32, i32, i32, P, P, P, P, P]
+        lib.spec_build_sparse_tree.restype = i32
+        lib.spec_mtp_plug.argtypes = [P, i32, i32, P, P, ctypes.c_int32, P, P, P, P]
+        lib.spec_mtp_plug.restype = i32
         lib.spec_workspace_bytes_tree_sample.restype = u64
         lib.spec_verify_linear.argtypes = [P, P, i32, i32, i32, i32, P, P, P, f32, P, P, P, P, P, P, u64, P]
         lib.spec_verify_linear.restype = i32
@@ -472,3 +482,59 @@ def spec_tree_mask(parents, *, status=None, out=None, stream=None):
         st = lib.spec_tree_mask(_ptr(parents), N, _ptr(out["mask"]), _ptr(out["depth"]), _ptr(status), h)
     _check(st)
     return out
+
+
+def spec_mtp_plug(in_tokens, out_tokens, num_emitted, pad=0, seq_lens=None, *, in_place=False, out=None,
+                  status=None, stream=None):
+    """The MTP draft layer's next input tokens [B, K+1]: in_tokens shifted left by one, with
+    the verify's emitted tokens (out_tokens [B, K+1], num_emitted [B]) in their places and
+    `pad` at the end; seq_lens [B] (int32, optional) grows by num_emitted in place.
+    in_place=True writes into in_tokens.  Returns dict(next_tokens, seq_lens, status)."""
+    lib = load_library()
+    _cuda(in_tokens, "in_tokens", torch.int32)
+    if in_tokens.dim() != 2:
+        raise ValueError("in_tokens must be [B, K+1]")
+    B, W = in_tokens.shape
+    dev = in_tokens.device
+    _cuda(out_tokens, "out_tokens", torch.int32, dev)
+    _cuda(num_emitted, "num_emitted", torch.int32, dev)
+    _cuda(seq_lens, "seq_lens", torch.int32, dev)
+    if out_tokens is None or tuple(out_tokens.shape) != (B, W):
+        raise ValueError("out_tokens must be [B, K+1]")
+    if num_emitted is None or tuple(num_emitted.shape) != (B,):
+        raise ValueError("num_emitted must be [B]")
+    if seq_lens is not None and tuple(seq_lens.shape) != (B,):
+        raise ValueError("seq_lens must be [B]")
+    h, s = _stream_handle(dev, stream)
+    if in_place:
+        nxt = in_tokens
+    else:
+        nxt = out if out is not None else torch.empty((B, W), dtype=torch.int32, device=dev)
+        _outputs(dict(next_tokens=nxt), {"next_tokens": ((B, W), torch.int32)}, dev)
+    status = _status(status, dev, s)
+    with torch.cuda.device(dev):
+        st = lib.spec_mtp_plug(_ptr(in_tokens), B, W - 1, _ptr(out_tokens), _ptr(num_emitted), int(pad), _ptr(nxt),
+                               _ptr(seq_lens), _ptr(status), h)
+    _check(st)
+    return dict(next_tokens=nxt, seq_lens=seq_lens, status=status)
+
+
+def spec_build_sparse_tree(accuracy, n_nodes):
+    """Greedy sparse candidate tree (host): accuracy [K, S] (a_k^(i) at [k-1, i-1], numpy or
+    a CPU tensor, values in [0, 1]) and the node count wanted (root included).  Returns
+    dict(parents, depth, rank) as int32 numpy arrays of the nodes built, and expected_len."""
+    import numpy as np
+    lib = load_library()
+    acc = np.ascontiguousarray(np.asarray(accuracy, dtype=np.float64))
+    if acc.ndim != 2:
+        raise ValueError("accuracy must be [K, S]")
+    K, S = acc.shape
+    n = int(n_nodes)
+    par, dep, rk = (np.zeros(max(n, 1), np.int32) for _ in range(3))
+    nb, el = ctypes.c_int(0), ctypes.c_double(0.0)
+    st = lib.spec_build_sparse_tree(acc.ctypes.data_as(ctypes.c_void_p), K, S, n,
+                                    par.ctypes.data_as(ctypes.c_void_p), dep.ctypes.data_as(ctypes.c_void_p),
+                                    rk.ctypes.data_as(ctypes.c_void_p), ctypes.byref(nb), ctypes.byref(el))
+    _check(st)
+    m = nb.value
+    return dict(parents=par[:m].copy(), depth=dep[:m].copy(), rank=rk[:m].copy(), expected_len=el.value)

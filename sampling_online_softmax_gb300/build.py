@@ -1,7 +1,8 @@
 """Compile libspecverify.so (the CUDA kernels and their C ABI) in-tree for sm_103a.
 
 The kernel's modes live in separate translation units (csrc/kern_*.cu), which
-are compiled in parallel and linked with the host side (csrc/spec_verify.cu).
+are compiled in parallel and linked with the host side (csrc/spec_verify.cu,
+csrc/tree_build.cpp).
 """
 from __future__ import annotations
 
@@ -16,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
-SOURCES = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+SOURCES = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 DEPENDS = SOURCES + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))) + \
     [os.path.join(INCLUDE, "spec_verify.h")]
 

@@ -17,6 +17,7 @@
 
 #include "host.h"
 #include "spec_verify.h"
+#include "mtp_plug.cuh"
 #include "tree_mask.cuh"
 
 namespace spec {
@@ -463,6 +464,27 @@ extern "C" spec_status spec_tree_mask(const int32_t *parents, int N, uint32_t *m
                                                                                          depth, dev_status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "tree mask launch: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+extern "C" spec_status spec_mtp_plug(const int32_t *in_tokens, int B, int K, const int32_t *out_tokens,
+                                     const int32_t *num_emitted, int32_t pad, int32_t *next_tokens,
+                                     int32_t *seq_lens, uint32_t *dev_status, void *stream) {
+    g_last_error[0] = '\0';
+    if (B < 0 || K < 0) return fail(SPEC_ERR_INVALID_ARG, "need B >= 0, K >= 0 (B=%d K=%d)", B, K);
+    if (B == 0) return SPEC_OK;
+    if (static_cast<long long>(B) * (K + 1) > INT_MAX) return fail(SPEC_ERR_UNSUPPORTED, "B * (K + 1) too large");
+    if (!in_tokens || !out_tokens || !num_emitted || !next_tokens || !dev_status)
+        return fail(SPEC_ERR_INVALID_ARG, "a pointer is null");
+    if (!aligned(in_tokens, 4) || !aligned(out_tokens, 4) || !aligned(num_emitted, 4) || !aligned(next_tokens, 4) ||
+        !aligned(dev_status, 4) || (seq_lens && !aligned(seq_lens, 4)))
+        return fail(SPEC_ERR_INVALID_ARG, "a pointer is misaligned");
+    if (next_tokens == out_tokens) return fail(SPEC_ERR_INVALID_ARG, "next_tokens must not be out_tokens");
+    const int grid = (B + kPlugWarps - 1) / kPlugWarps;
+    mtp_plug_kernel<<<grid, kPlugWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        in_tokens, B, K, out_tokens, num_emitted, pad, next_tokens, seq_lens, dev_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "MTP plug-in launch: %s", cudaGetErrorString(e));
     return SPEC_OK;
 }
 

@@ -176,6 +176,22 @@ def test_tree_mask_host_validation(lib):
     assert f(ctypes.c_void_p(0x10002), 10, FAKE, FAKE, FAKE, None) == sv.SPEC_ERR_INVALID_ARG   # misaligned
 
 
+def test_mtp_plug_host_validation(lib):
+    f = lib.spec_mtp_plug
+    OTHER = ctypes.c_void_p(0x20000)
+
+    def call(inp=FAKE, B=4, K=1, ot=OTHER, ne=FAKE, nxt=FAKE, lens=FAKE, st=FAKE):
+        return f(inp, B, K, ot, ne, 0, nxt, lens, st, None)
+    assert call(B=-1) == sv.SPEC_ERR_INVALID_ARG
+    assert call(K=-1) == sv.SPEC_ERR_INVALID_ARG
+    assert call(B=0) == sv.SPEC_OK
+    for kw in (dict(inp=None), dict(ot=None), dict(ne=None), dict(nxt=None), dict(st=None)):
+        assert call(**kw) == sv.SPEC_ERR_INVALID_ARG
+    assert call(nxt=OTHER) == sv.SPEC_ERR_INVALID_ARG                  # next_tokens must not be out_tokens
+    assert call(lens=ctypes.c_void_p(0x10002)) == sv.SPEC_ERR_INVALID_ARG  # misaligned
+    assert call(B=1 << 30, K=8) == sv.SPEC_ERR_UNSUPPORTED
+
+
 def test_tree_sample_host_validation(lib):
     t = lib.spec_verify_tree_sample
     W = 1 << 20

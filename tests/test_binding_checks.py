@@ -170,3 +170,18 @@ def test_other_outputs_passed_in_are_checked(fake):
     with pytest.raises(ValueError):
         sv.spec_tree_mask(torch.zeros(N, dtype=i32), out=dict(mask=torch.zeros((N, 2), dtype=i32),
                                                              depth=torch.zeros(N, dtype=i32)))
+
+
+def test_mtp_plug(fake):
+    inp, ot, ne = torch.zeros((B, K + 1), dtype=i32), torch.zeros((B, K + 1), dtype=i32), torch.zeros(B, dtype=i32)
+    sv.spec_mtp_plug(inp, ot, ne, 0, torch.zeros(B, dtype=i32))
+    sv.spec_mtp_plug(inp, ot, ne, 0, None, in_place=True)
+    assert "spec_mtp_plug" in fake
+    for a in ((inp, torch.zeros((B, K), dtype=i32), ne, None), (inp, ot, torch.zeros(B + 1, dtype=i32), None),
+              (inp, ot, ne, torch.zeros(B - 1, dtype=i32))):
+        with pytest.raises(ValueError):
+            sv.spec_mtp_plug(*a)
+    with pytest.raises(ValueError):
+        sv.spec_mtp_plug(inp, ot, ne, out=torch.zeros((B, K), dtype=i32))
+    with pytest.raises(TypeError):
+        sv.spec_mtp_plug(inp, ot, ne.to(torch.int64))

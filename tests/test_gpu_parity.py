@@ -402,6 +402,38 @@ def test_tree_mask_of_the_medusa_tree_and_a_chain():
     _mask_parity(np.arange(-1, 700, dtype=np.int32))
 
 
+def test_built_tree_feeds_the_mask_and_the_walk():
+    """The library's builder (host) makes the post's 64-node tree; the mask kernel and the greedy
+    walk consume its parent array as it is, and both agree with the oracle on the oracle's tree."""
+    acc = np.array([[0.6 * 0.8 ** k * 0.5 ** i for i in range(1, 9)] for k in range(1, 5)])
+    built = sv.spec_build_sparse_tree(acc, 64)
+    ot = oracle.build_sparse_tree(acc, 64)
+    np.testing.assert_array_equal(built["parents"], ot["parents"])
+    par = torch.from_numpy(built["parents"]).cuda()
+    m = sv.spec_tree_mask(par)
+    torch.cuda.synchronize()
+    o = oracle.tree_mask(ot["parents"])
+    assert np.array_equal(m["mask"].cpu().numpy().view(np.uint32), o["mask"])
+    np.testing.assert_array_equal(m["depth"].cpu().numpy(), ot["depth"])
+    # the greedy walk over the built tree, with node tokens that follow the argmax on a random part of it
+    g = torch.Generator().manual_seed(8)
+    B, N, V = 12, 64, 3000
+    target = 3.0 * torch.randn((B, N, V), generator=g)
+    am = target.argmax(-1)
+    tok = torch.randint(0, V, (B, N), generator=g, dtype=torch.int32)
+    hit = torch.rand((B, N), generator=g) < 0.6
+    p_idx = torch.from_numpy(built["parents"]).long().clamp(min=0)
+    tok = torch.where(hit, am[:, p_idx].to(torch.int32), tok)
+    tok[:, 0] = 0
+    D = int(built["depth"].max())
+    r = sv.spec_verify_tree(target.cuda(), par, tok.cuda(), D)
+    torch.cuda.synchronize()
+    ow = oracle.verify_tree(target.numpy(), ot["parents"], tok.numpy(), D)
+    rep = compare.compare_tree({k: v.cpu().numpy() for k, v in r.items()}, ow)
+    assert rep.ok, rep.failures[:5]
+    assert ow["path_len"].max() >= 2
+
+
 def test_tree_mask_flags_a_bad_parent():
     _mask_parity(np.array([-1, 0, 7, 1, 2, 3], np.int32))
 
