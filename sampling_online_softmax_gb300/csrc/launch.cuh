@@ -34,7 +34,8 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
     p.Sr = rs.S;
     p.Lr = rs.L;
     p.stats_segs = static_cast<long long>(p.B) * p.rows_per_seq * p.nseg;
-    p.res_tiles = draws ? static_cast<long long>(MODE == kTreeSample ? p.n_units : p.B) * p.Sr : 0;
+    p.n_draws = draws ? (MODE == kTreeSample ? p.n_units : p.B) : 0;
+    p.res_tiles = static_cast<long long>(p.n_draws) * p.Sr;
 #ifdef SPEC_TEST_HOOKS
     p.test_withhold = test_withhold_unit();
 #endif
@@ -75,7 +76,7 @@ spec_status launch(const Params &p0, bool draws, cudaStream_t stream) {
         const long long cand = (MODE == kLinearSample) ? 2ll * p.K * p.B : static_cast<long long>(p.B) * p.rows_per_seq;
         p.keep_rows = static_cast<int>(std::min(budget, cand));
     }
-    if (p.stats_segs + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles + (warps + 1) * kMaxClaim >= (1ll << 31))
+    if (p.stats_segs + (warps + 1) * kMaxGrab >= (1ll << 31) || p.res_tiles >= (1ll << 31))
         return fail(SPEC_ERR_UNSUPPORTED, "too many tiles (B=%d, V=%d)", p.B, p.V);
     // Warps wait on values that warps of other CTAs publish, so every CTA must be resident at once: a
     // cooperative launch guarantees that, or fails here (e.g. when other work holds part of the GPU).

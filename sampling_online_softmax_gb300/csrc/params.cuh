@@ -34,16 +34,11 @@ static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout
 #endif
 constexpr int kSegTiles = SPEC_SEG_TILES;  // stats tiles per segment: one partial each, never split between warps
 constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
-#ifndef SPEC_MAX_CLAIM
-#define SPEC_MAX_CLAIM 4
-#endif
-constexpr int kMaxClaim = SPEC_MAX_CLAIM;  // residual tiles claimed at once (at most)
 constexpr int kTailZone = 4;            // below this many segments per warp left, grab without reserve
 #ifndef SPEC_KEEP_DIV
 #define SPEC_KEEP_DIV 4
 #endif
 constexpr int kKeepDiv = SPEC_KEEP_DIV;  // rows kept in L2 for a residual pass: at most 1/kKeepDiv of L2
-constexpr int kEntWords = 32;           // a draw entry's record and counter share one 128-byte line of their own
 constexpr int kHold = 12;               // chunk sums per lane held in registers while an extra token is located
 constexpr long long kStaticTilesPerWarp = 32;  // up to this many stats tiles per warp: a static split
 #ifndef SPEC_WAIT_LIMIT
@@ -68,7 +63,7 @@ enum Mode : int {
 
 enum TileKind : int { kTileNone = 0, kTileStats = 1, kTileResid = 2 };
 
-// A draw entry: (unit + 1) | pair | skip.
+// A draw record: (unit + 1) | pair | skip.
 constexpr uint32_t kRecUnit = (1u << 30) - 1;
 constexpr uint32_t kRecPair = 1u << 30;  // weights max(0, p - q); else p
 constexpr uint32_t kRecSkip = 1u << 31;  // nothing to draw (non-finite row, bad length)
@@ -93,7 +88,8 @@ struct Params {
     int Sr, Lr;                    // residual slices per entry, elements per slice
     int nstage;                    // stages per warp ring (2..kMaxStages)
     long long stats_segs;          // B * rows_per_seq * nseg
-    long long res_tiles;           // (draw entries: B or 0) * Sr
+    int n_draws;                   // draws recorded: B (linear, extra token alone), B * N (sampled tree) or 0
+    long long res_tiles;           // n_draws * Sr
     float c;                       // log2(e) / T  (sampling modes)
     const int32_t *tokens;         // [B, K] draft tokens, or [B, N] node tokens
     const float *u_accept;         // [B, K]
@@ -109,7 +105,7 @@ struct Params {
     int32_t *bonus_token;          // [B]
     uint32_t *status;              // [1]
     uint32_t *ws_ctrl;             // [0] stats segments taken, [1] CTAs finished, [2] draw entries,
-                                   // [3] residual tiles taken, [4] some wait gave up (clear everything)
+                                   // [3] unused, [4] some wait gave up (clear everything), [5] grid barrier
     unsigned char *ws_base;        // the workspace: ws_bytes bytes, 16-byte aligned
     unsigned long long ws_bytes;
 #ifdef SPEC_TEST_HOOKS
@@ -123,9 +119,8 @@ struct Params {
     unsigned long long *ws_part;   // [n_units * 2 * S] run partials at the run's first tile: (mc | s << 32) or (max | (index + 1) << 32)
     unsigned long long *ws_txw;    // [n_units * 2] the draft token's logit in each row: bits | 1 << 32
     float4 *ws_stats;              // [n_units] (MCt, 1/St, MCd, 1/Sd) of units that may draw
-    uint32_t *ws_rq;               // draw entry e's record: ws_rq[e * kEntWords]
-    uint32_t *ws_res_cnt;          // its residual tiles counted: ws_res_cnt[e * kEntWords] (same line)
-    unsigned long long *ws_csum;   // [B * Sr * kCpt] residual chunk sums, stored plus one
+    uint32_t *ws_draw;             // [n_draws] draw records: (unit + 1) | pair | skip
+    unsigned long long *ws_csum;   // [n_draws * Sr * kCpt] residual chunk sums (int64, units of 2^-52)
 };
 
 }  // namespace spec

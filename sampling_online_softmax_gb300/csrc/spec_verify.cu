@@ -126,10 +126,9 @@ inline bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintpt
 //   [decided / accepted masks: B u64]
 //   [accept bits: B*K i32][argmax: n_units i32][run partials: n_units*2*S u64]
 //   [t(x), d(x): n_units * 2 u64][draw statistics: n_units float4]
-//   [draw entries: B lines of kEntWords u32, the record at word 0 and the residual
-//    tile count at word 16][chunk sums: B*Sr*kCpt i64]
+//   [draw records: entries u32][chunk sums: entries*Sr*kCpt i64]
 struct WsLayout {
-    size_t ctrl, unit_cnt, seq_cnt, seqmask, acc, val, part, tx, stats, rq, res_cnt, csum, total;
+    size_t ctrl, unit_cnt, seq_cnt, seqmask, acc, val, part, tx, stats, draw, csum, total;
 };
 WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, size_t entries) {
     const bool draws = entries > 0;
@@ -144,9 +143,8 @@ WsLayout ws_layout(int B, int K, int units_per_seq, int S, int Sr, size_t entrie
     w.part = w.val + align16(n_units * 4);
     w.tx = w.part + align16(n_units * 2 * static_cast<size_t>(S) * 8);
     w.stats = w.tx + align16(n_units * 16);
-    w.rq = w.stats + (draws ? align16(n_units * 16) : 0);
-    w.res_cnt = w.rq + 64;  // in the record's line
-    w.csum = w.rq + entries * kEntWords * 4;
+    w.draw = w.stats + (draws ? align16(n_units * 16) : 0);
+    w.csum = w.draw + align16(entries * 4);
     w.total = w.csum + align16(entries * static_cast<size_t>(Sr) * kCpt * 8);
     return w;
 }
@@ -163,8 +161,7 @@ void bind_workspace(Params &p, unsigned char *ws, const WsLayout &wl) {
     p.ws_part = reinterpret_cast<unsigned long long *>(ws + wl.part);
     p.ws_txw = reinterpret_cast<unsigned long long *>(ws + wl.tx);
     p.ws_stats = reinterpret_cast<float4 *>(ws + wl.stats);
-    p.ws_rq = reinterpret_cast<uint32_t *>(ws + wl.rq);
-    p.ws_res_cnt = reinterpret_cast<uint32_t *>(ws + wl.res_cnt);
+    p.ws_draw = reinterpret_cast<uint32_t *>(ws + wl.draw);
     p.ws_csum = reinterpret_cast<unsigned long long *>(ws + wl.csum);
 }
 

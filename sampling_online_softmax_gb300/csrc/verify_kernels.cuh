@@ -33,22 +33,25 @@
 //     lowest argmax).  One warp reduces each whole run (or segment) and
 //     publishes one partial; the runs depend only on the shape, so results do
 //     not depend on timing.
-//   * Publishing costs no fence: a partial (or the draft token's logit, or a
-//     residual chunk sum) is written once per call as a non-zero 64-bit value
-//     with a relaxed store and counted with a relaxed atomic.  The warp whose
-//     count completes a unit reads the values, waiting for any that still read
-//     zero, decides the unit, and records it in the sequence's decided/accepted
-//     mask; the update that makes the first rejection known publishes a draw
-//     entry (or emits the sequence).
-//   * A draw entry names one row pair (or one row: the tail, a tree node, a
-//     row to sample) and is cut into Sr residual tiles of at most 4 KB per
-//     row.  Warps claim residual tiles once their stats work is exhausted
-//     (the stats stream has priority: the tail rows it ends with decide the
-//     last draws).  A residual tile sums the fp32 weights max(0, p - q) (or p)
-//     of every 16-byte group exactly in int64 fixed point (units of 2^-52) per
-//     64-group chunk.  The warp that completes an entry's residual locates the
-//     token (a prefix over the chunk sums, then a rescan of one chunk) and
-//     emits it.
+//   * Publishing costs no fence: a partial (or the draft token's logit) is
+//     written once per call as a non-zero 64-bit value with a relaxed store and
+//     counted with a relaxed atomic.  The warp whose count completes a unit
+//     reads the values, waiting for any that still read zero, decides the
+//     unit, and records it in the sequence's decided/accepted mask; the update
+//     that makes the first rejection known records the sequence's draw in the
+//     sequence's own slot (or emits the sequence).
+//   * The extra token is drawn in three more phases separated by grid-wide
+//     barriers (the launch is cooperative, so every CTA is resident):
+//       C. the B * Sr residual tiles -- slices of at most 4 KB of each drawn
+//          row pair (or row: the tail, a tree node, a row to sample) -- are
+//          split statically over all warps; a tile sums the fp32 weights
+//          max(0, p - q) (or p) of every 16-byte group exactly in int64 fixed
+//          point (units of 2^-52) per 64-group chunk;
+//       D. one warp per draw locates the token: a prefix over the chunk sums,
+//          then a rescan of one chunk with bit-identical weights;
+//       E. (sampled tree) one warp per sequence walks the tree.
+//     No counter, claim or record is polled after the stream: each phase's
+//     inputs are complete when its barrier opens.
 //   * L2 policy: the rows a residual pass is likely to re-read (the first
 //     positions' row pairs in stream order, up to 1/kKeepDiv of L2) load at
 //     normal priority, everything else evict-first, so the re-reads mostly
@@ -591,6 +594,26 @@ __device__ __forceinline__ bool run_starts_at(const Params &p, long long t, int 
     return (T * w) / W == t;
 }
 
+// One grid-wide barrier (the target-th arrival in all): every CTA's writes
+// before it are visible to every CTA after it.  The launch is cooperative, so
+// every CTA is resident and the barrier completes; the wait is bounded all the
+// same, and a wait that gives up answers false.  All threads of the CTA call it.
+__device__ __forceinline__ bool grid_barrier(uint32_t *ctr, unsigned target, int *s_flag) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        (void)atom_add_release(ctr, 1u);
+        unsigned v = ld_acquire(ctr);
+        for (uint32_t i = 0; v < target && i < kSpinLimit; ++i) {
+            __nanosleep(32);
+            v = ld_acquire(ctr);
+        }
+        *s_flag = (v >= target) ? 1 : 0;
+    }
+    __syncthreads();
+    return *s_flag != 0;
+}
+
 // =================================================================== kernel
 template <int EB, int MODE>
 __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const Params p) {
@@ -599,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ WarpCtl wctl[kWarps];
+    __shared__ int s_flag;             // a CTA-wide answer: a grid barrier's, then "last CTA"
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -620,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     const size_t row_bytes = static_cast<size_t>(p.V) * EB;
     const bool draws = T::kSample && (T::kBonus || p.u_bonus != nullptr);
     const long long nwarps = static_cast<long long>(gridDim.x) * kWarps;
+    const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;  // this warp's index in the grid
     bool timed_out = false;
 
     // A row of the stats tiling: row slot rs of sequence b.
@@ -705,7 +730,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     bool ahead_issued = false;         // the next grab was requested ahead (away from the end)
     bool stats_done = (NSEG == 0);
     if (p.static_split) {
-        const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;
         sc = p.stats_tiles * gw / p.nwarps;
         se = p.stats_tiles * (gw + 1) / p.nwarps;
         stats_done = sc >= se;
@@ -714,16 +738,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (lane == 0) s_ahead = atomicAdd(&p.ws_ctrl[0], static_cast<unsigned>(s_ahead_n));
         ahead_issued = true;
     }
-    long long rc = 0, re = 0;          // residual tiles [rc, re) claimed, not yet issued
-    int r_entry = -1;                  // entry of r_rec
-    uint32_t r_rec = 0;                // its record (0: not yet seen published)
-    bool rec_inflight = false;
-    uint32_t rec_val = 0;              // lane 0: a record load in flight
-    bool claim_inflight = false;
-    unsigned claim_res = 0;            // lane 0: start of a residual claim in flight
-    int claim_n = 0;
-    long long claim_seen = 0;          // residual tiles claimed by all warps, as of this warp's last claim
-    bool res_done = (RT == 0);
     int issued = 0, handled = 0;
     int islot = 0;                     // stage of the next issue
     auto next_islot = [&]() {
@@ -779,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         ++issued;
     };
 
+    // issue residual tile q (slice q % Sr of draw e = q / Sr, whose record is rec)
     auto issue_resid = [&](long long q, uint32_t rec) {
         const int e = static_cast<int>(q / p.Sr);
         const int k = static_cast<int>(q - static_cast<long long>(e) * p.Sr);
@@ -813,69 +828,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         ++issued;
     };
 
-    auto claim_resid = [&](int n) {
-        if (lane == 0) claim_res = atomicAdd(&p.ws_ctrl[3], static_cast<unsigned>(n));
-        claim_n = n;
-        claim_inflight = true;
-    };
-
-    // Hand the next tile to the ring.  Returns false when nothing was issued:
-    // nothing is ready now (blocking == false), or no work is left at all.
+    // Hand the next stats tile to the ring.  Returns false when nothing was issued:
+    // nothing is ready now (blocking == false), or no stats work is left at all.
     auto try_issue = [&](bool blocking) -> bool {
         for (int guard = 0; guard < (1 << 20); ++guard) {
-            if (claim_inflight) {
-                const unsigned r = __shfl_sync(kFull, claim_res, 0);
-                claim_inflight = false;
-                claim_seen = static_cast<long long>(r) + claim_n;
-                if (static_cast<long long>(r) >= RT) {
-                    res_done = true;
-                } else {
-                    rc = r;
-                    re = min(RT, static_cast<long long>(r) + claim_n);
-                }
-            }
-            // 1. claimed residual tiles, once their entry is published
-            if (rc < re) {
-                const int e = static_cast<int>(rc / p.Sr);
-                if (e != r_entry) {
-                    r_entry = e;
-                    r_rec = 0;
-                    rec_inflight = false;
-                }
-                if (r_rec == 0) {
-                    if (rec_inflight) {
-                        r_rec = __shfl_sync(kFull, rec_val, 0);
-                        rec_inflight = false;
-                    }
-                    if (r_rec == 0 && blocking) {
-                        uint32_t rec = 0;
-                        if (lane == 0) {
-                            rec = ld_relaxed(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
-                            for (uint32_t i = 0; rec == 0 && i < kSpinLimit; ++i) {
-                                __nanosleep(128);
-                                rec = ld_relaxed(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
-                            }
-                        }
-                        r_rec = __shfl_sync(kFull, rec, 0);
-                        if (r_rec == 0) {  // the entry never appeared: give up the residual work
-                            timed_out = true;
-                            rc = re;
-                            res_done = true;
-                            continue;
-                        }
-                    }
-                    if (r_rec == 0 && !rec_inflight) {  // look again at the next call
-                        if (lane == 0) rec_val = ld_relaxed(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
-                        rec_inflight = true;
-                    }
-                }
-                if (r_rec != 0) {
-                    issue_resid(rc, r_rec);
-                    ++rc;
-                    return true;
-                }
-            }
-            // 2. the next stats tile
             if (!stats_done && p.static_split) {
                 if (ik >= ik1) {
                     if (sc >= se) {
@@ -920,26 +876,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     return true;
                 }
             }
-            // 3. stats exhausted: claim residual tiles.  Every sequence publishes exactly one draw
-            //    entry, so the entry of every claimed tile appears; step 1 waits for its record.
-            if (!res_done && rc >= re && !claim_inflight) {
-                // once what is left (as far as this warp knows) fits one round of every warp, an even
-                // share of it; before that one tile at a time, which keeps the warps balanced
-                const long long left = RT - claim_seen;
-                const long long share = (left + nwarps - 1) / nwarps;
-                claim_resid(share <= kMaxClaim ? static_cast<int>(max(1ll, share)) : 1);
-                if (blocking) continue;
-                return false;
-            }
-            if (!blocking) return false;
-            if (stats_done && res_done && rc >= re && !claim_inflight) return false;
+            return false;
         }
         timed_out = true;
         return false;
     };
     auto fill_ring = [&]() {
         while (issued - handled < NS) {
-            if (!claim_inflight && rc >= re && ik < ik1) {  // the next tile of the segment
+            if (ik < ik1) {  // the next tile of the segment
                 issue_stats();
                 continue;
             }
@@ -949,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
 
     // ----------------------------------------------------- processing side
-    // the stats segment being reduced (one row, tiles [k0, k1)), and the residual run
+    // the stats segment being reduced (one row, tiles [k0, k1))
     bool srun = false;
     int run_k0 = 0, run_last = 0, run_len = 0;
     Row prow = {};
@@ -959,15 +903,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     int ai = INT_MAX;                  // lane: index of the max (greedy)
     int hasx = 0;
     float xval = 0.f;
-    bool rrun = false;
-    long long r_next = -1;             // residual tile that would continue the residual run
-    int r_len = 0;
-    int r_e = -1, r_u = 0, r_b = 0, r_pos = 0;
-    uint32_t r_rec_run = 0;            // the residual run's record
-    bool r_pair = false, r_skip = false;
-    float4 r_js = make_float4(0.f, 0.f, 0.f, 0.f);
-    // a counter increment whose result is consumed later (1: unit tiles, 2: residual tiles)
-    int pend_kind = 0, pend_unit = 0, pend_b = 0, pend_pos = 0, pend_entry = 0, pend_add = 0;
+    // a unit-tile count whose result is consumed later
+    bool pend = false;
+    int pend_unit = 0, pend_b = 0, pend_pos = 0, pend_add = 0;
     unsigned pend_old = 0;             // lane 0
 
     // ----------------------------------------------------- finishing side
@@ -985,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
     };
 
-    // Greedy tree walk of sequence b (every node's argmax is in ws_val).
+    // Greedy tree walk of sequence b (every node's choice is in ws_val).
     auto emit_tree = [&](int b) {
         const int N = p.units_per_seq;
         int *par_s = tscratch;
@@ -1041,17 +979,15 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         __syncwarp();
     };
 
-    // Publish a draw entry for unit u.
-    auto push_entry = [&](int u, bool pair, bool skip) {
-        if (lane == 0) {
-            const unsigned e = atomicAdd(&p.ws_ctrl[2], 1u);
-            st_release(&p.ws_rq[static_cast<size_t>(e) * kEntWords], (static_cast<uint32_t>(u) + 1u) | (pair ? kRecPair : 0u) | (skip ? kRecSkip : 0u));
-        }
+    // Record the draw of unit u in slot e (the sequence's, or the node's own).
+    auto set_draw = [&](int e, int u, bool pair, bool skip) {
+        if (lane == 0)
+            p.ws_draw[e] = (static_cast<uint32_t>(u) + 1u) | (pair ? kRecPair : 0u) | (skip ? kRecSkip : 0u);
         __syncwarp();
     };
 
-    // The first rejection j of linear sequence b is known: draw the extra token
-    // (publish a draw entry) or emit the sequence; unit j's scratch is ours.
+    // The first rejection j of linear sequence b is known: record its draw of the
+    // extra token, or emit the sequence; unit j's scratch is ours.
     // skip: 1 / 0 when the caller knows whether unit j is non-finite, -1 if not.
     auto draw_or_emit = [&](int b, int j, int skip) {
         const int U = p.units_per_seq;
@@ -1059,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (MODE == kLinearSample) {
             if (draws) {
                 if (skip < 0) skip = (__ldcg(&p.ws_stats[u]).y > 0.f) ? 0 : 1;  // a non-finite unit recorded 1/St = 0
-                push_entry(u, j < p.K, skip != 0);
+                set_draw(b, u, j < p.K, skip != 0);
             } else {
                 emit_linear(b, j, -1, false);
             }
@@ -1245,8 +1181,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             if (fl) atomicOr(p.status, fl);
         }
         __syncwarp();
-        if (T::kBonus || MODE == kTreeSample) {  // every unit draws: publish its entry
-            if (T::kSample) push_entry(u, nrows == 2, pos < 0 || !finite);
+        if (T::kBonus || MODE == kTreeSample) {  // every unit draws, in a slot of its own
+            if (T::kSample) set_draw(u, u, nrows == 2, pos < 0 || !finite);
             return;
         }
         if ((MODE == kLinearSample || MODE == kLinearGreedy) && K < 32) {
@@ -1303,34 +1239,28 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
             for (int c = 0; c < kCpt; ++c) {
                 const long long t = warp_sum64(q[c]);
-                if (lane == 0) st_relaxed64(&cs[k * kCpt + c], static_cast<unsigned long long>(t) + 1ull);
+                if (lane == 0) cs[k * kCpt + c] = static_cast<unsigned long long>(t);
             }
         }
         __syncwarp();
     };
 
-    // Locate the extra token of entry e; -1 when the weights sum to zero.
+    // Locate the extra token of draw e from its chunk sums; -1 when the weights sum to zero.
     auto select_token = [&](int e, int b, int pos, bool pair, const float4 &js, float ub) -> int {
         const int n = p.Sr * kCpt;
         const unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * n;
-        // lane l owns the chunk sums [l0, l0 + m), l0 = lane * m; the first kHold stay in registers.  Each
-        // sum is stored plus one, so a zero means "not visible yet".
+        // lane l owns the chunk sums [l0, l0 + m), l0 = lane * m; the first kHold stay in registers
         const int m = (n + 31) / 32;
         const int l0 = lane * m;
-        bool late = false;
         long long v[kHold];
 #pragma unroll
         for (int r = 0; r < kHold; ++r)
-            v[r] = (r < m && l0 + r < n) ? static_cast<long long>(ld_relaxed64(&cs[l0 + r])) : 1;
+            v[r] = (r < m && l0 + r < n) ? static_cast<long long>(__ldcg(&cs[l0 + r])) : 0;
         long long mine = 0;
 #pragma unroll
-        for (int r = 0; r < kHold; ++r) {
-            if (v[r] == 0) v[r] = static_cast<long long>(await64(&cs[l0 + r], late));
-            v[r] -= 1;
-            mine += v[r];
-        }
+        for (int r = 0; r < kHold; ++r) mine += v[r];
         for (int j = kHold; j < m && l0 + j < n; ++j)  // long rows only
-            mine += static_cast<long long>(await64(&cs[l0 + j], late)) - 1;
+            mine += static_cast<long long>(__ldcg(&cs[l0 + j]));
         long long incl = mine;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -1338,10 +1268,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             if (lane >= off) incl += y;
         }
         const long long tot = __shfl_sync(kFull, incl, 31);
-        if (__any_sync(kFull, late)) {
-            timed_out = true;
-            return -1;
-        }
         if (tot <= 0) return -1;
         const double ud = (ub >= 0.f) ? static_cast<double>(ub) : 0.0;  // a NaN uniform counts as 0
         long long target = static_cast<long long>(ud * static_cast<double>(tot));
@@ -1361,8 +1287,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                         a += v[r];
                 }
             }
-            for (int j = kHold; ch < 0 && j < m && l0 + j < n; ++j) {  // seen non-zero above
-                const long long w = static_cast<long long>(ld_relaxed64(&cs[l0 + j])) - 1;
+            for (int j = kHold; ch < 0 && j < m && l0 + j < n; ++j) {
+                const long long w = static_cast<long long>(__ldcg(&cs[l0 + j]));
                 if (a + w > target)
                     ch = l0 + j;
                 else
@@ -1441,11 +1367,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         return token < 0 ? 0 : token;
     };
 
-    // Every residual tile of entry e is summed: draw, emit, and clean up.  When this
-    // warp's last residual run was entry e, its record and statistics are at hand.
+    // Draw e's chunk sums are all in: select its token, emit it, clear its scratch.
     auto finish_entry = [&](int e) {
-        const bool mine = (e == r_e);
-        const uint32_t rec = mine ? r_rec_run : __ldcg(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);
+        const uint32_t rec = __ldcg(&p.ws_draw[e]);
+        if (rec == 0u) {  // never recorded: only after a wait upstream gave up
+            timed_out = true;
+            return;
+        }
         const int u = static_cast<int>(rec & kRecUnit) - 1;
         const bool pair = (rec & kRecPair) != 0;
         const bool skip = (rec & kRecSkip) != 0;
@@ -1459,7 +1387,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         int token = 0;
         if (!skip) {
-            const float4 js = mine ? r_js : __ldcg(&p.ws_stats[u]);
+            const float4 js = __ldcg(&p.ws_stats[u]);
             const float ub = __ldg(&p.u_bonus[MODE == kTreeSample ? u : b]);  // per node, or per sequence
             token = select_token(e, b, pos, pair, js, ub);
             if (token < 0 && pair) {
@@ -1470,54 +1398,35 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             }
             if (token < 0) token = 0;
         }
-        int walk = 0;  // sampled tree: this was the sequence's last draw
         if (T::kBonus) {
             if (lane == 0) p.bonus_token[b] = (pos < 0) ? -1 : token;
         } else if (MODE == kTreeSample) {
-            if (lane == 0) {
-                p.ws_val[u] = token;  // the target's choice at node pos
-                walk = (atom_add_acq_rel(&p.ws_seq_cnt[b], 1u) == static_cast<unsigned>(p.units_per_seq - 1)) ? 1 : 0;
-            }
-            walk = __shfl_sync(kFull, walk, 0);
+            if (lane == 0) p.ws_val[u] = token;  // the target's choice at node pos
         } else {
             emit_linear(b, pos, token, true);
         }
         // leave the workspace zeroed
         unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
         for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0ull;
-        if (lane == 0) p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // the other units' by their sequence
         if (lane == 0) {
-            p.ws_rq[static_cast<size_t>(e) * kEntWords] = 0u;
-            p.ws_res_cnt[static_cast<size_t>(e) * kEntWords] = 0u;
+            p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // the other units' by their sequence
+            p.ws_draw[e] = 0u;
         }
         __syncwarp();
-        if (MODE == kTreeSample && walk) {  // every node of sequence b is drawn
-            emit_tree(b);
-            if (lane == 0) p.ws_seq_cnt[b] = 0u;
-            __syncwarp();
-        }
     };
 
-    // consume the pending counter increment
+    // consume the pending unit-tile count: the warp that completes a unit finishes it
     auto resolve_pending = [&]() {
-        if (pend_kind == 0) return;
-        const int kind = pend_kind;
-        pend_kind = 0;
+        if (!pend) return;
+        pend = false;
         int last = 0;
-        if (lane == 0) {
-            const unsigned now = pend_old + static_cast<unsigned>(pend_add);
-            if (kind == 1)
-                last = (now == static_cast<unsigned>(unit_nrows<MODE>(p, pend_pos) * S)) ? 1 : 0;
-            else
-                last = (now == static_cast<unsigned>(p.Sr)) ? 1 : 0;
-        }
+        if (lane == 0)
+            last = (pend_old + static_cast<unsigned>(pend_add) == static_cast<unsigned>(unit_nrows<MODE>(p, pend_pos) * S))
+                       ? 1 : 0;
         last = __shfl_sync(kFull, last, 0);
         if (!last) return;
         __syncwarp();  // (the partials are validated as they are read: no fence needed)
-        if (kind == 1)
-            finish_unit(pend_unit, pend_b, pend_pos);
-        else
-            finish_entry(pend_entry);
+        finish_unit(pend_unit, pend_b, pend_pos);
     };
 
     // the segment's last tile is reduced: merge the lanes, publish, count its tiles
@@ -1540,32 +1449,39 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                              static_cast<unsigned long long>(__float_as_uint(xval)) | (1ull << 32));
             pend_old = atomicAdd(&p.ws_unit_cnt[prow.unit], static_cast<unsigned>(run_len));
         }
-        pend_kind = 1;
+        pend = true;
         pend_unit = prow.unit;
         pend_b = prow.b;
         pend_pos = prow.pos;
         pend_add = run_len;
         srun = false;
     };
-    // the residual run ends: count its tiles
-    auto close_resid = [&]() {
-        resolve_pending();
-        if (lane == 0) pend_old = atomicAdd(&p.ws_res_cnt[static_cast<size_t>(r_e) * kEntWords], static_cast<unsigned>(r_len));
-        pend_kind = 2;
-        pend_entry = r_e;
-        pend_add = r_len;
-        rrun = false;
-    };
 
-    // ------------------------------------------------------------ main loop
     int hslot = 0;                     // stage of the next tile to reduce
     uint32_t hphase = 0;               // its mbarrier phase parity
+    auto advance_slot = [&]() {
+        ++handled;
+        if (++hslot == NS) {
+            hslot = 0;
+            hphase ^= 1u;
+        }
+    };
+    // A wait that gave up can leave bulk copies in flight into this warp's ring:
+    // let them land (each wait bounded again) before the ring is used again or the CTA exits.
+    auto drain = [&]() {
+        while (handled < issued) {
+            (void)wait_bar(ptx::smem_addr(&wc.full[hslot]), hphase);
+            advance_slot();
+        }
+    };
+
+    // ======================================================= phase A: statistics
+    // Every row is streamed once; the warp that completes a unit decides it, and the
+    // update that fixes a sequence's first rejection records its draw (or emits it).
     fill_ring();
     for (;;) {
         if (issued == handled) {
-            // nothing in flight: settle before anything that may wait
-            if (rrun) close_resid();
-            resolve_pending();
+            resolve_pending();  // settle before anything that may wait
             if (!try_issue(true)) break;
             fill_ring();
         }
@@ -1574,87 +1490,115 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
         const uint32_t bar = ptx::smem_addr(&wc.full[s]);
         const uint32_t parity = hphase;
-        if (d.x == kTileStats) {
-            const int k = d.z;
-            if (!srun) {
-                // a new run: its row, and fresh lane statistics
-                if (d.y != prow.id) prow = decode_row(d.y);
-                srun = true;
-                run_k0 = k;
-                run_last = d.w;
-                run_len = 0;
-                am = neg_inf();
-                as = 0.f;
-                ai = INT_MAX;
-                hasx = 0;
-                xval = 0.f;
-                px = -1;
-                if (MODE == kLinearSample && prow.pos < p.K) {
-                    const int x = __ldg(&p.tokens[static_cast<size_t>(prow.b) * p.K + prow.pos]);
-                    px = (x >= 0 && x < p.V) ? x : -1;
-                }
+        const int k = d.z;
+        if (!srun) {
+            // a new run: its row, and fresh lane statistics
+            if (d.y != prow.id) prow = decode_row(d.y);
+            srun = true;
+            run_k0 = k;
+            run_last = d.w;
+            run_len = 0;
+            am = neg_inf();
+            as = 0.f;
+            ai = INT_MAX;
+            hasx = 0;
+            xval = 0.f;
+            px = -1;
+            if (MODE == kLinearSample && prow.pos < p.K) {
+                const int x = __ldg(&p.tokens[static_cast<size_t>(prow.b) * p.K + prow.pos]);
+                px = (x >= 0 && x < p.V) ? x : -1;
             }
-            if (!wait_bar(bar, parity)) {
-                timed_out = true;
-                break;
-            }
-            uintptr_t w0, w1, c0, c1;
-            tile_window(prow, k, w0, w1, c0, c1);
-            const int ngran = static_cast<int>((w1 - w0) >> 4);
-            const int vbase = static_cast<int>((static_cast<long long>(w0) - static_cast<long long>(prow.R0)) / EB);
-            const uintptr_t R1 = prow.R0 + row_bytes;
-            const bool patch = ngran > 0 && (w0 < prow.R0 || w1 > R1 || c0 > w0 || c1 < w1);
-            if (patch) {
-                if (lane < 16) {
-                    Geo g;
-                    g.glo = reinterpret_cast<const unsigned char *>(w0);
-                    g.ngran = ngran;
-                    g.c0 = static_cast<int>(c0 - w0);
-                    g.c1 = static_cast<int>(c1 - w0);
-                    g.a0 = w0 < prow.R0 ? static_cast<int>(prow.R0 - w0) : 0;
-                    g.a1 = static_cast<int>((R1 < w1 ? R1 : w1) - w0);
-                    g.vbase = vbase;
-                    g.patch = true;
-                    patch_row<EB>(buf, g, lane);
-                }
-                __syncwarp();
-            }
-            if (T::kSample)
-                lane_sum<EB>(buf, ngran, p.c, lane, am, as);
-            else
-                lane_argmax<EB>(buf, ngran, vbase, lane, am, ai);
-            if (px >= 0) {
-                const int off = px - vbase;
-                if (off >= 0 && off < ngran * G) {
-                    hasx = 1;
-                    xval = Elt<EB>::load(buf + off * EB);
-                }
+        }
+        if (!wait_bar(bar, parity)) {
+            timed_out = true;
+            break;
+        }
+        uintptr_t w0, w1, c0, c1;
+        tile_window(prow, k, w0, w1, c0, c1);
+        const int ngran = static_cast<int>((w1 - w0) >> 4);
+        const int vbase = static_cast<int>((static_cast<long long>(w0) - static_cast<long long>(prow.R0)) / EB);
+        const uintptr_t R1 = prow.R0 + row_bytes;
+        const bool patch = ngran > 0 && (w0 < prow.R0 || w1 > R1 || c0 > w0 || c1 < w1);
+        if (patch) {
+            if (lane < 16) {
+                Geo g;
+                g.glo = reinterpret_cast<const unsigned char *>(w0);
+                g.ngran = ngran;
+                g.c0 = static_cast<int>(c0 - w0);
+                g.c1 = static_cast<int>(c1 - w0);
+                g.a0 = w0 < prow.R0 ? static_cast<int>(prow.R0 - w0) : 0;
+                g.a1 = static_cast<int>((R1 < w1 ? R1 : w1) - w0);
+                g.vbase = vbase;
+                g.patch = true;
+                patch_row<EB>(buf, g, lane);
             }
             __syncwarp();
-            if (patch) fence_proxy_async();  // generic writes to this stage precede its next bulk copy
-            ++run_len;
-        } else {
-            // ---- a residual tile
+        }
+        if (T::kSample)
+            lane_sum<EB>(buf, ngran, p.c, lane, am, as);
+        else
+            lane_argmax<EB>(buf, ngran, vbase, lane, am, ai);
+        if (px >= 0) {
+            const int off = px - vbase;
+            if (off >= 0 && off < ngran * G) {
+                hasx = 1;
+                xval = Elt<EB>::load(buf + off * EB);
+            }
+        }
+        __syncwarp();
+        if (patch) fence_proxy_async();  // generic writes to this stage precede its next bulk copy
+        ++run_len;
+        advance_slot();
+        fill_ring();
+        resolve_pending();
+        if (k == run_last) close_stats();
+    }
+
+    if (draws) {
+        drain();
+        // ================================================= phase C: residual tiles
+        // Every draw is recorded once every CTA is here.  Warp gw then takes the
+        // residual tiles [RT * gw / W, RT * (gw + 1) / W): slices of the drawn row
+        // pairs (or rows), each reduced to exact chunk sums of its weights.
+        if (!grid_barrier(&p.ws_ctrl[5], gridDim.x, &s_flag)) timed_out = true;
+        const long long q1 = RT * (gw + 1) / nwarps;
+        long long qi = RT * gw / nwarps;   // the next tile to issue
+        int ie = -1;
+        uint32_t irec = 0;
+        auto issue_next = [&]() {
+            const int e = static_cast<int>(qi / p.Sr);
+            if (e != ie) {
+                ie = e;
+                irec = __ldcg(&p.ws_draw[e]);
+                if (irec == 0u) {          // never recorded (only after a timed-out wait): read nothing
+                    timed_out = true;
+                    irec = 1u | kRecSkip;
+                }
+            }
+            issue_resid(qi, irec);
+            ++qi;
+        };
+        while (qi < q1 && issued - handled < NS) issue_next();
+        __syncwarp();
+        int ce = -1, cu = 0, cb = 0, cpos = 0;
+        bool cpair = false, cskip = true;
+        float4 js = make_float4(0.f, 0.f, 0.f, 0.f);
+        while (handled < issued) {
+            const int s = hslot;
+            const int4 d = wc.desc[s];
+            unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
             const long long idx = static_cast<unsigned>(d.y);
             const uint32_t rec = static_cast<uint32_t>(d.z);
             const int e = static_cast<int>(idx / p.Sr);
             const int k = static_cast<int>(idx - static_cast<long long>(e) * p.Sr);
-            if (rrun && idx != r_next) close_resid();
-            if (!rrun) {
-                rrun = true;
-                r_len = 0;
-                r_e = e;
-                r_pair = (rec & kRecPair) != 0;
-                r_skip = (rec & kRecSkip) != 0;
-                r_rec_run = rec;
-                entry_unit(rec, r_u, r_b, r_pos);
-                if (!r_skip) {
-                    if (lane == 0) (void)ld_acquire(&p.ws_rq[static_cast<size_t>(e) * kEntWords]);  // orders the loads of the entry's statistics
-                    __syncwarp();
-                    r_js = __ldcg(&p.ws_stats[r_u]);
-                }
+            if (e != ce) {
+                ce = e;
+                cpair = (rec & kRecPair) != 0;
+                cskip = (rec & kRecSkip) != 0;
+                entry_unit(rec, cu, cb, cpos);
+                if (!cskip) js = __ldcg(&p.ws_stats[cu]);
             }
-            if (!wait_bar(bar, parity)) {
+            if (!wait_bar(ptx::smem_addr(&wc.full[s]), hphase)) {
                 timed_out = true;
                 break;
             }
@@ -1662,22 +1606,22 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
             for (int c = 0; c < kCpt; ++c) q[c] = 0;
             bool patched = false;
-            if (!r_skip) {
+            if (!cskip) {
                 const int s0 = k * p.Lr;
                 const int s1 = min(p.V, s0 + p.Lr);
-                const Geo g0 = make_geo<EB>(row_ptr<EB>(p, r_b, r_pos, 0), s0, s1, p.target, p.t_end);
+                const Geo g0 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 0), s0, s1, p.target, p.t_end);
                 Geo g1 = g0;
-                if (r_pair) g1 = make_geo<EB>(row_ptr<EB>(p, r_b, r_pos, 1), s0, s1, p.draft, p.d_end);
-                patched = g0.patch || (r_pair && g1.patch);
+                if (cpair) g1 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 1), s0, s1, p.draft, p.d_end);
+                patched = g0.patch || (cpair && g1.patch);
                 if (patched) {
                     if (lane < 16) {
                         if (g0.patch) patch_row<EB>(buf, g0, lane);
-                    } else if (r_pair && g1.patch) {
+                    } else if (cpair && g1.patch) {
                         patch_row<EB>(buf + kRowBuf, g1, lane - 16);
                     }
                     __syncwarp();
                 }
-                tile_resid<EB>(buf, g0.ngran, g0.vbase, g1.vbase, s0, s1, r_pair, g0.vbase == g1.vbase, r_js, p.c,
+                tile_resid<EB>(buf, g0.ngran, g0.vbase, g1.vbase, s0, s1, cpair, g0.vbase == g1.vbase, js, p.c,
                                lane, q);
             }
             __syncwarp();
@@ -1685,55 +1629,37 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             if (lane == 0) {
                 unsigned long long *dst = p.ws_csum + (static_cast<size_t>(e) * p.Sr + k) * kCpt;
 #pragma unroll
-                for (int c = 0; c < kCpt; ++c) st_relaxed64(&dst[c], static_cast<unsigned long long>(q[c]) + 1ull);
+                for (int c = 0; c < kCpt; ++c) dst[c] = static_cast<unsigned long long>(q[c]);
             }
-            ++r_len;
-            r_next = (k + 1 < p.Sr) ? idx + 1 : -1;
+            advance_slot();
+            while (qi < q1 && issued - handled < NS) issue_next();
+            __syncwarp();
         }
-        ++handled;
-        if (++hslot == NS) {
-            hslot = 0;
-            hphase ^= 1u;
-        }
-        fill_ring();
-        resolve_pending();
-        if (d.x == kTileStats) {
-            if (d.z == run_last) close_stats();
-        } else if (rrun) {
-            // close the residual run now unless the next tile in the ring continues it
-            bool cont = false;
-            if (r_next >= 0 && issued > handled) {
-                const int4 nd = wc.desc[hslot];
-                cont = nd.x == kTileResid && static_cast<long long>(static_cast<unsigned>(nd.y)) == r_next;
-            }
-            if (!cont) close_resid();
+        drain();
+        // ================================================= phase D: one select per draw
+        if (!grid_barrier(&p.ws_ctrl[5], 2 * gridDim.x, &s_flag)) timed_out = true;
+        for (long long e = gw; e < p.n_draws; e += nwarps) finish_entry(static_cast<int>(e));
+        if (MODE == kTreeSample) {
+            // ============================================= phase E: the walks
+            if (!grid_barrier(&p.ws_ctrl[5], 3 * gridDim.x, &s_flag)) timed_out = true;
+            for (long long b = gw; b < p.B; b += nwarps) emit_tree(static_cast<int>(b));
         }
     }
 
-    // A wait that gave up can leave bulk copies in flight into this warp's ring:
-    // let them land (each wait bounded again) before the CTA may exit.
-    while (handled < issued) {
-        (void)wait_bar(ptx::smem_addr(&wc.full[hslot]), hphase);
-        ++handled;
-        if (++hslot == NS) {
-            hslot = 0;
-            hphase ^= 1u;
-        }
-    }
+    drain();
     timed_out = __any_sync(kFull, timed_out);
     if (lane == 0 && timed_out) {
         atomicOr(p.status, SPEC_DEV_TIMEOUT);
         atomicOr(&p.ws_ctrl[4], 1u);  // leftovers anywhere: the last CTA clears the whole workspace
     }
-    // ---- the last CTA to finish leaves the workspace zeroed: the counters always,
+    // ---- the last CTA to finish leaves the workspace zeroed: the control words always,
     //      everything else after a timed-out wait (whose values may have landed late,
     //      or never been consumed)
-    __shared__ int s_last;
     __threadfence();  // this CTA's workspace writes precede its count
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atom_add_acq_rel(&p.ws_ctrl[1], 1u) == gridDim.x - 1) ? 1 : 0;
+    if (threadIdx.x == 0) s_flag = (atom_add_acq_rel(&p.ws_ctrl[1], 1u) == gridDim.x - 1) ? 1 : 0;
     __syncthreads();
-    if (s_last) {
+    if (s_flag) {
         if (__ldcg(&p.ws_ctrl[4]) != 0u) {
             uint4 *w = reinterpret_cast<uint4 *>(p.ws_base + kCtrlWords * 4);
             const unsigned long long n = (p.ws_bytes - kCtrlWords * 4) / 16;
