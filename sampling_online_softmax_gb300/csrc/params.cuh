@@ -14,7 +14,7 @@ namespace spec {
 #endif
 constexpr int kWarps = SPEC_WARPS;  // streaming warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 4;             // mbarriers per warp: the residual phase splits the ring finer
 #ifndef SPEC_TILE_KB
 #define SPEC_TILE_KB 8
 #endif
@@ -23,12 +23,15 @@ constexpr int kMaxStages = 4;
 #endif
 constexpr int kMinCtas = SPEC_MIN_CTAS;              // CTAs resident per SM
 constexpr int kTileBytes = SPEC_TILE_KB * 1024;      // stats tile: a window of one row on the 16-byte grid
-constexpr int kResidSliceBytes = kTileBytes / 2;     // at most this many bytes of each row per residual tile
-constexpr int kRowBuf = kResidSliceBytes + 64;       // residual row buffer: a slice plus its ragged groups
-constexpr int kStageBytes = 2 * kRowBuf;
+constexpr int kStageBytes = kTileBytes;              // a stats stage of a warp's ring
+constexpr int kResidSliceBytes = 4064;               // at most this many bytes of each row per residual tile
+constexpr int kRowBuf = 4096;                        // residual row buffer: a slice plus its two ragged groups
+constexpr int kCStageBytes = 2 * kRowBuf;            // a residual stage: the slice of a row pair
 constexpr int kChunk = 64;                           // 16-byte groups per residual chunk
-constexpr int kCpt = (kResidSliceBytes / 16 + 2 + kChunk - 1) / kChunk;  // residual chunks per tile
-static_assert(kStageBytes >= kTileBytes && kStageBytes % 128 == 0, "stage layout");
+constexpr int kCpt = kRowBuf / 16 / kChunk;          // residual chunks per tile (the whole row buffer)
+static_assert(kResidSliceBytes % 16 == 0 && kResidSliceBytes + 32 <= kRowBuf, "a slice's window fits its buffer");
+static_assert(kRowBuf % (16 * kChunk) == 0 && kCpt == 4, "four chunks per residual tile");
+static_assert(kStageBytes % kCStageBytes == 0 && kStageBytes % 128 == 0, "stage layout");
 #ifndef SPEC_SEG_TILES
 #define SPEC_SEG_TILES 4
 #endif
@@ -40,7 +43,10 @@ constexpr int kTailZone = 4;            // below this many segments per warp lef
 #endif
 constexpr int kKeepDiv = SPEC_KEEP_DIV;  // rows kept in L2 for a residual pass: at most 1/kKeepDiv of L2
 constexpr int kHold = 12;               // chunk sums per lane held in registers while an extra token is located
-constexpr long long kStaticTilesPerWarp = 32;  // up to this many stats tiles per warp: a static split
+#ifndef SPEC_STATIC_TILES_PER_WARP
+#define SPEC_STATIC_TILES_PER_WARP 32
+#endif
+constexpr long long kStaticTilesPerWarp = SPEC_STATIC_TILES_PER_WARP;  // up to this many stats tiles per warp: a static split
 #ifndef SPEC_WAIT_LIMIT
 #define SPEC_WAIT_LIMIT (1u << 22)
 #endif

@@ -67,8 +67,12 @@ Slicing resid_slicing(int V, int eb) {
     const int G = 16 / eb;
     const long long row_bytes = static_cast<long long>(V) * eb;
     int S = static_cast<int>(std::max<long long>(1, (row_bytes + kResidSliceBytes - 1) / kResidSliceBytes));
-    int L = (V + S - 1) / S;
-    L = (L + G - 1) / G * G;  // still <= kResidSliceBytes / eb, a multiple of G
+    int L = 0;
+    for (;; ++S) {  // the fewest slices whose length, rounded up to whole groups, still fits
+        L = (V + S - 1) / S;
+        L = (L + G - 1) / G * G;
+        if (static_cast<long long>(L) * eb <= kResidSliceBytes) break;
+    }
     S = (V + L - 1) / L;
     return {S, L};
 }

@@ -627,13 +627,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     WarpCtl &wc = wctl[warp];
-    const int NS = p.nstage;
+    const int NS = p.nstage;  // stats stages of the ring; the residual phase splits the same bytes finer
+    const int NSC = min(kMaxStages, NS * kStageBytes / kCStageBytes);
     unsigned char *ring = dsm + static_cast<size_t>(warp) * NS * kStageBytes;
     int *tscratch = reinterpret_cast<int *>(dsm + static_cast<size_t>(kWarps) * NS * kStageBytes) +
                     static_cast<size_t>(warp) * 3 * p.units_per_seq;
 
     if (lane == 0) {
-        for (int s = 0; s < NS; ++s) ptx::mbar_init(ptx::smem_addr(&wc.full[s]), 1);
+        for (int s = 0; s < kMaxStages; ++s) ptx::mbar_init(ptx::smem_addr(&wc.full[s]), 1);
         ptx::fence_mbar_init();
     }
     __syncwarp();
@@ -739,10 +740,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         ahead_issued = true;
     }
     int issued = 0, handled = 0;
+    int nst = NS;                      // stages in use: NS of kStageBytes, then NSC of kCStageBytes
     int islot = 0;                     // stage of the next issue
     auto next_islot = [&]() {
         const int s = islot;
-        islot = (islot + 1 == NS) ? 0 : islot + 1;
+        islot = (islot + 1 == nst) ? 0 : islot + 1;
         return s;
     };
 
@@ -802,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         int u, b, pos;
         entry_unit(rec, u, b, pos);
         const int s = next_islot();
-        unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
+        unsigned char *buf = ring + static_cast<size_t>(s) * kCStageBytes;
         const int s0 = k * p.Lr;
         const int s1 = min(p.V, s0 + p.Lr);
         const Geo g0 = make_geo<EB>(row_ptr<EB>(p, b, pos, 0), s0, s1, p.target, p.t_end);
@@ -882,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         return false;
     };
     auto fill_ring = [&]() {
-        while (issued - handled < NS) {
+        while (issued - handled < nst) {
             if (ik < ik1) {  // the next tile of the segment
                 issue_stats();
                 continue;
@@ -1368,8 +1370,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
 
     // Draw e's chunk sums are all in: select its token, emit it, clear its scratch.
-    auto finish_entry = [&](int e) {
-        const uint32_t rec = __ldcg(&p.ws_draw[e]);
+    // rec, js and ub were loaded once the draws were recorded (see phase C).
+    auto finish_entry = [&](int e, uint32_t rec, const float4 &js, float ub) {
         if (rec == 0u) {  // never recorded: only after a wait upstream gave up
             timed_out = true;
             return;
@@ -1387,8 +1389,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         int token = 0;
         if (!skip) {
-            const float4 js = __ldcg(&p.ws_stats[u]);
-            const float ub = __ldg(&p.u_bonus[MODE == kTreeSample ? u : b]);  // per node, or per sequence
             token = select_token(e, b, pos, pair, js, ub);
             if (token < 0 && pair) {
                 // the residual vanished through rounding: draw from p_j instead
@@ -1458,19 +1458,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
 
     int hslot = 0;                     // stage of the next tile to reduce
-    uint32_t hphase = 0;               // its mbarrier phase parity
+    uint32_t bar_par = 0;              // bit s: the phase parity stage s's mbarrier completes next
     auto advance_slot = [&]() {
         ++handled;
-        if (++hslot == NS) {
-            hslot = 0;
-            hphase ^= 1u;
-        }
+        bar_par ^= 1u << hslot;
+        if (++hslot == nst) hslot = 0;
     };
     // A wait that gave up can leave bulk copies in flight into this warp's ring:
     // let them land (each wait bounded again) before the ring is used again or the CTA exits.
     auto drain = [&]() {
         while (handled < issued) {
-            (void)wait_bar(ptx::smem_addr(&wc.full[hslot]), hphase);
+            (void)wait_bar(ptx::smem_addr(&wc.full[hslot]), (bar_par >> hslot) & 1u);
             advance_slot();
         }
     };
@@ -1489,7 +1487,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         const int4 d = wc.desc[s];
         unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
         const uint32_t bar = ptx::smem_addr(&wc.full[s]);
-        const uint32_t parity = hphase;
+        const uint32_t parity = (bar_par >> s) & 1u;
         const int k = d.z;
         if (!srun) {
             // a new run: its row, and fresh lane statistics
@@ -1561,6 +1559,24 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         // residual tiles [RT * gw / W, RT * (gw + 1) / W): slices of the drawn row
         // pairs (or rows), each reduced to exact chunk sums of its weights.
         if (!grid_barrier(&p.ws_ctrl[5], gridDim.x, &s_flag)) timed_out = true;
+        // The selects of phase D are spread over the grid (consecutive draws on different SMs):
+        // warp gw selects draws [n * gw / W, n * (gw + 1) / W).  Their records, statistics and
+        // uniforms are complete now; load them ahead of the selects.
+        const long long nd = p.n_draws;
+        const int d0 = static_cast<int>(nd * gw / nwarps), d1 = static_cast<int>(nd * (gw + 1) / nwarps);
+        uint32_t drec = 0u;
+        float4 djs = make_float4(0.f, 0.f, 0.f, 0.f);
+        float dub = 0.f;
+        if (d0 < d1) {
+            drec = __ldcg(&p.ws_draw[d0]);
+            if (drec != 0u && !(drec & kRecSkip)) {
+                const int u = static_cast<int>(drec & kRecUnit) - 1;
+                djs = __ldcg(&p.ws_stats[u]);
+                dub = __ldg(&p.u_bonus[(MODE == kTreeSample || T::kBonus) ? u : u / p.units_per_seq]);
+            }
+        }
+        nst = NSC;  // nothing is in flight: re-cut the ring into NSC smaller stages
+        islot = hslot = 0;
         const long long q1 = RT * (gw + 1) / nwarps;
         long long qi = RT * gw / nwarps;   // the next tile to issue
         int ie = -1;
@@ -1578,7 +1594,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             issue_resid(qi, irec);
             ++qi;
         };
-        while (qi < q1 && issued - handled < NS) issue_next();
+        while (qi < q1 && issued - handled < nst) issue_next();
         __syncwarp();
         int ce = -1, cu = 0, cb = 0, cpos = 0;
         bool cpair = false, cskip = true;
@@ -1586,7 +1602,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         while (handled < issued) {
             const int s = hslot;
             const int4 d = wc.desc[s];
-            unsigned char *buf = ring + static_cast<size_t>(s) * kStageBytes;
+            unsigned char *buf = ring + static_cast<size_t>(s) * kCStageBytes;
             const long long idx = static_cast<unsigned>(d.y);
             const uint32_t rec = static_cast<uint32_t>(d.z);
             const int e = static_cast<int>(idx / p.Sr);
@@ -1598,7 +1614,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 entry_unit(rec, cu, cb, cpos);
                 if (!cskip) js = __ldcg(&p.ws_stats[cu]);
             }
-            if (!wait_bar(ptx::smem_addr(&wc.full[s]), hphase)) {
+            if (!wait_bar(ptx::smem_addr(&wc.full[s]), (bar_par >> s) & 1u)) {
                 timed_out = true;
                 break;
             }
@@ -1632,17 +1648,29 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 for (int c = 0; c < kCpt; ++c) dst[c] = static_cast<unsigned long long>(q[c]);
             }
             advance_slot();
-            while (qi < q1 && issued - handled < NS) issue_next();
+            while (qi < q1 && issued - handled < nst) issue_next();
             __syncwarp();
         }
         drain();
         // ================================================= phase D: one select per draw
         if (!grid_barrier(&p.ws_ctrl[5], 2 * gridDim.x, &s_flag)) timed_out = true;
-        for (long long e = gw; e < p.n_draws; e += nwarps) finish_entry(static_cast<int>(e));
+        for (int e = d0; e < d1; ++e) {
+            if (e > d0) {  // more draws than warps: the later ones load here
+                drec = __ldcg(&p.ws_draw[e]);
+                if (drec != 0u && !(drec & kRecSkip)) {
+                    const int u = static_cast<int>(drec & kRecUnit) - 1;
+                    djs = __ldcg(&p.ws_stats[u]);
+                    dub = __ldg(&p.u_bonus[(MODE == kTreeSample || T::kBonus) ? u : u / p.units_per_seq]);
+                }
+            }
+            finish_entry(e, drec, djs, dub);
+        }
         if (MODE == kTreeSample) {
             // ============================================= phase E: the walks
             if (!grid_barrier(&p.ws_ctrl[5], 3 * gridDim.x, &s_flag)) timed_out = true;
-            for (long long b = gw; b < p.B; b += nwarps) emit_tree(static_cast<int>(b));
+            const int b0 = static_cast<int>(static_cast<long long>(p.B) * gw / nwarps);
+            const int b1 = static_cast<int>(static_cast<long long>(p.B) * (gw + 1) / nwarps);
+            for (int b = b0; b < b1; ++b) emit_tree(b);
         }
     }
 
