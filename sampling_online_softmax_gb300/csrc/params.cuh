@@ -14,7 +14,7 @@ namespace spec {
 #endif
 constexpr int kWarps = SPEC_WARPS;  // streaming warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxStages = 4;             // mbarriers per warp: the residual phase splits the ring finer
+constexpr int kMaxStages = 4;             // mbarriers per warp: the residual phase may use more stages
 #ifndef SPEC_TILE_KB
 #define SPEC_TILE_KB 8
 #endif
@@ -32,6 +32,9 @@ constexpr int kCpt = kRowBuf / 16 / kChunk;          // residual chunks per tile
 static_assert(kResidSliceBytes % 16 == 0 && kResidSliceBytes + 32 <= kRowBuf, "a slice's window fits its buffer");
 static_assert(kRowBuf % (16 * kChunk) == 0 && kCpt == 4, "four chunks per residual tile");
 static_assert(kStageBytes % kCStageBytes == 0 && kStageBytes % 128 == 0, "stage layout");
+// Warps of a CTA that reduce residual tiles (all of them: the reduction is bound by each warp's
+// dependent arithmetic, so fewer warps with deeper rings measured slower).
+constexpr int kCWarps = kWarps;
 #ifndef SPEC_SEG_TILES
 #define SPEC_SEG_TILES 4
 #endif

@@ -385,6 +385,11 @@ __device__ __forceinline__ long long warp_sum64(long long q) {
     return q;
 }
 
+#ifndef SPEC_RESID_UNROLL
+#define SPEC_RESID_UNROLL 4
+#endif
+constexpr int kResidUnroll = SPEC_RESID_UNROLL;  // group iterations of a residual tile unrolled together
+
 // ------------------------------------------------------ extra-token weights
 // The weights of a 16-byte group are summed as (w0 + w2 + w4 + ...) + (w1 + w3
 // + w5 + ...): even and odd elements in order, then the two; the packed tile
@@ -471,7 +476,10 @@ __device__ __forceinline__ void lane_argmax(const unsigned char *buf, int ngran,
 // Exact weight sums of one residual tile per chunk of 64 groups (every lane
 // ends with them).  Groups follow the target row's window; `same` when both
 // row buffers share the 16-byte phase.  Packed fp32x2 arithmetic on element
-// pairs; every weight is the same as elem_weight's.
+// pairs; every weight is the same as elem_weight's.  All 2 * kCpt groups of a
+// lane are reduced without a branch (they lie inside the row buffers); groups
+// past the window hold stale bytes and are given no weight, so the iterations
+// are independent and overlap.
 template <int EB>
 __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, int vbase0, int vbase1, int s0,
                                            int s1, bool pair, bool same, const float4 &js, float c, int lane,
@@ -483,13 +491,12 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
     const unsigned long long c2 = f2pack(c, c);
     const unsigned long long nmt = f2pack(-js.x, -js.x), ist = f2pack(js.y, js.y);
     const unsigned long long nmd = f2pack(-js.z, -js.z), isd = f2pack(js.w, js.w);
-    static_assert(kChunk == 64, "two groups per lane and chunk");
+    static_assert(kChunk == 64 && 2 * kCpt * 32 * 16 == kRowBuf, "two groups per lane and chunk, covering the buffer");
 #pragma unroll
     for (int ch = 0; ch < kCpt; ++ch) q[ch] = 0;
-#pragma unroll
+#pragma unroll (kResidUnroll)
     for (int it = 0; it < 2 * kCpt; ++it) {
         const int g = it * 32 + lane;  // chunk it / 2
-        if (g >= ngran) break;
         unsigned long long t2[P], d2[P];
         Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bt + 16 * g), t2);
         if (pair) {
@@ -520,7 +527,7 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
         }
         float se, so;
         f2unpack(acc, se, so);
-        q[it >> 1] += fixq(se + so);
+        q[it >> 1] += fixq(g < ngran ? se + so : 0.0f);
     }
 #pragma unroll
     for (int ch = 0; ch < kCpt; ++ch) q[ch] = warp_sum64(q[ch]);
@@ -628,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     const int warp = threadIdx.x >> 5;
     WarpCtl &wc = wctl[warp];
     const int NS = p.nstage;  // stats stages of the ring; the residual phase splits the same bytes finer
-    const int NSC = min(kMaxStages, NS * kStageBytes / kCStageBytes);
+    const int NSC = min(kMaxStages, (kWarps / kCWarps) * NS * kStageBytes / kCStageBytes);
+    const int cspr = NS * kStageBytes / kCStageBytes;  // residual stages within one warp's ring
     unsigned char *ring = dsm + static_cast<size_t>(warp) * NS * kStageBytes;
     int *tscratch = reinterpret_cast<int *>(dsm + static_cast<size_t>(kWarps) * NS * kStageBytes) +
                     static_cast<size_t>(warp) * 3 * p.units_per_seq;
@@ -795,6 +803,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         ++issued;
     };
 
+    // Residual stage s of this warp: stages beyond its own ring lie in the rings of the warps
+    // kCWarps, 2 * kCWarps, ... above it, which reduce no residual tiles.
+    auto cstage = [&](int s) -> unsigned char * {
+        return dsm + (static_cast<size_t>(warp + (s / cspr) * kCWarps) * NS * kStageBytes) +
+               static_cast<size_t>(s % cspr) * kCStageBytes;
+    };
     // issue residual tile q (slice q % Sr of draw e = q / Sr, whose record is rec)
     auto issue_resid = [&](long long q, uint32_t rec) {
         const int e = static_cast<int>(q / p.Sr);
@@ -804,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         int u, b, pos;
         entry_unit(rec, u, b, pos);
         const int s = next_islot();
-        unsigned char *buf = ring + static_cast<size_t>(s) * kCStageBytes;
+        unsigned char *buf = cstage(s);
         const int s0 = k * p.Lr;
         const int s1 = min(p.V, s0 + p.Lr);
         const Geo g0 = make_geo<EB>(row_ptr<EB>(p, b, pos, 0), s0, s1, p.target, p.t_end);
@@ -1575,10 +1589,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 dub = __ldg(&p.u_bonus[(MODE == kTreeSample || T::kBonus) ? u : u / p.units_per_seq]);
             }
         }
-        nst = NSC;  // nothing is in flight: re-cut the ring into NSC smaller stages
+        nst = NSC;  // nothing is in flight: re-cut the ring(s) into NSC residual stages
         islot = hslot = 0;
-        const long long q1 = RT * (gw + 1) / nwarps;
-        long long qi = RT * gw / nwarps;   // the next tile to issue
+        const long long cwarps = static_cast<long long>(gridDim.x) * kCWarps;
+        const long long cw = static_cast<long long>(blockIdx.x) * kCWarps + warp;
+        const bool cactive = warp < kCWarps;
+        const long long q1 = cactive ? RT * (cw + 1) / cwarps : 0;
+        long long qi = cactive ? RT * cw / cwarps : 0;   // the next tile to issue
         int ie = -1;
         uint32_t irec = 0;
         auto issue_next = [&]() {
@@ -1602,7 +1619,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         while (handled < issued) {
             const int s = hslot;
             const int4 d = wc.desc[s];
-            unsigned char *buf = ring + static_cast<size_t>(s) * kCStageBytes;
+            unsigned char *buf = cstage(s);
             const long long idx = static_cast<unsigned>(d.y);
             const uint32_t rec = static_cast<uint32_t>(d.z);
             const int e = static_cast<int>(idx / p.Sr);
