@@ -69,7 +69,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="the headline line without per_config")
     ap.add_argument("--workload", default="headline",
-                    help="headline, or one configuration alone: " + ", ".join(CONFIGS) + ", all")
+                    help="headline, or one configuration alone: " + ", ".join(list(CONFIGS) + list(ALONE)) + ", all")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --workload: the first N sequences only (a smaller case of the same kernel, for "
+                         "profiler captures)")
     return ap.parse_args()
 
 
@@ -443,6 +446,10 @@ CONFIGS = {
     "mtp_plug_T1": (3, 1.0, "plug"),
     "medusa_tree_build": (4, 0.0, "build"),
 }
+# configurations timed only when named with --workload (the headline's own workload, for captures)
+ALONE = {
+    "stress_T0.7": (5, 0.7, "linear"),
+}
 # committed ncu summaries (profiles/) behind each configuration's traffic figure
 CONFIG_PROFILES = {
     "small_T1": "spec_verify_kernel_linear_sample_small.md",
@@ -466,14 +473,20 @@ CONFIG_KERNELS = {
 }
 
 
-def config_inputs(name, dev):
-    """Device inputs of one configuration (with a uniform per node for the sampled tree)."""
+def config_inputs(name, dev, batch=0):
+    """Device inputs of one configuration (with a uniform per node for the sampled tree);
+    batch > 0 keeps the first `batch` sequences of a linear configuration."""
+    import dataclasses
+
     import numpy as np
     import torch
     from workloads import WORKLOADS, make_linear, make_tree
-    number, T, kind = CONFIGS[name]
+    number, T, kind = {**CONFIGS, **ALONE}[name]
     w = WORKLOADS[number]
     if kind == "linear":
+        if batch:
+            w = dataclasses.replace(w, B=min(batch, w.B))
+            return w, T, kind, make_linear(number, T, device=dev, B=w.B)
         return w, T, kind, make_linear(number, T, device=dev)
     if kind == "mask":
         return w, T, kind, dict(parents=make_tree(number, device=dev, B=1, V=64)["parents"])
@@ -664,13 +677,13 @@ def run_build_config(args, name, in_line=False):
 def run_config(args, name, in_line=False):
     """One configuration, the kernel alone, replayed from a CUDA graph; clocks, roofline, oracle beside it."""
     import torch
-    if CONFIGS[name][2] == "build":
+    if {**CONFIGS, **ALONE}[name][2] == "build":
         return run_build_config(args, name, in_line)
 
     import sampling_online_softmax_gb300 as sv
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    w, T, kind, d = config_inputs(name, dev)
+    w, T, kind, d = config_inputs(name, dev, getattr(args, "batch", 0))
     bytes_per_step = config_bytes(w, T, kind, d)
     rotate = max(1, min(4, int(2 * L2_BYTES // bytes_per_step) + 1))   # more than L2 over the copies
     keys = {"linear": ("target", "draft"), "rows": ("rows",), "mask": ("parents",),
@@ -745,7 +758,7 @@ def run_config(args, name, in_line=False):
            "seed": w.seed}
     if kind in ("tree", "tree_sample"):
         cfg["N"] = int(d["node_tokens"].shape[1])
-    prof = CONFIG_PROFILES.get(name)
+    prof = CONFIG_PROFILES.get(name) if not getattr(args, "batch", 0) else None
     entry = {"us_per_call": 1e6 * step_s, "value": B / step_s, "unit": unit,
              "timing": "kernel alone, %d calls per CUDA graph replay, %d replays" % (per_graph, reps),
              "config": cfg,
@@ -767,7 +780,10 @@ def main():
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "--workload times the oracle beside our arm"}))
             return
-        for name in (list(CONFIGS) if args.workload == "all" else [args.workload]):
+        names = list(CONFIGS) if args.workload == "all" else [args.workload]
+        for name in names:
+            if name not in CONFIGS and name not in ALONE:
+                raise SystemExit("unknown workload %r" % name)
             run_config(args, name)
         return
     if args.impl == "reference":
