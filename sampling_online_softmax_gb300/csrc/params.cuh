@@ -113,8 +113,8 @@ struct Params {
     int32_t *path_nodes;           // [B, max_depth+1]
     int32_t *bonus_token;          // [B]
     uint32_t *status;              // [1]
-    uint32_t *ws_ctrl;             // [0] stats segments taken, [1] CTAs finished, [2] draw entries,
-                                   // [3] unused, [4] some wait gave up (clear everything), [5] grid barrier
+    uint32_t *ws_ctrl;             // [0] stats segments taken, [1] CTAs finished, [4] some wait gave up
+                                   // (clear everything), [5] grid-barrier arrivals; [2], [3], [6], [7] unused
     unsigned char *ws_base;        // the workspace: ws_bytes bytes, 16-byte aligned
     unsigned long long ws_bytes;
 #ifdef SPEC_TEST_HOOKS
