@@ -39,8 +39,18 @@ constexpr int kCWarps = kWarps;
 #define SPEC_SEG_TILES 4
 #endif
 constexpr int kSegTiles = SPEC_SEG_TILES;  // stats tiles per segment: one partial each, never split between warps
-constexpr int kMaxGrab = 8;             // stats segments taken from the global counter at once (at most)
-constexpr int kTailZone = 4;            // below this many segments per warp left, grab without reserve
+#ifndef SPEC_MAX_GRAB
+#define SPEC_MAX_GRAB 4
+#endif
+constexpr int kMaxGrab = SPEC_MAX_GRAB;  // stats segments taken from the global counter at once (at most)
+#ifndef SPEC_TAIL_ZONE
+#define SPEC_TAIL_ZONE 16
+#endif
+#ifndef SPEC_GUIDED_DIV
+#define SPEC_GUIDED_DIV 2
+#endif
+constexpr int kTailZone = SPEC_TAIL_ZONE;    // below this many segments per warp left, grab without reserve
+constexpr int kGuidedDiv = SPEC_GUIDED_DIV;  // a grab takes 1/kGuidedDiv of a fair share of what is left
 #ifndef SPEC_KEEP_DIV
 #define SPEC_KEEP_DIV 4
 #endif

@@ -722,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     };
     // tiles to take at once: shrinks as the space runs out, so the last grabs are short
     auto guided = [&](long long left, int most) -> int {
-        const long long g = left / nwarps;
+        const long long g = left / (nwarps * kGuidedDiv);
         return static_cast<int>(g < 1 ? 1 : (g > most ? most : g));
     };
 
