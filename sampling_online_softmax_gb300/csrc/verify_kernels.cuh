@@ -69,10 +69,13 @@
 
 namespace spec {
 
-// One stage's tile: {kTileStats, tile} or {kTileResid, residual tile, entry record}.
+// One stage's tile: {kTileStats, row, tile, run's last tile} or {kTileResid, draw, entry record,
+// slice}; a residual stage also carries the geometry its issue computed: {target window's groups,
+// target vbase, draft vbase, 1 if an edge group needs fixing}.
 struct __align__(16) WarpCtl {
     unsigned long long full[kMaxStages];
     int4 desc[kMaxStages];
+    int4 cgeo[kMaxStages];
 };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
@@ -379,10 +382,18 @@ __device__ __forceinline__ void warp_merge_vi(float &v, int &i) {
         merge_vi(v, i, __shfl_xor_sync(kFull, v, off), __shfl_xor_sync(kFull, i, off));
 }
 
-__device__ __forceinline__ long long warp_sum64(long long q) {
+// The warp sums of four per-lane values at once: lanes trade halves of what they hold
+// (xor 16, then 8), then sum the one value left (xor 4, 2, 1).  Lane l returns the sum
+// of q[((l >> 4) & 1) * 2 + ((l >> 3) & 1)] over all lanes.  Integer sums are exact, so
+// the order does not matter.
+__device__ __forceinline__ long long warp_sum64x4(const long long (&q)[4], int lane) {
+    const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+    const long long a0 = (hi16 ? q[2] : q[0]) + __shfl_xor_sync(kFull, hi16 ? q[0] : q[2], 16);
+    const long long a1 = (hi16 ? q[3] : q[1]) + __shfl_xor_sync(kFull, hi16 ? q[1] : q[3], 16);
+    long long b = (hi8 ? a1 : a0) + __shfl_xor_sync(kFull, hi8 ? a0 : a1, 8);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) q += __shfl_xor_sync(kFull, q, off);
-    return q;
+    for (int off = 4; off > 0; off >>= 1) b += __shfl_xor_sync(kFull, b, off);
+    return b;
 }
 
 #ifndef SPEC_RESID_UNROLL
@@ -391,9 +402,8 @@ __device__ __forceinline__ long long warp_sum64(long long q) {
 constexpr int kResidUnroll = SPEC_RESID_UNROLL;  // group iterations of a residual tile unrolled together
 
 // ------------------------------------------------------ extra-token weights
-// The weights of a 16-byte group are summed as (w0 + w2 + w4 + ...) + (w1 + w3
-// + w5 + ...): even and odd elements in order, then the two; the packed tile
-// pass and the element-wise rescan both follow it.
+// The weights of a 16-byte group are summed by group_sum's order (below); the
+// packed tile pass and the element-wise rescans all follow it.
 // Weight of one element: pair (residual) max(0, p_v - q_v) with
 // p_v = 2^(t c - MCt) / St and q_v = 2^(d c - MCd) / Sd; tail p_v.
 // js = (MCt, 1/St, MCd, 1/Sd).  The explicit _rn intrinsics keep every
@@ -403,6 +413,20 @@ __device__ __forceinline__ float elem_weight(float t, float d, bool pair, const 
     if (!pair) return pv;
     const float qv = __fmul_rn(ptx::ex2(__fmaf_rn(d, c, -js.z)), js.w);
     return fmaxf(0.0f, __fsub_rn(pv, qv));
+}
+
+// The sum of one 16-byte group's weights: the even and the odd elements apart,
+// each as a pairwise tree, then the two.  The packed tile pass (pairs of
+// adjacent elements) forms exactly these sums, so every pass agrees bit for bit.
+template <int G>
+__device__ __forceinline__ float group_sum(const float (&w)[G]) {
+    static_assert(G == 4 || G == 8, "16-byte groups of fp32 or bf16");
+    if (G == 8) {
+        const float se = (w[0] + w[2]) + (w[4] + w[6]);
+        const float so = (w[1] + w[3]) + (w[5] + w[7]);
+        return se + so;
+    }
+    return (w[0] + w[2]) + (w[1] + w[3]);
 }
 
 // ---------------------------------------------------------- tile reductions
@@ -473,8 +497,8 @@ __device__ __forceinline__ void lane_argmax(const unsigned char *buf, int ngran,
     }
 }
 
-// Exact weight sums of one residual tile per chunk of 64 groups (every lane
-// ends with them).  Groups follow the target row's window; `same` when both
+// Exact weight sums of one residual tile per chunk of 64 groups: this lane's
+// share of each (warp_sum64x4 adds the shares up).  Groups follow the target row's window; `same` when both
 // row buffers share the 16-byte phase.  Packed fp32x2 arithmetic on element
 // pairs; every weight is the same as elem_weight's.  All 2 * kCpt groups of a
 // lane are reduced without a branch (they lie inside the row buffers); groups
@@ -513,24 +537,24 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
                 for (int k = 0; k < P; ++k) d2[k] = f2pack(d[2 * k], d[2 * k + 1]);
             }
         }
-        unsigned long long acc = 0ull;  // (even sum, odd sum)
+        unsigned long long w2[P];  // the weights of element pairs (2k, 2k + 1)
 #pragma unroll
         for (int k = 0; k < P; ++k) {
-            unsigned long long w2 = f2mul(f2ex2(f2fma(t2[k], c2, nmt)), ist);  // p of two elements
+            w2[k] = f2mul(f2ex2(f2fma(t2[k], c2, nmt)), ist);  // p of two elements
             if (pair) {
                 const unsigned long long q2 = f2mul(f2ex2(f2fma(d2[k], c2, nmd)), isd);
                 float a, b;
-                f2unpack(f2sub(w2, q2), a, b);
-                w2 = f2pack(fmaxf(0.0f, a), fmaxf(0.0f, b));
+                f2unpack(f2sub(w2[k], q2), a, b);
+                w2[k] = f2pack(fmaxf(0.0f, a), fmaxf(0.0f, b));
             }
-            acc = f2add(acc, w2);
         }
+        // (even sum, odd sum), each a pairwise tree: group_sum's order
+        const unsigned long long acc =
+            (P == 4) ? f2add(f2add(w2[0], w2[1]), f2add(w2[2 % P], w2[3 % P])) : f2add(w2[0], w2[1 % P]);
         float se, so;
         f2unpack(acc, se, so);
         q[it >> 1] += fixq(g < ngran ? se + so : 0.0f);
     }
-#pragma unroll
-    for (int ch = 0; ch < kCpt; ++ch) q[ch] = warp_sum64(q[ch]);
 }
 
 // ---------------------------------------------------------- unit layout
@@ -809,10 +833,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         return dsm + (static_cast<size_t>(warp + (s / cspr) * kCWarps) * NS * kStageBytes) +
                static_cast<size_t>(s % cspr) * kCStageBytes;
     };
-    // issue residual tile q (slice q % Sr of draw e = q / Sr, whose record is rec)
-    auto issue_resid = [&](long long q, uint32_t rec) {
-        const int e = static_cast<int>(q / p.Sr);
-        const int k = static_cast<int>(q - static_cast<long long>(e) * p.Sr);
+    // issue residual slice k of draw e, whose record is rec
+    auto issue_resid = [&](int e, int k, uint32_t rec) {
         const bool pair = (rec & kRecPair) != 0;
         const bool skip = (rec & kRecSkip) != 0;
         int u, b, pos;
@@ -825,7 +847,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         Geo g1 = g0;
         if (pair) g1 = make_geo<EB>(row_ptr<EB>(p, b, pos, 1), s0, s1, p.draft, p.d_end);
         if (lane == 0) {
-            wc.desc[s] = make_int4(kTileResid, static_cast<int>(q), static_cast<int>(rec), 0);
+            wc.desc[s] = make_int4(kTileResid, e, static_cast<int>(rec), k);
+            wc.cgeo[s] = make_int4(g0.ngran, g0.vbase, g1.vbase, (g0.patch || (pair && g1.patch)) ? 1 : 0);
             const uint32_t bar = ptx::smem_addr(&wc.full[s]);
             uint32_t bytes = 0;
             if (!skip)
@@ -1238,25 +1261,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
             for (int h = 0; h < (kCpt * kChunk) / 32; ++h) {
                 const int gi = h * 32 + lane;
-                float se = 0.f, so = 0.f;  // even and odd elements, in order
+                float w[G];
 #pragma unroll
                 for (int k2 = 0; k2 < G; ++k2) {
                     const int v = g.vbase + gi * G + k2;
-                    float w = 0.f;
+                    w[k2] = 0.f;
                     if (gi < g.ngran && v >= s0 && v < s1)
-                        w = elem_weight(Elt<EB>::gload(rt + static_cast<size_t>(v) * EB), 0.f, false, js, p.c);
-                    if (k2 & 1)
-                        so += w;
-                    else
-                        se += w;
+                        w[k2] = elem_weight(Elt<EB>::gload(rt + static_cast<size_t>(v) * EB), 0.f, false, js, p.c);
                 }
-                q[h / 2] += fixq(se + so);
+                q[h / 2] += fixq(group_sum<G>(w));
             }
-#pragma unroll
-            for (int c = 0; c < kCpt; ++c) {
-                const long long t = warp_sum64(q[c]);
-                if (lane == 0) cs[k * kCpt + c] = static_cast<unsigned long long>(t);
-            }
+            const long long t = warp_sum64x4(q, lane);  // chunk lane >> 3 on lanes 0, 8, 16, 24
+            if ((lane & 7) == 0) cs[k * kCpt + (lane >> 3)] = static_cast<unsigned long long>(t);
         }
         __syncwarp();
     };
@@ -1328,7 +1344,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int g = cc * kChunk + h * 32 + lane;
-            float se = 0.f, so = 0.f;  // the group's sum, in the tile pass's order
 #pragma unroll
             for (int k2 = 0; k2 < G; ++k2) {
                 const int v = gt.vbase + g * G + k2;
@@ -1339,12 +1354,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     we = elem_weight(t, d, pair, js, p.c);
                 }
                 w[h][k2] = we;
-                if (k2 & 1)
-                    so += we;
-                else
-                    se += we;
             }
-            q[h] = fixq(se + so);
+            q[h] = fixq(group_sum<G>(w[h]));  // the group's sum, as the tile pass forms it
         }
         long long i0 = q[0], i1 = q[1];
 #pragma unroll
@@ -1596,20 +1607,27 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         const bool cactive = warp < kCWarps;
         const long long q1 = cactive ? RT * (cw + 1) / cwarps : 0;
         long long qi = cactive ? RT * cw / cwarps : 0;   // the next tile to issue
-        int ie = -1;
+        // it is slice ik of draw ie (tracked as qi advances: no division per tile)
+        int ie = static_cast<int>(qi / p.Sr);
+        int ik = static_cast<int>(qi - static_cast<long long>(ie) * p.Sr);
         uint32_t irec = 0;
+        bool irec_ok = false;
         auto issue_next = [&]() {
-            const int e = static_cast<int>(qi / p.Sr);
-            if (e != ie) {
-                ie = e;
-                irec = __ldcg(&p.ws_draw[e]);
+            if (!irec_ok) {
+                irec_ok = true;
+                irec = __ldcg(&p.ws_draw[ie]);
                 if (irec == 0u) {          // never recorded (only after a timed-out wait): read nothing
                     timed_out = true;
                     irec = 1u | kRecSkip;
                 }
             }
-            issue_resid(qi, irec);
+            issue_resid(ie, ik, irec);
             ++qi;
+            if (++ik == p.Sr) {
+                ik = 0;
+                ++ie;
+                irec_ok = false;
+            }
         };
         while (qi < q1 && issued - handled < nst) issue_next();
         __syncwarp();
@@ -1619,11 +1637,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         while (handled < issued) {
             const int s = hslot;
             const int4 d = wc.desc[s];
+            const int4 cg = wc.cgeo[s];
             unsigned char *buf = cstage(s);
-            const long long idx = static_cast<unsigned>(d.y);
             const uint32_t rec = static_cast<uint32_t>(d.z);
-            const int e = static_cast<int>(idx / p.Sr);
-            const int k = static_cast<int>(idx - static_cast<long long>(e) * p.Sr);
+            const int e = d.y;
+            const int k = d.w;
             if (e != ce) {
                 ce = e;
                 cpair = (rec & kRecPair) != 0;
@@ -1638,15 +1656,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             long long q[kCpt];
 #pragma unroll
             for (int c = 0; c < kCpt; ++c) q[c] = 0;
-            bool patched = false;
+            const bool patched = !cskip && cg.w != 0;
             if (!cskip) {
                 const int s0 = k * p.Lr;
                 const int s1 = min(p.V, s0 + p.Lr);
-                const Geo g0 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 0), s0, s1, p.target, p.t_end);
-                Geo g1 = g0;
-                if (cpair) g1 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 1), s0, s1, p.draft, p.d_end);
-                patched = g0.patch || (cpair && g1.patch);
-                if (patched) {
+                if (patched) {  // an edge group to fix (rows off the 16-byte grid, tensor ends)
+                    const Geo g0 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 0), s0, s1, p.target, p.t_end);
+                    Geo g1 = g0;
+                    if (cpair) g1 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 1), s0, s1, p.draft, p.d_end);
                     if (lane < 16) {
                         if (g0.patch) patch_row<EB>(buf, g0, lane);
                     } else if (cpair && g1.patch) {
@@ -1654,15 +1671,16 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     }
                     __syncwarp();
                 }
-                tile_resid<EB>(buf, g0.ngran, g0.vbase, g1.vbase, s0, s1, cpair, g0.vbase == g1.vbase, js, p.c,
-                               lane, q);
+                tile_resid<EB>(buf, cg.x, cg.y, cg.z, s0, s1, cpair, cg.y == cg.z, js, p.c, lane, q);
             }
             __syncwarp();
             if (patched) fence_proxy_async();
-            if (lane == 0) {
-                unsigned long long *dst = p.ws_csum + (static_cast<size_t>(e) * p.Sr + k) * kCpt;
-#pragma unroll
-                for (int c = 0; c < kCpt; ++c) dst[c] = static_cast<unsigned long long>(q[c]);
+            {
+                // lanes 0, 8, 16 and 24 hold the sums of chunks 0, 1, 2 and 3
+                const long long t = warp_sum64x4(q, lane);
+                if ((lane & 7) == 0)
+                    p.ws_csum[(static_cast<size_t>(e) * p.Sr + k) * kCpt + (lane >> 3)] =
+                        static_cast<unsigned long long>(t);
             }
             advance_slot();
             while (qi < q1 && issued - handled < nst) issue_next();
