@@ -24,13 +24,16 @@ constexpr int kMaxStages = 4;             // mbarriers per warp: the residual ph
 constexpr int kMinCtas = SPEC_MIN_CTAS;              // CTAs resident per SM
 constexpr int kTileBytes = SPEC_TILE_KB * 1024;      // stats tile: a window of one row on the 16-byte grid
 constexpr int kStageBytes = kTileBytes;              // a stats stage of a warp's ring
-constexpr int kResidSliceBytes = 4064;               // at most this many bytes of each row per residual tile
-constexpr int kRowBuf = 4096;                        // residual row buffer: a slice plus its two ragged groups
+#ifndef SPEC_ROW_BUF
+#define SPEC_ROW_BUF 4096
+#endif
+constexpr int kRowBuf = SPEC_ROW_BUF;                // residual row buffer: a slice plus its two ragged groups
+constexpr int kResidSliceBytes = kRowBuf - 32;       // at most this many bytes of each row per residual tile
 constexpr int kCStageBytes = 2 * kRowBuf;            // a residual stage: the slice of a row pair
 constexpr int kChunk = 64;                           // 16-byte groups per residual chunk
 constexpr int kCpt = kRowBuf / 16 / kChunk;          // residual chunks per tile (the whole row buffer)
 static_assert(kResidSliceBytes % 16 == 0 && kResidSliceBytes + 32 <= kRowBuf, "a slice's window fits its buffer");
-static_assert(kRowBuf % (16 * kChunk) == 0 && kCpt == 4, "four chunks per residual tile");
+static_assert(kRowBuf % (16 * kChunk) == 0 && (kCpt == 2 || kCpt == 4), "two or four chunks per residual tile");
 static_assert(kStageBytes % kCStageBytes == 0 && kStageBytes % 128 == 0, "stage layout");
 // Warps of a CTA that reduce residual tiles (all of them: the reduction is bound by each warp's
 // dependent arithmetic, so fewer warps with deeper rings measured slower).

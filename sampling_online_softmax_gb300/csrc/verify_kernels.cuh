@@ -382,19 +382,28 @@ __device__ __forceinline__ void warp_merge_vi(float &v, int &i) {
         merge_vi(v, i, __shfl_xor_sync(kFull, v, off), __shfl_xor_sync(kFull, i, off));
 }
 
-// The warp sums of four per-lane values at once: lanes trade halves of what they hold
-// (xor 16, then 8), then sum the one value left (xor 4, 2, 1).  Lane l returns the sum
-// of q[((l >> 4) & 1) * 2 + ((l >> 3) & 1)] over all lanes.  Integer sums are exact, so
-// the order does not matter.
-__device__ __forceinline__ long long warp_sum64x4(const long long (&q)[4], int lane) {
-    const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
-    const long long a0 = (hi16 ? q[2] : q[0]) + __shfl_xor_sync(kFull, hi16 ? q[0] : q[2], 16);
-    const long long a1 = (hi16 ? q[3] : q[1]) + __shfl_xor_sync(kFull, hi16 ? q[1] : q[3], 16);
-    long long b = (hi8 ? a1 : a0) + __shfl_xor_sync(kFull, hi8 ? a0 : a1, 8);
+// The warp sums of N (2 or 4) per-lane values at once: lanes trade halves of
+// what they hold (xor 16, then 8 when N is 4), then sum the one value left.
+// Lane l returns the sum over all lanes of q[l / (32 / N)].  Integer sums are
+// exact, so the order does not matter.
+template <int N>
+__device__ __forceinline__ long long warp_sum64xN(const long long (&q)[N], int lane) {
+    static_assert(N == 2 || N == 4, "two or four values");
+    const bool hi16 = (lane & 16) != 0;
+    long long b;
+    if (N == 4) {
+        const bool hi8 = (lane & 8) != 0;
+        const long long a0 = (hi16 ? q[2 % N] : q[0]) + __shfl_xor_sync(kFull, hi16 ? q[0] : q[2 % N], 16);
+        const long long a1 = (hi16 ? q[3 % N] : q[1]) + __shfl_xor_sync(kFull, hi16 ? q[1] : q[3 % N], 16);
+        b = (hi8 ? a1 : a0) + __shfl_xor_sync(kFull, hi8 ? a0 : a1, 8);
+    } else {
+        b = (hi16 ? q[1] : q[0]) + __shfl_xor_sync(kFull, hi16 ? q[0] : q[1], 16);
+    }
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) b += __shfl_xor_sync(kFull, b, off);
+    for (int off = (N == 4) ? 4 : 8; off > 0; off >>= 1) b += __shfl_xor_sync(kFull, b, off);
     return b;
 }
+constexpr int kSumLanes = 32 / kCpt;  // lanes l with l % kSumLanes == 0 hold chunk l / kSumLanes
 
 #ifndef SPEC_RESID_UNROLL
 #define SPEC_RESID_UNROLL 4
@@ -498,7 +507,7 @@ __device__ __forceinline__ void lane_argmax(const unsigned char *buf, int ngran,
 }
 
 // Exact weight sums of one residual tile per chunk of 64 groups: this lane's
-// share of each (warp_sum64x4 adds the shares up).  Groups follow the target row's window; `same` when both
+// share of each (warp_sum64xN adds the shares up).  Groups follow the target row's window; `same` when both
 // row buffers share the 16-byte phase.  Packed fp32x2 arithmetic on element
 // pairs; every weight is the same as elem_weight's.  All 2 * kCpt groups of a
 // lane are reduced without a branch (they lie inside the row buffers); groups
@@ -516,44 +525,52 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
     const unsigned long long nmt = f2pack(-js.x, -js.x), ist = f2pack(js.y, js.y);
     const unsigned long long nmd = f2pack(-js.z, -js.z), isd = f2pack(js.w, js.w);
     static_assert(kChunk == 64 && 2 * kCpt * 32 * 16 == kRowBuf, "two groups per lane and chunk, covering the buffer");
+    // Chunk ch's two groups are summed into `cs`, which then enters q[kCpt - 1] as the
+    // earlier chunks shift down (after kCpt chunks q[c] is chunk c): every index stays a
+    // compile-time constant under a partial unroll, so q lives in registers.
+#pragma unroll (kResidUnroll / 2)
+    for (int ch = 0; ch < kCpt; ++ch) {
+        long long cs = 0;
 #pragma unroll
-    for (int ch = 0; ch < kCpt; ++ch) q[ch] = 0;
-#pragma unroll (kResidUnroll)
-    for (int it = 0; it < 2 * kCpt; ++it) {
-        const int g = it * 32 + lane;  // chunk it / 2
-        unsigned long long t2[P], d2[P];
-        Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bt + 16 * g), t2);
-        if (pair) {
-            if (same) {
-                Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bd + 16 * g), d2);
-            } else {
-                float d[G];
-#pragma unroll
-                for (int k = 0; k < G; ++k) {
-                    const int v = vbase0 + g * G + k;
-                    d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(bd + (v - vbase1) * EB) : neg_inf();
-                }
-#pragma unroll
-                for (int k = 0; k < P; ++k) d2[k] = f2pack(d[2 * k], d[2 * k + 1]);
-            }
-        }
-        unsigned long long w2[P];  // the weights of element pairs (2k, 2k + 1)
-#pragma unroll
-        for (int k = 0; k < P; ++k) {
-            w2[k] = f2mul(f2ex2(f2fma(t2[k], c2, nmt)), ist);  // p of two elements
+        for (int h = 0; h < 2; ++h) {
+            const int g = (2 * ch + h) * 32 + lane;
+            unsigned long long t2[P], d2[P];
+            Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bt + 16 * g), t2);
             if (pair) {
-                const unsigned long long q2 = f2mul(f2ex2(f2fma(d2[k], c2, nmd)), isd);
-                float a, b;
-                f2unpack(f2sub(w2[k], q2), a, b);
-                w2[k] = f2pack(fmaxf(0.0f, a), fmaxf(0.0f, b));
+                if (same) {
+                    Elt<EB>::pairs(*reinterpret_cast<const uint4 *>(bd + 16 * g), d2);
+                } else {
+                    float d[G];
+#pragma unroll
+                    for (int k = 0; k < G; ++k) {
+                        const int v = vbase0 + g * G + k;
+                        d[k] = (v >= s0 && v < s1) ? Elt<EB>::load(bd + (v - vbase1) * EB) : neg_inf();
+                    }
+#pragma unroll
+                    for (int k = 0; k < P; ++k) d2[k] = f2pack(d[2 * k], d[2 * k + 1]);
+                }
             }
+            unsigned long long w2[P];  // the weights of element pairs (2k, 2k + 1)
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                w2[k] = f2mul(f2ex2(f2fma(t2[k], c2, nmt)), ist);  // p of two elements
+                if (pair) {
+                    const unsigned long long q2 = f2mul(f2ex2(f2fma(d2[k], c2, nmd)), isd);
+                    float a, b;
+                    f2unpack(f2sub(w2[k], q2), a, b);
+                    w2[k] = f2pack(fmaxf(0.0f, a), fmaxf(0.0f, b));
+                }
+            }
+            // (even sum, odd sum), each a pairwise tree: group_sum's order
+            const unsigned long long acc =
+                (P == 4) ? f2add(f2add(w2[0], w2[1]), f2add(w2[2 % P], w2[3 % P])) : f2add(w2[0], w2[1 % P]);
+            float se, so;
+            f2unpack(acc, se, so);
+            cs += fixq(g < ngran ? se + so : 0.0f);
         }
-        // (even sum, odd sum), each a pairwise tree: group_sum's order
-        const unsigned long long acc =
-            (P == 4) ? f2add(f2add(w2[0], w2[1]), f2add(w2[2 % P], w2[3 % P])) : f2add(w2[0], w2[1 % P]);
-        float se, so;
-        f2unpack(acc, se, so);
-        q[it >> 1] += fixq(g < ngran ? se + so : 0.0f);
+#pragma unroll
+        for (int c = 0; c + 1 < kCpt; ++c) q[c] = q[c + 1];
+        q[kCpt - 1] = cs;
     }
 }
 
@@ -948,13 +965,19 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     unsigned pend_old = 0;             // lane 0
 
     // ----------------------------------------------------- finishing side
-    // Emit the sequence: the first j draft tokens, then `extra` (if any), then -1.
-    auto emit_linear = [&](int b, int j, int extra, bool has_extra) {
+    // Draft token `lane` of sequence b when lane < j (else -1): loaded ahead of an emission.
+    auto lane_draft_token = [&](int b, int j) -> int {
+        return (lane < j && lane < p.K && p.out_tokens) ? __ldg(&p.tokens[static_cast<size_t>(b) * p.K + lane]) : -1;
+    };
+    // Emit the sequence: the first j draft tokens, then `extra` (if any), then -1.  `pre` is
+    // lane_draft_token(b, j).
+    auto emit_linear = [&](int b, int j, int extra, bool has_extra, int pre) {
         const int K = p.K;
         if (p.out_tokens) {
             for (int i = lane; i <= K; i += 32)
                 p.out_tokens[static_cast<size_t>(b) * (K + 1) + i] =
-                    (i < j) ? __ldg(&p.tokens[static_cast<size_t>(b) * K + i]) : ((i == j && has_extra) ? extra : -1);
+                    (i < j) ? (i < 32 ? pre : __ldg(&p.tokens[static_cast<size_t>(b) * K + i]))
+                            : ((i == j && has_extra) ? extra : -1);
         }
         if (lane == 0) {
             p.accept_len[b] = j;
@@ -1036,13 +1059,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 if (skip < 0) skip = (__ldcg(&p.ws_stats[u]).y > 0.f) ? 0 : 1;  // a non-finite unit recorded 1/St = 0
                 set_draw(b, u, j < p.K, skip != 0);
             } else {
-                emit_linear(b, j, -1, false);
+                emit_linear(b, j, -1, false, lane_draft_token(b, j));
             }
         } else if (MODE == kLinearGreedy) {
+            const int pre = lane_draft_token(b, j);
             const int extra = (p.u_bonus != nullptr) ? __ldcg(&p.ws_val[u]) : -1;
             __syncwarp();
             if (lane == 0) p.ws_val[u] = 0;
-            emit_linear(b, j, extra, p.u_bonus != nullptr);
+            emit_linear(b, j, extra, p.u_bonus != nullptr, pre);
         }
         __syncwarp();
     };
@@ -1271,8 +1295,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 }
                 q[h / 2] += fixq(group_sum<G>(w));
             }
-            const long long t = warp_sum64x4(q, lane);  // chunk lane >> 3 on lanes 0, 8, 16, 24
-            if ((lane & 7) == 0) cs[k * kCpt + (lane >> 3)] = static_cast<unsigned long long>(t);
+            const long long t = warp_sum64xN<kCpt>(q, lane);
+            if (lane % kSumLanes == 0) cs[k * kCpt + lane / kSumLanes] = static_cast<unsigned long long>(t);
         }
         __syncwarp();
     };
@@ -1412,6 +1436,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             b = u / p.units_per_seq;
             pos = u - b * p.units_per_seq;
         }
+        // the draft tokens to emit, loaded while the token is located
+        const int pre = (T::kBonus || MODE == kTreeSample) ? -1 : lane_draft_token(b, pos);
         int token = 0;
         if (!skip) {
             token = select_token(e, b, pos, pair, js, ub);
@@ -1428,7 +1454,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         } else if (MODE == kTreeSample) {
             if (lane == 0) p.ws_val[u] = token;  // the target's choice at node pos
         } else {
-            emit_linear(b, pos, token, true);
+            emit_linear(b, pos, token, true, pre);
         }
         // leave the workspace zeroed
         unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
@@ -1676,10 +1702,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             __syncwarp();
             if (patched) fence_proxy_async();
             {
-                // lanes 0, 8, 16 and 24 hold the sums of chunks 0, 1, 2 and 3
-                const long long t = warp_sum64x4(q, lane);
-                if ((lane & 7) == 0)
-                    p.ws_csum[(static_cast<size_t>(e) * p.Sr + k) * kCpt + (lane >> 3)] =
+                const long long t = warp_sum64xN<kCpt>(q, lane);
+                if (lane % kSumLanes == 0)
+                    p.ws_csum[(static_cast<size_t>(e) * p.Sr + k) * kCpt + lane / kSumLanes] =
                         static_cast<unsigned long long>(t);
             }
             advance_slot();
