@@ -234,6 +234,10 @@ struct Elt<4> {
     __device__ __forceinline__ static void copy(unsigned char *dst, const unsigned char *src) {
         *reinterpret_cast<uint32_t *>(dst) = __ldg(reinterpret_cast<const uint32_t *>(src));
     }
+    // max of one group's elements (NaN only if all are NaN)
+    __device__ __forceinline__ static float max16(const uint4 &w) {
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
     __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1) {
         float m = neg_inf();
 #pragma unroll 4
@@ -277,6 +281,11 @@ struct Elt<2> {
     }
     __device__ __forceinline__ static void copy(unsigned char *dst, const unsigned char *src) {
         *reinterpret_cast<uint16_t *>(dst) = __ldg(reinterpret_cast<const unsigned short *>(src));
+    }
+    // max of one group's elements (NaN only if all are NaN)
+    __device__ __forceinline__ static float max16(const uint4 &w) {
+        const uint32_t m = ptx::bmax2(ptx::bmax2(w.x, w.y), ptx::bmax2(w.z, w.w));
+        return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
     }
     __device__ __forceinline__ static float group_max(const unsigned char *buf, int g0, int g1) {
         uint32_t m = 0xff80ff80u;  // (-inf, -inf)
@@ -490,33 +499,51 @@ __device__ __forceinline__ void lane_sum(const unsigned char *buf, int ngran, fl
 }
 
 // Add one stats tile to this lane's running (max, lowest index of the max).
+// The lane's best group comes first (its elements' max, a tree with no index), then the
+// lowest element of that group holding it: the lane's elements run in index order, so a
+// strictly greater max is needed to move (ties keep the lowest index; NaN never wins).
 template <int EB>
 __device__ __forceinline__ void lane_argmax(const unsigned char *buf, int ngran, int vbase, int lane, float &bv,
                                             int &bi) {
     constexpr int G = Elt<EB>::G;
+    float tm = neg_inf();
+    int tg = -1;
+#pragma unroll 4
     for (int g = lane; g < ngran; g += 32) {
+        const float gm = Elt<EB>::max16(*reinterpret_cast<const uint4 *>(buf + 16 * g));
+        if (gm > tm) {
+            tm = gm;
+            tg = g;
+        }
+    }
+    if (tm > bv) {
         float va[G];
-        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(buf + 16 * g), va);
+        Elt<EB>::unpack(*reinterpret_cast<const uint4 *>(buf + 16 * tg), va);
+        int k0 = G - 1;
 #pragma unroll
-        for (int k = 0; k < G; ++k)
-            if (va[k] > bv) {
-                bv = va[k];
-                bi = vbase + g * G + k;
-            }
+        for (int k = G - 1; k >= 0; --k)
+            if (va[k] == tm) k0 = k;
+        bv = tm;
+        bi = vbase + tg * G + k0;
     }
 }
 
 // Exact weight sums of one residual tile per chunk of 64 groups: this lane's
-// share of each (warp_sum64xN adds the shares up).  Groups follow the target row's window; `same` when both
-// row buffers share the 16-byte phase.  Packed fp32x2 arithmetic on element
+// share of each (warp_sum64xN adds the shares up).  Groups follow the target
+// row's window.  Packed fp32x2 arithmetic on element
 // pairs; every weight is the same as elem_weight's.  All 2 * kCpt groups of a
 // lane are reduced without a branch (they lie inside the row buffers); groups
 // past the window hold stale bytes and are given no weight, so the iterations
 // are independent and overlap.
-template <int EB>
+// KIND (fixed at compile time, so the unrolled groups carry no branch): kResidTail, a target
+// row alone; kResidPair, a row pair whose buffers share the 16-byte phase; kResidPairShifted,
+// a row pair whose draft row is read element by element.
+constexpr int kResidTail = 0, kResidPair = 1, kResidPairShifted = 2;
+template <int EB, int KIND>
 __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, int vbase0, int vbase1, int s0,
-                                           int s1, bool pair, bool same, const float4 &js, float c, int lane,
-                                           long long (&q)[kCpt]) {
+                                           int s1, const float4 &js, float c, int lane, long long (&q)[kCpt]) {
+    constexpr bool pair = KIND != kResidTail;
+    constexpr bool same = KIND == kResidPair;
     constexpr int G = Elt<EB>::G;
     constexpr int P = Elt<EB>::P;
     const unsigned char *bt = buf;
@@ -528,7 +555,7 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
     // Chunk ch's two groups are summed into `cs`, which then enters q[kCpt - 1] as the
     // earlier chunks shift down (after kCpt chunks q[c] is chunk c): every index stays a
     // compile-time constant under a partial unroll, so q lives in registers.
-#pragma unroll (kResidUnroll / 2)
+#pragma unroll (KIND == kResidPairShifted ? 1 : kResidUnroll / 2)
     for (int ch = 0; ch < kCpt; ++ch) {
         long long cs = 0;
 #pragma unroll
@@ -850,19 +877,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         return dsm + (static_cast<size_t>(warp + (s / cspr) * kCWarps) * NS * kStageBytes) +
                static_cast<size_t>(s % cspr) * kCStageBytes;
     };
-    // issue residual slice k of draw e, whose record is rec
-    auto issue_resid = [&](int e, int k, uint32_t rec) {
+    // issue residual slice k of draw e: record rec, rows rt (target) and rd (draft, pairs only)
+    auto issue_resid = [&](int e, int k, uint32_t rec, const unsigned char *rt, const unsigned char *rd) {
         const bool pair = (rec & kRecPair) != 0;
         const bool skip = (rec & kRecSkip) != 0;
-        int u, b, pos;
-        entry_unit(rec, u, b, pos);
         const int s = next_islot();
         unsigned char *buf = cstage(s);
         const int s0 = k * p.Lr;
         const int s1 = min(p.V, s0 + p.Lr);
-        const Geo g0 = make_geo<EB>(row_ptr<EB>(p, b, pos, 0), s0, s1, p.target, p.t_end);
+        const Geo g0 = make_geo<EB>(rt, s0, s1, p.target, p.t_end);
         Geo g1 = g0;
-        if (pair) g1 = make_geo<EB>(row_ptr<EB>(p, b, pos, 1), s0, s1, p.draft, p.d_end);
+        if (pair) g1 = make_geo<EB>(rd, s0, s1, p.draft, p.d_end);
         if (lane == 0) {
             wc.desc[s] = make_int4(kTileResid, e, static_cast<int>(rec), k);
             wc.cgeo[s] = make_int4(g0.ngran, g0.vbase, g1.vbase, (g0.patch || (pair && g1.patch)) ? 1 : 0);
@@ -1610,22 +1635,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         // residual tiles [RT * gw / W, RT * (gw + 1) / W): slices of the drawn row
         // pairs (or rows), each reduced to exact chunk sums of its weights.
         if (!grid_barrier(&p.ws_ctrl[5], gridDim.x, &s_flag)) timed_out = true;
-        // The selects of phase D are spread over the grid (consecutive draws on different SMs):
-        // warp gw selects draws [n * gw / W, n * (gw + 1) / W).  Their records, statistics and
-        // uniforms are complete now; load them ahead of the selects.
-        const long long nd = p.n_draws;
-        const int d0 = static_cast<int>(nd * gw / nwarps), d1 = static_cast<int>(nd * (gw + 1) / nwarps);
-        uint32_t drec = 0u;
-        float4 djs = make_float4(0.f, 0.f, 0.f, 0.f);
-        float dub = 0.f;
-        if (d0 < d1) {
-            drec = __ldcg(&p.ws_draw[d0]);
-            if (drec != 0u && !(drec & kRecSkip)) {
-                const int u = static_cast<int>(drec & kRecUnit) - 1;
-                djs = __ldcg(&p.ws_stats[u]);
-                dub = __ldg(&p.u_bonus[(MODE == kTreeSample || T::kBonus) ? u : u / p.units_per_seq]);
-            }
-        }
         nst = NSC;  // nothing is in flight: re-cut the ring(s) into NSC residual stages
         islot = hslot = 0;
         const long long cwarps = static_cast<long long>(gridDim.x) * kCWarps;
@@ -1636,18 +1645,40 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         // it is slice ik of draw ie (tracked as qi advances: no division per tile)
         int ie = static_cast<int>(qi / p.Sr);
         int ik = static_cast<int>(qi - static_cast<long long>(ie) * p.Sr);
-        uint32_t irec = 0;
-        bool irec_ok = false;
+        // The selects of phase D are spread over the grid (consecutive draws on different SMs):
+        // warp gw selects draws [n * gw / W, n * (gw + 1) / W).  Every record is complete now:
+        // the first one this warp issues and the first one it selects load together.
+        const long long nd = p.n_draws;
+        const int d0 = static_cast<int>(nd * gw / nwarps), d1 = static_cast<int>(nd * (gw + 1) / nwarps);
+        uint32_t irec = (qi < q1) ? __ldcg(&p.ws_draw[ie]) : 0u;
+        uint32_t drec = (d0 < d1) ? __ldcg(&p.ws_draw[d0]) : 0u;
+        bool irec_ok = true;
+        // The draw being issued, decoded once: its rows; its statistics are loaded for the
+        // reducing side (hand_e / hand_js), which reaches the draw a tile or two later.
+        const unsigned char *irt = nullptr, *ird = nullptr;
+        int hand_e = -1;
+        float4 hand_js = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto begin_draw = [&]() {
+            if (irec == 0u) {          // never recorded (only after a timed-out wait): read nothing
+                timed_out = true;
+                irec = 1u | kRecSkip;
+            }
+            int u, b, pos;
+            entry_unit(irec, u, b, pos);
+            irt = row_ptr<EB>(p, b, pos, 0);
+            ird = (irec & kRecPair) ? row_ptr<EB>(p, b, pos, 1) : irt;
+            if (!(irec & kRecSkip)) {
+                hand_e = ie;
+                hand_js = __ldcg(&p.ws_stats[u]);
+            }
+        };
         auto issue_next = [&]() {
             if (!irec_ok) {
                 irec_ok = true;
                 irec = __ldcg(&p.ws_draw[ie]);
-                if (irec == 0u) {          // never recorded (only after a timed-out wait): read nothing
-                    timed_out = true;
-                    irec = 1u | kRecSkip;
-                }
+                begin_draw();
             }
-            issue_resid(ie, ik, irec);
+            issue_resid(ie, ik, irec, irt, ird);
             ++qi;
             if (++ik == p.Sr) {
                 ik = 0;
@@ -1655,9 +1686,18 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 irec_ok = false;
             }
         };
+        if (qi < q1) begin_draw();
         while (qi < q1 && issued - handled < nst) issue_next();
         __syncwarp();
-        int ce = -1, cu = 0, cb = 0, cpos = 0;
+        // phase D's statistics and uniform for its first draw: not needed before then
+        float4 djs = make_float4(0.f, 0.f, 0.f, 0.f);
+        float dub = 0.f;
+        if (d0 < d1 && drec != 0u && !(drec & kRecSkip)) {
+            const int u = static_cast<int>(drec & kRecUnit) - 1;
+            djs = __ldcg(&p.ws_stats[u]);
+            dub = __ldg(&p.u_bonus[(MODE == kTreeSample || T::kBonus) ? u : u / p.units_per_seq]);
+        }
+        int ce = -1, cu = 0;
         bool cpair = false, cskip = true;
         float4 js = make_float4(0.f, 0.f, 0.f, 0.f);
         while (handled < issued) {
@@ -1672,8 +1712,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 ce = e;
                 cpair = (rec & kRecPair) != 0;
                 cskip = (rec & kRecSkip) != 0;
-                entry_unit(rec, cu, cb, cpos);
-                if (!cskip) js = __ldcg(&p.ws_stats[cu]);
+                cu = static_cast<int>(rec & kRecUnit) - 1;
+                if (!cskip) js = (e == hand_e) ? hand_js : __ldcg(&p.ws_stats[cu]);
             }
             if (!wait_bar(ptx::smem_addr(&wc.full[s]), (bar_par >> s) & 1u)) {
                 timed_out = true;
@@ -1687,6 +1727,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 const int s0 = k * p.Lr;
                 const int s1 = min(p.V, s0 + p.Lr);
                 if (patched) {  // an edge group to fix (rows off the 16-byte grid, tensor ends)
+                    int cuu, cb, cpos;
+                    entry_unit(rec, cuu, cb, cpos);
                     const Geo g0 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 0), s0, s1, p.target, p.t_end);
                     Geo g1 = g0;
                     if (cpair) g1 = make_geo<EB>(row_ptr<EB>(p, cb, cpos, 1), s0, s1, p.draft, p.d_end);
@@ -1697,7 +1739,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                     }
                     __syncwarp();
                 }
-                tile_resid<EB>(buf, cg.x, cg.y, cg.z, s0, s1, cpair, cg.y == cg.z, js, p.c, lane, q);
+                if (!cpair)
+                    tile_resid<EB, kResidTail>(buf, cg.x, cg.y, cg.z, s0, s1, js, p.c, lane, q);
+                else if (cg.y == cg.z)
+                    tile_resid<EB, kResidPair>(buf, cg.x, cg.y, cg.z, s0, s1, js, p.c, lane, q);
+                else
+                    tile_resid<EB, kResidPairShifted>(buf, cg.x, cg.y, cg.z, s0, s1, js, p.c, lane, q);
             }
             __syncwarp();
             if (patched) fence_proxy_async();
