@@ -186,11 +186,6 @@ __device__ __forceinline__ unsigned long long f2mul(unsigned long long a, unsign
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ unsigned long long f2sub(unsigned long long a, unsigned long long b) {
-    unsigned long long d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 __device__ __forceinline__ unsigned long long f2ex2(unsigned long long v) {
     float a, b;
     f2unpack(v, a, b);
@@ -424,13 +419,14 @@ constexpr int kResidUnroll = SPEC_RESID_UNROLL;  // group iterations of a residu
 // packed tile pass and the element-wise rescans all follow it.
 // Weight of one element: pair (residual) max(0, p_v - q_v) with
 // p_v = 2^(t c - MCt) / St and q_v = 2^(d c - MCd) / Sd; tail p_v.
-// js = (MCt, 1/St, MCd, 1/Sd).  The explicit _rn intrinsics keep every
-// evaluation of a weight bit-identical (no contraction into an FMA).
+// js = (MCt, 1/St, MCd, 1/Sd).  The pair weight is one fused multiply-add,
+// 2^(t c - MCt) * (1/St) + (-q_v), so p_v is never rounded on its own.  The
+// explicit _rn intrinsics keep every evaluation of a weight bit-identical.
 __device__ __forceinline__ float elem_weight(float t, float d, bool pair, const float4 &js, float c) {
-    const float pv = __fmul_rn(ptx::ex2(__fmaf_rn(t, c, -js.x)), js.y);
-    if (!pair) return pv;
-    const float qv = __fmul_rn(ptx::ex2(__fmaf_rn(d, c, -js.z)), js.w);
-    return fmaxf(0.0f, __fsub_rn(pv, qv));
+    const float et = ptx::ex2(__fmaf_rn(t, c, -js.x));
+    if (!pair) return __fmul_rn(et, js.y);
+    const float nqv = __fmul_rn(ptx::ex2(__fmaf_rn(d, c, -js.z)), -js.w);  // -q_v, exactly
+    return fmaxf(0.0f, __fmaf_rn(et, js.y, nqv));
 }
 
 // The sum of one 16-byte group's weights: the even and the odd elements apart,
@@ -550,7 +546,7 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
     const unsigned char *bd = buf + kRowBuf;
     const unsigned long long c2 = f2pack(c, c);
     const unsigned long long nmt = f2pack(-js.x, -js.x), ist = f2pack(js.y, js.y);
-    const unsigned long long nmd = f2pack(-js.z, -js.z), isd = f2pack(js.w, js.w);
+    const unsigned long long nmd = f2pack(-js.z, -js.z), nisd = f2pack(-js.w, -js.w);
     static_assert(kChunk == 64 && 2 * kCpt * 32 * 16 == kRowBuf, "two groups per lane and chunk, covering the buffer");
     // Chunk ch's two groups are summed into `cs`, which then enters q[kCpt - 1] as the
     // earlier chunks shift down (after kCpt chunks q[c] is chunk c): every index stays a
@@ -580,12 +576,14 @@ __device__ __forceinline__ void tile_resid(const unsigned char *buf, int ngran, 
             unsigned long long w2[P];  // the weights of element pairs (2k, 2k + 1)
 #pragma unroll
             for (int k = 0; k < P; ++k) {
-                w2[k] = f2mul(f2ex2(f2fma(t2[k], c2, nmt)), ist);  // p of two elements
+                const unsigned long long et = f2ex2(f2fma(t2[k], c2, nmt));
                 if (pair) {
-                    const unsigned long long q2 = f2mul(f2ex2(f2fma(d2[k], c2, nmd)), isd);
+                    const unsigned long long nq2 = f2mul(f2ex2(f2fma(d2[k], c2, nmd)), nisd);  // -q of two elements
                     float a, b;
-                    f2unpack(f2sub(w2[k], q2), a, b);
+                    f2unpack(f2fma(et, ist, nq2), a, b);
                     w2[k] = f2pack(fmaxf(0.0f, a), fmaxf(0.0f, b));
+                } else {
+                    w2[k] = f2mul(et, ist);  // p of two elements
                 }
             }
             // (even sum, odd sum), each a pairwise tree: group_sum's order
