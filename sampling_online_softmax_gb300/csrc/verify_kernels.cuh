@@ -1073,8 +1073,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
 
     // The first rejection j of linear sequence b is known: record its draw of the
     // extra token, or emit the sequence; unit j's scratch is ours.
-    // skip: 1 / 0 when the caller knows whether unit j is non-finite, -1 if not.
-    auto draw_or_emit = [&](int b, int j, int skip) {
+    // skip: 1 / 0 when the caller knows whether unit j is non-finite, -1 if not.  own: unit
+    // j's argmax when the caller has just found it (greedy), else INT_MIN.  pre: this lane's
+    // draft token, lane_draft_token(b, K) (valid wherever lane < j).
+    auto draw_or_emit = [&](int b, int j, int skip, int own, int pre) {
         const int U = p.units_per_seq;
         const int u = b * U + j;
         if (MODE == kLinearSample) {
@@ -1082,11 +1084,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 if (skip < 0) skip = (__ldcg(&p.ws_stats[u]).y > 0.f) ? 0 : 1;  // a non-finite unit recorded 1/St = 0
                 set_draw(b, u, j < p.K, skip != 0);
             } else {
-                emit_linear(b, j, -1, false, lane_draft_token(b, j));
+                emit_linear(b, j, -1, false, pre);
             }
         } else if (MODE == kLinearGreedy) {
-            const int pre = lane_draft_token(b, j);
-            const int extra = (p.u_bonus != nullptr) ? __ldcg(&p.ws_val[u]) : -1;
+            const int extra = (p.u_bonus == nullptr) ? -1 : (own != INT_MIN ? own : __ldcg(&p.ws_val[u]));
             __syncwarp();
             if (lane == 0) p.ws_val[u] = 0;
             emit_linear(b, j, extra, p.u_bonus != nullptr, pre);
@@ -1139,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
                 break;
             }
         }
-        draw_or_emit(b, j, -1);
+        draw_or_emit(b, j, -1, INT_MIN, lane_draft_token(b, j));
         cleanup_seq(b, j, false);
     };
 
@@ -1147,9 +1148,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     auto finish_unit = [&](int u, int b, int pos) {
         const int K = p.K;
         const int nrows = unit_nrows<MODE>(p, pos);
-        // the decision's inputs, loaded while the partials are merged
+        // the decision's inputs, loaded while the partials are merged (and the draft tokens, for
+        // an emission at the end)
         int x = -1;
         float ua = 0.f;
+        const int pre = ((MODE == kLinearSample && !draws) || MODE == kLinearGreedy) ? lane_draft_token(b, K) : -1;
         if ((MODE == kLinearSample || MODE == kLinearGreedy) && pos >= 0 && pos < K) {
             x = __ldg(&p.tokens[static_cast<size_t>(b) * K + pos]);
             if (MODE == kLinearSample) ua = __ldg(&p.u_accept[static_cast<size_t>(b) * K + pos]);
@@ -1281,7 +1284,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             __syncwarp();
             const unsigned long long now = old | bits;
             const int jn = first_rejection(now, K);
-            if (first_rejection(old, K) < 0 && jn >= 0) draw_or_emit(b, jn, jn == pos ? (finite ? 0 : 1) : -1);
+            if (first_rejection(old, K) < 0 && jn >= 0)
+                draw_or_emit(b, jn, jn == pos ? (finite ? 0 : 1) : -1, (!T::kSample && jn == pos) ? Ar[0] : INT_MIN,
+                             pre);
             if (__popc(static_cast<unsigned>(now)) == K + 1) cleanup_seq(b, jn, true);
             return;
         }
