@@ -453,12 +453,14 @@ ALONE = {
 # committed ncu summaries (profiles/) behind each configuration's traffic figure
 CONFIG_PROFILES = {
     "small_T1": "spec_verify_kernel_linear_sample_small.md",
+    "small_greedy": "spec_verify_kernel_linear_greedy_small.md",
     "draft_target_T0.7": "spec_verify_kernel_linear_sample_draft_target.md",
     "mtp_greedy": "spec_verify_kernel_linear_greedy_mtp.md",
     "mtp_T1": "spec_verify_kernel_linear_sample_mtp.md",
     "medusa_tree_greedy": "spec_verify_kernel_tree_greedy_medusa.md",
     "medusa_tree_sampled_T1": "spec_verify_kernel_tree_sample_medusa.md",
     "draft_sampler_T0.7": "spec_verify_kernel_bonus_sample_draft_rows.md",
+    "draft_sampler_greedy": "spec_verify_kernel_bonus_greedy_draft_rows.md",
     "medusa_tree_mask": "tree_mask_kernel_medusa.md",
     "mtp_plug_T1": "mtp_plug_kernel_mtp.md",
 }
