@@ -68,6 +68,13 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// A read-only 32-bit load issued where it stands: the volatile form keeps the compiler from
+// sinking it to its first use, so a value wanted much later is in flight meanwhile.
+__device__ __forceinline__ int ld_nc_early(const int *p) {
+    int v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
 // Lane-wise max of two packed bf16 pairs.
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     uint32_t r;

@@ -990,7 +990,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     // ----------------------------------------------------- finishing side
     // Draft token `lane` of sequence b when lane < j (else -1): loaded ahead of an emission.
     auto lane_draft_token = [&](int b, int j) -> int {
-        return (lane < j && lane < p.K && p.out_tokens) ? __ldg(&p.tokens[static_cast<size_t>(b) * p.K + lane]) : -1;
+        return (lane < j && lane < p.K && p.out_tokens) ? ptx::ld_nc_early(&p.tokens[static_cast<size_t>(b) * p.K + lane])
+                                                       : -1;
     };
     // Emit the sequence: the first j draft tokens, then `extra` (if any), then -1.  `pre` is
     // lane_draft_token(b, j).
