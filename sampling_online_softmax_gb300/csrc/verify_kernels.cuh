@@ -701,8 +701,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     const int warp = threadIdx.x >> 5;
     WarpCtl &wc = wctl[warp];
     const int NS = p.nstage;  // stats stages of the ring; the residual phase splits the same bytes finer
-    const int NSC = min(kMaxStages, (kWarps / kCWarps) * NS * kStageBytes / kCStageBytes);
-    const int cspr = NS * kStageBytes / kCStageBytes;  // residual stages within one warp's ring
+    static_assert(kCWarps == kWarps, "every warp reduces residual tiles in its own ring");
+    const int NSC = min(kMaxStages, NS * kStageBytes / kCStageBytes);  // residual stages of a warp's ring
     unsigned char *ring = dsm + static_cast<size_t>(warp) * NS * kStageBytes;
     int *tscratch = reinterpret_cast<int *>(dsm + static_cast<size_t>(kWarps) * NS * kStageBytes) +
                     static_cast<size_t>(warp) * 3 * p.units_per_seq;
@@ -869,12 +869,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         ++issued;
     };
 
-    // Residual stage s of this warp: stages beyond its own ring lie in the rings of the warps
-    // kCWarps, 2 * kCWarps, ... above it, which reduce no residual tiles.
-    auto cstage = [&](int s) -> unsigned char * {
-        return dsm + (static_cast<size_t>(warp + (s / cspr) * kCWarps) * NS * kStageBytes) +
-               static_cast<size_t>(s % cspr) * kCStageBytes;
-    };
+    // Residual stage s of this warp: the ring re-cut into stages of kCStageBytes.
+    auto cstage = [&](int s) -> unsigned char * { return ring + static_cast<size_t>(s) * kCStageBytes; };
     // issue residual slice k of draw e: record rec, rows rt (target) and rd (draft, pairs only)
     auto issue_resid = [&](int e, int k, uint32_t rec, const unsigned char *rt, const unsigned char *rd) {
         const bool pair = (rec & kRecPair) != 0;
@@ -1641,11 +1637,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         if (!grid_barrier(&p.ws_ctrl[5], gridDim.x, &s_flag)) timed_out = true;
         nst = NSC;  // nothing is in flight: re-cut the ring(s) into NSC residual stages
         islot = hslot = 0;
-        const long long cwarps = static_cast<long long>(gridDim.x) * kCWarps;
-        const long long cw = static_cast<long long>(blockIdx.x) * kCWarps + warp;
-        const bool cactive = warp < kCWarps;
-        const long long q1 = cactive ? RT * (cw + 1) / cwarps : 0;
-        long long qi = cactive ? RT * cw / cwarps : 0;   // the next tile to issue
+        const long long q1 = RT * (gw + 1) / nwarps;
+        long long qi = RT * gw / nwarps;   // the next tile to issue
         // it is slice ik of draw ie (tracked as qi advances: no division per tile)
         int ie = static_cast<int>(qi / p.Sr);
         int ik = static_cast<int>(qi - static_cast<long long>(ie) * p.Sr);
