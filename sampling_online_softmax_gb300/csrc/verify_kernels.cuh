@@ -1650,6 +1650,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         uint32_t irec = (qi < q1) ? __ldcg(&p.ws_draw[ie]) : 0u;
         uint32_t drec = (d0 < d1) ? __ldcg(&p.ws_draw[d0]) : 0u;
         bool irec_ok = true;
+        // the record of the next draw this warp issues, loaded one draw ahead
+        uint32_t nrec = (qi < q1 && ie + 1 < nd && static_cast<long long>(ie + 1) * p.Sr < q1) ? __ldcg(&p.ws_draw[ie + 1]) : 0u;
         // The draw being issued, decoded once: its rows; its statistics are loaded for the
         // reducing side (hand_e / hand_js), which reaches the draw a tile or two later.
         const unsigned char *irt = nullptr, *ird = nullptr;
@@ -1672,7 +1674,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         auto issue_next = [&]() {
             if (!irec_ok) {
                 irec_ok = true;
-                irec = __ldcg(&p.ws_draw[ie]);
+                irec = nrec;
+                nrec = (ie + 1 < nd && static_cast<long long>(ie + 1) * p.Sr < q1) ? __ldcg(&p.ws_draw[ie + 1]) : 0u;
                 begin_draw();
             }
             issue_resid(ie, ik, irec, irt, ird);
