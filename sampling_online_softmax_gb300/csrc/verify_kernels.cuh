@@ -97,6 +97,11 @@ __device__ __forceinline__ unsigned long long atom_or_acq_rel64(unsigned long lo
     asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
     return old;
 }
+__device__ __forceinline__ unsigned long long atom_or_relaxed64(unsigned long long *p, unsigned long long v) {
+    unsigned long long old;
+    asm volatile("atom.relaxed.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
 // First rejected position of a sequence once it is known from a decided /
 // accepted mask (every earlier position decided and accepted), K when every
 // position 0..K is decided and none rejected, else -1.  K < 32.
@@ -721,6 +726,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
     const long long nwarps = static_cast<long long>(gridDim.x) * kWarps;
     const long long gw = static_cast<long long>(blockIdx.x) * kWarps + warp;  // this warp's index in the grid
     bool timed_out = false;
+    // Linear sampling with an extra token and K < 32: a draw record carries no skip bit; the
+    // residual and select phases test the drawn unit's statistics (1/St = 0 when non-finite)
+    // and the select clears the sequence's mask and statistics.
+    const bool late_skip = MODE == kLinearSample && draws && p.K < 32;
 
     // A row of the stats tiling: row slot rs of sequence b.
     struct Row {
@@ -1275,16 +1284,24 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             // the first rejection is known as soon as every earlier position is decided
             unsigned long long bits = 1ull << pos;
             if (pos < K && __shfl_sync(kFull, accept, 0)) bits |= 1ull << (32 + pos);
+            // Linear sampling with an extra token: the draw's readers (residual tiles, selects)
+            // run after a grid barrier, so the mask update orders nothing here; whether the drawn
+            // unit is non-finite, and the sequence's cleanup, are left to them (late_skip).
             unsigned long long old = 0;
-            if (lane == 0) old = atom_or_acq_rel64(&p.ws_seqmask[b], bits);
+            if (lane == 0)
+                old = late_skip ? atom_or_relaxed64(&p.ws_seqmask[b], bits) : atom_or_acq_rel64(&p.ws_seqmask[b], bits);
             old = __shfl_sync(kFull, old, 0);
             __syncwarp();
             const unsigned long long now = old | bits;
             const int jn = first_rejection(now, K);
-            if (first_rejection(old, K) < 0 && jn >= 0)
-                draw_or_emit(b, jn, jn == pos ? (finite ? 0 : 1) : -1, (!T::kSample && jn == pos) ? Ar[0] : INT_MIN,
-                             pre);
-            if (__popc(static_cast<unsigned>(now)) == K + 1) cleanup_seq(b, jn, true);
+            if (first_rejection(old, K) < 0 && jn >= 0) {
+                if (late_skip)
+                    set_draw(b, b * p.units_per_seq + jn, jn < K, false);
+                else
+                    draw_or_emit(b, jn, jn == pos ? (finite ? 0 : 1) : -1, (!T::kSample && jn == pos) ? Ar[0] : INT_MIN,
+                                 pre);
+            }
+            if (!late_skip && __popc(static_cast<unsigned>(now)) == K + 1) cleanup_seq(b, jn, true);
             return;
         }
         int last = 0;
@@ -1452,7 +1469,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         const int u = static_cast<int>(rec & kRecUnit) - 1;
         const bool pair = (rec & kRecPair) != 0;
-        const bool skip = (rec & kRecSkip) != 0;
+        const bool skip = (rec & kRecSkip) != 0 || (late_skip && !(js.y > 0.f));
         int b, pos;
         if (T::kBonus) {
             b = u;
@@ -1481,9 +1498,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         } else {
             emit_linear(b, pos, token, true, pre);
         }
-        // leave the workspace zeroed
+        // leave the workspace zeroed (late_skip: the sequence's mask and every unit's statistics too)
         unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
         for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0ull;
+        if (late_skip) {
+            for (int i = lane; i < p.units_per_seq; i += 32)
+                p.ws_stats[static_cast<size_t>(b) * p.units_per_seq + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (lane == 0) p.ws_seqmask[b] = 0ull;
+        }
         if (lane == 0) {
             p.ws_stats[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // the other units' by their sequence
             p.ws_draw[e] = 0u;
@@ -1722,8 +1744,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             long long q[kCpt];
 #pragma unroll
             for (int c = 0; c < kCpt; ++c) q[c] = 0;
-            const bool patched = !cskip && cg.w != 0;
-            if (!cskip) {
+            const bool tskip = cskip || (late_skip && !(js.y > 0.f));  // a non-finite unit: its bytes are ignored
+            const bool patched = !tskip && cg.w != 0;
+            if (!tskip) {
                 const int s0 = k * p.Lr;
                 const int s1 = min(p.V, s0 + p.Lr);
                 if (patched) {  // an edge group to fix (rows off the 16-byte grid, tensor ends)
