@@ -102,6 +102,27 @@ __device__ __forceinline__ unsigned long long atom_or_relaxed64(unsigned long lo
     asm volatile("atom.relaxed.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
     return old;
 }
+// floor(u * tot) for a uniform u in [0, 1), exactly, in integer arithmetic: u = m * 2^-s
+// with a 24-bit m, so u * tot is the 88-bit product m * tot shifted right by s.  A NaN or
+// negative u counts as 0, u >= 1 as the largest target, tot - 1.
+__device__ __forceinline__ long long cdf_target(float u, long long tot) {
+    if (!(u > 0.f)) return 0;
+    if (u >= 1.f) return tot - 1;
+    const uint32_t bits = __float_as_uint(u);
+    const uint32_t ex = bits >> 23;  // 1..126 (normal) or 0 (subnormal)
+    const unsigned long long m = ex ? ((bits & 0x7fffffu) | 0x800000u) : (bits & 0x7fffffu);
+    const int sh = ex ? 150 - static_cast<int>(ex) : 149;  // u = m * 2^-sh, sh >= 24
+    const unsigned long long t = static_cast<unsigned long long>(tot);
+    const unsigned long long lo = m * t, hi = __umul64hi(m, t);
+    unsigned long long r;
+    if (sh >= 128)
+        r = 0;
+    else if (sh >= 64)
+        r = hi >> (sh - 64);
+    else
+        r = (hi << (64 - sh)) | (lo >> sh);
+    return static_cast<long long>(r);  // < tot, since u < 1
+}
 // First rejected position of a sequence once it is known from a decided /
 // accepted mask (every earlier position decided and accepted), K when every
 // position 0..K is decided and none rejected, else -1.  K < 32.
@@ -1367,9 +1388,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
         }
         const long long tot = __shfl_sync(kFull, incl, 31);
         if (tot <= 0) return -1;
-        const double ud = (ub >= 0.f) ? static_cast<double>(ub) : 0.0;  // a NaN uniform counts as 0
-        long long target = static_cast<long long>(ud * static_cast<double>(tot));
-        if (target >= tot) target = tot - 1;
+        const long long target = cdf_target(ub, tot);
         // the first chunk whose cumulative sum exceeds the target: its lane, then its place there
         const unsigned bl = __ballot_sync(kFull, incl > target);
         const int ol = __ffs(bl) - 1;  // bl != 0: lane 31 holds tot > target
@@ -1499,8 +1518,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtas) spec_verify_kernel(const P
             emit_linear(b, pos, token, true, pre);
         }
         // leave the workspace zeroed (late_skip: the sequence's mask and every unit's statistics too)
-        unsigned long long *cs = p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt;
-        for (int i = lane; i < p.Sr * kCpt; i += 32) cs[i] = 0ull;
+        uint4 *cs = reinterpret_cast<uint4 *>(p.ws_csum + static_cast<size_t>(e) * p.Sr * kCpt);
+        for (int i = lane; i < p.Sr * kCpt / 2; i += 32) cs[i] = make_uint4(0u, 0u, 0u, 0u);
         if (late_skip) {
             for (int i = lane; i < p.units_per_seq; i += 32)
                 p.ws_stats[static_cast<size_t>(b) * p.units_per_seq + i] = make_float4(0.f, 0.f, 0.f, 0.f);
