@@ -30,7 +30,8 @@
 //     (mc, s), s = sum 2^(fma(l, c, -mc)), c = log2(e) / T, with packed fp32x2
 //     FMA/ADD and one MUFU ex2 per logit; mc is only an offset, re-based on the
 //     lane's max when a tile's terms grow past 2^64.  Greedy lanes keep (max,
-//     lowest argmax).  One warp reduces each whole run (or segment) and
+//     lowest argmax), a tile's best group found first by a max tree.  One warp
+//     reduces each whole run (or segment) and
 //     publishes one partial; the runs depend only on the shape, so results do
 //     not depend on timing.
 //   * Publishing costs no fence: a partial (or the draft token's logit) is
@@ -39,14 +40,17 @@
 //     reads the values, waiting for any that still read zero, decides the
 //     unit, and records it in the sequence's decided/accepted mask; the update
 //     that makes the first rejection known records the sequence's draw in the
-//     sequence's own slot (or emits the sequence).
+//     sequence's own slot (or emits the sequence).  For a linear draw that
+//     update is relaxed: its readers come after a grid barrier.
 //   * The extra token is drawn in three more phases separated by grid-wide
 //     barriers (the launch is cooperative, so every CTA is resident):
 //       C. the B * Sr residual tiles -- slices of at most 4 KB of each drawn
 //          row pair (or row: the tail, a tree node, a row to sample) -- are
 //          split statically over all warps; a tile sums the fp32 weights
 //          max(0, p - q) (or p) of every 16-byte group exactly in int64 fixed
-//          point (units of 2^-52) per 64-group chunk;
+//          point (units of 2^-52) per 64-group chunk, in code specialised at
+//          compile time on the row kind, with the slice's geometry carried by
+//          its stage from the issue;
 //       D. one warp per draw locates the token: a prefix over the chunk sums,
 //          then a rescan of one chunk with bit-identical weights;
 //       E. (sampled tree) one warp per sequence walks the tree.

@@ -140,6 +140,17 @@ def test_greedy_exact_ties_take_lowest_index():
     assert_parity(g, o, d, 0.0)
 
 
+def test_extreme_uniforms_for_the_extra_token():
+    # u_b at the ends of [0, 1): zero, the smallest subnormal, a subnormal, a tiny normal, one half and
+    # the largest float below one; the draw takes the first / last positive weight at the ends
+    us = np.array([0.0, 1.4e-45, 1e-40, 1e-30, 0.5, np.nextafter(np.float32(1), np.float32(0))], dtype=np.float32)
+    for dtype, T in (("bf16", 0.7), ("f32", 1.0)):
+        d = rand_linear(len(us), 3, 5003, dtype, seed=17)
+        d["u_bonus"] = torch.from_numpy(us).cuda()
+        g, o = run_linear(d, T)
+        assert_parity(g, o, d, T)
+
+
 def test_no_extra_token_and_no_probs():
     d = rand_linear(8, 3, 7001, "bf16", seed=6)
     g, o = run_linear(d, 0.9, probs=False, with_bonus=False)
