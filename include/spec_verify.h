@@ -53,8 +53,10 @@
  *     the call returns SPEC_ERR_CUDA.  A launch can fail that way when other
  *     work holds SMs (an MPS client limited to part of the GPU, a green
  *     context); it never deadlocks waiting for a CTA that cannot start.
- *   - The functions keep no mutable global state apart from a per-thread copy
- *     of the last error message; they may be called from several host threads.
+ *   - Apart from a per-thread copy of the last error message, the library keeps
+ *     only caches filled once per device and guarded by locks (a kernel's
+ *     occupancy and shared-memory limit, the static workspace's address); the
+ *     functions may be called from several host threads.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
