@@ -1,6 +1,8 @@
 """The benchmark's extra configurations build their inputs on the CPU too: every
 generator path ends (no search that cannot finish), with the shapes the GPU
 calls expect.  The large configurations are left to the GPU runs."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -34,6 +36,18 @@ def test_every_config_name_has_a_kind_and_a_kernel():
     kinds = set(k for _, _, k in bench.CONFIGS.values())
     assert kinds <= set(bench.CONFIG_KERNELS)
     assert set(bench.CONFIG_PROFILES) <= set(bench.CONFIGS)
+
+
+def test_every_profile_the_bench_reads_exists_and_parses():
+    # the per-launch traffic comes from these summaries; each names the source hash it was taken on
+    import re
+    for name in [bench.HEADLINE_PROFILE, *bench.CONFIG_PROFILES.values()]:
+        text = open(os.path.join(bench.PROFILES, name)).read()
+        h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{16})", text)
+        t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+        assert h and t and int(t.group(1)) > 0, name
+        assert bench.committed_traffic(name, h.group(1)) == int(t.group(1))
+        assert bench.committed_traffic(name, "0" * 16) is None   # another source: no traffic claimed
 
 
 def test_clock_summary_reads_nvidia_smi_lines():
